@@ -1,0 +1,439 @@
+"""Benchmark of the MoE routing / dispatch / combine path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input on one
+GPU: route_topk -> dispatch_layout -> dispatch -> combine -> combine_bwd ->
+dispatch_bwd (the expert GEMMs between them are out of scope: the expert output
+y is a synthetic input and the expert backward is the identity, grecv = gy).
+
+Workload (default): DeepSeek-V3-shaped layer, T=16384, H=7168, E=256 sigmoid
+experts in 8 groups (top-4 groups, top-8 experts, correction bias), 64 virtual
+ranks, bf16 rows.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Under torchrun (N > 1) every rank runs an independent data-parallel replica on
+its own batch (the path shards by token; there is no exchange), and the step
+time is the max over ranks.  Prints one JSON line on rank 0.
+"""
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "dispatch+combine fwd+bwd tokens/s and achieved HBM GB/s (% of GB300 peak)"
+UNIT = "tokens/s"
+DOMINANT = "combine_bwd"
+KERNEL_SOURCES = ("combine_moe_route_05_gb300/csrc/rows.cu", "combine_moe_route_05_gb300/csrc/common.cuh")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "combine_bwd_deepseek_v3.md")
+
+
+# ----------------------------------------------------------------------------
+# byte accounting (algorithmic: every tensor read once and written once)
+
+
+def step_bytes(wl):
+    """Algorithmic HBM bytes of each stage of one step."""
+    T, H, E, K, R = wl.T, wl.H, wl.E, wl.K, wl.R
+    eb = 2 if wl.dtype == "bf16" else 4
+    row, tk = H * eb, T * K
+    return {
+        "route_topk": T * E * 4 + (E * 4 if wl.bias == "normal" else 0) + tk * 8,
+        "dispatch_layout": tk * 4 + 6 * tk * 4 + T * min(K, R) * 4,
+        "dispatch": T * row + tk * row + tk * 4 * 3,
+        "combine": tk * row + T * row + tk * 8,
+        "combine_bwd": T * row + 2 * tk * row + tk * 12,
+        "dispatch_bwd": tk * row + T * row + tk * 4,
+    }
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic_per_launch(workload_name):
+    """DRAM bytes (read + write) per launch of the dominant kernel, from the
+    committed ncu summary, if it was taken on the current kernel source."""
+    if not os.path.exists(TRAFFIC_SUMMARY):
+        return None
+    txt = open(TRAFFIC_SUMMARY).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+workload:\s*(\S+)\s+source:\s*(\w+)", txt)
+    if not m or m.group(2) != workload_name or m.group(3) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas only: a barrier and a max of the step time)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def replica_seed(base_seed, rank, world):
+    return base_seed if world == 1 else synth.shard_seed(base_seed, rank)
+
+
+def reduce_max(value, world, device=None):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle leg (rank 0 only)
+
+
+def oracle_chain(wl, inp):
+    import oracle
+    if wl.score_fn == "softmax":
+        idx, w = oracle.route_softmax(inp["logits"], wl.K, wl.renorm, wl.route_scale)
+    else:
+        idx, w = oracle.route_sigmoid_grouped(inp["logits"], inp["bias"], wl.K, wl.n_groups,
+                                              wl.topk_groups, wl.group_score_topk, wl.renorm,
+                                              wl.route_scale)
+    L = oracle.layout(idx, wl.E, wl.R)
+    oracle.dispatch(inp["x"], L, w)
+    oracle.combine(inp["y"], L, w)
+    gy, _ = oracle.combine_bwd(inp["g"], inp["y"], L, w)
+    oracle.dispatch_bwd(gy, L)
+
+
+def time_oracle(wl, tokens, reps=1):
+    sub = wl.with_tokens(tokens)
+    inp = synth.make_inputs(sub, seed=wl.seed)
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle_chain(sub, inp)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def cpu_baseline(wl, tokens):
+    t = time_oracle(wl, tokens)[0]
+    return {"value": tokens / t, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "first %d of %d tokens of the same workload, whole path (route, layout, "
+                      "dispatch, combine, combine_bwd, dispatch_bwd), single-threaded C++ oracle, "
+                      "%.1f s" % (tokens, wl.T, t)}
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from oracle import build as ob
+    ob.build()
+    tokens = args.ref_tokens
+    sub = wl.with_tokens(tokens)
+    inp = synth.make_inputs(sub, seed=wl.seed)
+    for _ in range(args.warmup):
+        oracle_chain(sub, inp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_chain(sub, inp)
+    el = time.perf_counter() - t0
+    value = tokens * args.steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(wl, extra={"sample_tokens_per_step": tokens}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "first %d of %d tokens per step, whole path, single-threaded "
+                                   "C++ oracle" % (tokens, wl.T)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# GPU leg
+
+
+def workload_config(wl, extra=None):
+    c = {"workload": "%s T=%d H=%d E=%d K=%d R=%d %s%s" % (
+        wl.name, wl.T, wl.H, wl.E, wl.K, wl.R, wl.score_fn,
+        (" groups=%d/%d" % (wl.topk_groups, wl.n_groups)) if wl.n_groups > 1 else ""),
+        "tokens_per_gpu": wl.T, "hidden": wl.H, "experts": wl.E, "top_k": wl.K,
+        "virtual_ranks": wl.R, "row_dtype": wl.dtype, "parallelism": "replicas",
+        "l2": "inputs larger than L2 (x %.0f MB, y %.0f MB per step; L2 129 MB)" % (
+            wl.T * wl.H * 2 / 1e6, wl.T * wl.K * wl.H * 2 / 1e6)}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_gpu(args, wl):
+    import torch
+    import combine_moe_route_05_gb300 as moe
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    seed = replica_seed(wl.seed, rank, world)
+    inp = synth.make_inputs(wl, seed=seed, want=("logits", "bias", "x", "y", "g"))
+
+    def dev_tensor(a):
+        if a is None:
+            return None
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+        return torch.from_numpy(a).to(device)
+
+    T, H, E, K = wl.T, wl.H, wl.E, wl.K
+    r = moe.MoeRouter(E, K, wl.R, T, score_fn=wl.score_fn, num_groups=wl.n_groups,
+                      topk_groups=wl.topk_groups, group_score_topk=wl.group_score_topk,
+                      renorm=wl.renorm, route_scale=wl.route_scale)
+    h = r.h
+    logits, bias, x, y, g = (dev_tensor(inp[k]) for k in ("logits", "bias", "x", "y", "g"))
+    bf = torch.bfloat16
+    idx = torch.empty(T, K, dtype=torch.int32, device=device)
+    w = torch.empty(T, K, dtype=torch.float32, device=device)
+    recv = torch.empty(T * K, H, dtype=bf, device=device)
+    recv_w = torch.empty(T * K, dtype=torch.float32, device=device)
+    out = torch.empty(T, H, dtype=bf, device=device)
+    gy = torch.empty(T * K, H, dtype=bf, device=device)
+    gw = torch.empty(T, K, dtype=torch.float32, device=device)
+    gx = torch.empty(T, H, dtype=bf, device=device)
+    stream = torch.cuda.current_stream()
+    names = ("route_topk", "dispatch_layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd")
+    launches_per_step = 7
+
+    def step(ev=None, logits=logits, bias=bias, x=x, y=y, g=g):
+        if ev is not None:
+            ev[0].record(stream)
+        moe.moe_route_topk(h, logits, bias, idx, w)
+        if ev is not None:
+            ev[1].record(stream)
+        moe.moe_dispatch_layout(h, idx)
+        if ev is not None:
+            ev[2].record(stream)
+        moe.moe_dispatch(h, x, w, recv, recv_w)
+        if ev is not None:
+            ev[3].record(stream)
+        moe.moe_combine(h, y, w, out)
+        if ev is not None:
+            ev[4].record(stream)
+        moe.moe_combine_bwd(h, g, y, w, gy, gw)
+        if ev is not None:
+            ev[5].record(stream)
+        moe.moe_dispatch_bwd(h, gy, gx)
+        if ev is not None:
+            ev[6].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(h) == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(world)
+    el_ms = start.elapsed_time(end)
+    ms_step = reduce_max(el_ms / args.steps, world, device)
+    stage_ms = {n: float(np.mean([e[j].elapsed_time(e[j + 1]) for e in evs])) for j, n in enumerate(names)}
+
+    # end to end through the same public calls, inputs from pinned host memory
+    # and outputs read back every step
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: torch.from_numpy(inp[k].view(np.int16) if inp[k].dtype == np.uint16 else inp[k])
+                   .pin_memory() for k in ("logits", "bias", "x", "y", "g") if inp[k] is not None}
+        dev_in = {"logits": logits, "bias": bias, "x": x, "y": y, "g": g}
+        host_out = {"idx": torch.empty(T, K, dtype=torch.int32).pin_memory(),
+                    "w": torch.empty(T, K, dtype=torch.float32).pin_memory(),
+                    "out": torch.empty(T, H, dtype=torch.int16).pin_memory(),
+                    "gw": torch.empty(T, K, dtype=torch.float32).pin_memory(),
+                    "gx": torch.empty(T, H, dtype=torch.int16).pin_memory()}
+        dev_out = {"idx": idx, "w": w, "out": out.view(torch.int16), "gw": gw, "gx": gx.view(torch.int16)}
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+        def e2e_step():
+            for k, t in host_in.items():
+                d = dev_in[k]
+                (d.view(torch.int16) if d.dtype == bf else d).copy_(t, non_blocking=True)
+            step()
+            for k, t in host_out.items():
+                t.copy_(dev_out[k], non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e2.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = reduce_max(s2.elapsed_time(e2) / args.steps, world, device)
+        e2e = {"value": world * T / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    assert moe.moe_read_device_status(h) == 0
+
+    if rank != 0:
+        return
+    peak, peak_src = read_peaks()
+    sb = step_bytes(wl)
+    total_bytes = sum(sb.values())
+    dom_ms = stage_ms[DOMINANT]
+    achieved = sb[DOMINANT] / (dom_ms / 1e3) / 1e9
+    traffic = measured_traffic_per_launch(wl.name)
+    cpu = None
+    if world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(wl, args.cpu_tokens)
+    line = {
+        "metric": METRIC, "value": world * T / (ms_step / 1e3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(wl),
+        "hbm_gbs": total_bytes / (ms_step / 1e3) / 1e9,
+        "hbm_frac_of_peak": total_bytes / (ms_step / 1e3) / 1e9 / peak,
+        "bytes_per_step": total_bytes,
+        "stage_ms": stage_ms,
+        "stage_gbs": {n: sb[n] / (stage_ms[n] / 1e3) / 1e9 for n in names},
+        "roofline": {"kernel": DOMINANT, "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes": sb[DOMINANT], "peak_source": peak_src},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "kernel_source": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--ref-tokens", type=int, default=256)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_gpu(args, wl)
+
+
+if __name__ == "__main__":
+    main()

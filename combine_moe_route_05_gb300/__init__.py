@@ -1,0 +1,353 @@
+"""Python binding of libmoeroute.so, the C-ABI MoE routing / dispatch / combine
+library for one GB300 (sm_103a).
+
+The functions named ``moe_*`` mirror the C entry points of
+``include/moe_route.h`` one to one: they take torch CUDA tensors (PyTorch only
+provides device memory and streams), check shapes and dtypes, and pass raw
+pointers; every step of the computation runs in the library's CUDA kernels.
+There is no fallback: if the library is missing or fails to load, the import
+of :func:`lib` raises.
+
+``MoeRouter`` is a convenience owner of a handle and its workspace with
+methods that allocate their outputs.
+"""
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = _build.LIB
+
+MOE_OK, MOE_ERR_INVALID, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_STATE = range(5)
+MOE_BF16, MOE_F32 = 0, 1
+MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
+MOE_DEVERR_BAD_EXPERT, MOE_DEVERR_DUP_EXPERT, MOE_DEVERR_NONFINITE, MOE_DEVERR_TIMEOUT = 1, 2, 4, 8
+MOE_MAX_EXPERTS, MOE_MAX_TOPK = 512, 16
+
+EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_handle_create", "moe_handle_destroy",
+           "moe_route_topk", "moe_dispatch_layout", "moe_layout_view", "moe_dispatch",
+           "moe_combine", "moe_combine_bwd", "moe_dispatch_bwd", "moe_scale_rows",
+           "moe_scale_rows_bwd", "moe_read_device_status", "moe_clear_device_status")
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [("num_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("num_ranks", ctypes.c_int32), ("score_fn", ctypes.c_int32),
+                ("num_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
+                ("group_score_topk", ctypes.c_int32), ("renorm", ctypes.c_int32),
+                ("route_scale", ctypes.c_double), ("max_tokens", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class MoeLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "cnt_e", "off_e", "cnt_send_r", "off_send_r", "cnt_recv_r", "off_recv_r", "pos",
+        "recv_token", "recv_k", "send_token", "send_row_of", "recv_send_row", "S")] + [
+        ("num_tokens", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__("%s failed: %s" % (fn, status_string(status)))
+
+
+_lib = None
+
+
+def lib():
+    """The loaded CUDA library (raises if it is not built or cannot load)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libmoeroute.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        st = ctypes.c_int
+        sigs = {
+            "moe_status_string": ([st], ctypes.c_char_p),
+            "moe_workspace_bytes": ([P], sz),
+            "moe_handle_create": ([P, P, sz, P], st),
+            "moe_handle_destroy": ([P], st),
+            "moe_route_topk": ([P, P, P, i32, P, P, P], st),
+            "moe_dispatch_layout": ([P, P, i32, P], st),
+            "moe_layout_view": ([P, P], st),
+            "moe_dispatch": ([P, P, i32, i32, P, P, P, P, P], st),
+            "moe_combine": ([P, P, i32, i32, P, P, P], st),
+            "moe_combine_bwd": ([P, P, P, i32, i32, P, P, P, P], st),
+            "moe_dispatch_bwd": ([P, P, i32, i32, P, P], st),
+            "moe_scale_rows": ([P, P, i32, i32, P, P, P], st),
+            "moe_scale_rows_bwd": ([P, P, P, i32, i32, P, P, P, P], st),
+            "moe_read_device_status": ([P, P], st),
+            "moe_clear_device_status": ([P, P], st),
+        }
+        for name, (args, res) in sigs.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def status_string(s):
+    return lib().moe_status_string(s).decode()
+
+
+def _check(fn, s):
+    if s != MOE_OK:
+        raise MoeError(fn, s)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _row_dtype(t):
+    if t.dtype == torch.bfloat16:
+        return MOE_BF16
+    if t.dtype == torch.float32:
+        return MOE_F32
+    raise TypeError("row tensors must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _req(t, dtype=None, shape=None, name="tensor"):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+
+
+def make_config(num_experts, top_k, num_ranks, max_tokens, score_fn="softmax", num_groups=1,
+                topk_groups=1, group_score_topk=1, renorm=True, route_scale=1.0):
+    fn = {"softmax": MOE_SCORE_SOFTMAX, "sigmoid": MOE_SCORE_SIGMOID}[score_fn] \
+        if isinstance(score_fn, str) else int(score_fn)
+    return MoeConfig(num_experts, top_k, num_ranks, fn, num_groups, topk_groups, group_score_topk,
+                     int(bool(renorm)), float(route_scale), max_tokens, 0)
+
+
+def moe_workspace_bytes(cfg):
+    return lib().moe_workspace_bytes(ctypes.byref(cfg))
+
+
+class Handle:
+    """A moe_handle plus the device workspace it lives in (owned here)."""
+
+    def __init__(self, cfg, device=None):
+        self.cfg = cfg
+        nbytes = moe_workspace_bytes(cfg)
+        if nbytes == 0:
+            raise MoeError("moe_workspace_bytes", MOE_ERR_INVALID)
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        with torch.cuda.device(dev):
+            # 256-byte aligned: the caching allocator returns 512-byte aligned blocks
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+            torch.cuda.current_stream().synchronize()
+            h = ctypes.c_void_p()
+            _check("moe_handle_create",
+                   lib().moe_handle_create(ctypes.byref(cfg), self.workspace.data_ptr(), nbytes,
+                                           ctypes.byref(h)))
+        self.ptr = h
+        self.device = dev
+        self.T = -1
+
+    def close(self):
+        if getattr(self, "ptr", None):
+            lib().moe_handle_destroy(self.ptr)
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def E(self):
+        return self.cfg.num_experts
+
+    @property
+    def K(self):
+        return self.cfg.top_k
+
+    @property
+    def R(self):
+        return self.cfg.num_ranks
+
+
+def moe_route_topk(h, logits, bias, idx, w, stream=None):
+    T = logits.shape[0]
+    _req(logits, torch.float32, (T, h.E), "logits")
+    _req(bias, torch.float32, (h.E,), "bias")
+    _req(idx, torch.int32, (T, h.K), "idx")
+    _req(w, torch.float32, (T, h.K), "w")
+    _check("moe_route_topk", lib().moe_route_topk(h.ptr, _ptr(logits), _ptr(bias), T, _ptr(idx),
+                                                  _ptr(w), _stream(stream)))
+
+
+def moe_dispatch_layout(h, idx, stream=None):
+    T = idx.shape[0]
+    _req(idx, torch.int32, (T, h.K), "idx")
+    _check("moe_dispatch_layout", lib().moe_dispatch_layout(h.ptr, _ptr(idx), T, _stream(stream)))
+    h.T = T
+
+
+def moe_layout_view(h):
+    v = MoeLayout()
+    _check("moe_layout_view", lib().moe_layout_view(h.ptr, ctypes.byref(v)))
+    return v
+
+
+def moe_dispatch(h, x, w, recv, recv_w, send=None, stream=None):
+    T, H = x.shape
+    _req(x, None, (h.T, H), "x")
+    _req(recv, x.dtype, (h.T * h.K, H), "recv")
+    _req(w, torch.float32, (h.T, h.K), "w")
+    _req(recv_w, torch.float32, (h.T * h.K,), "recv_w")
+    _req(send, x.dtype, (h.T * min(h.K, h.R), H), "send")
+    _check("moe_dispatch", lib().moe_dispatch(h.ptr, _ptr(x), H, _row_dtype(x), _ptr(w), _ptr(recv),
+                                              _ptr(recv_w), _ptr(send), _stream(stream)))
+
+
+def moe_combine(h, y, w, out, stream=None):
+    H = y.shape[1]
+    _req(y, None, (h.T * h.K, H), "y")
+    _req(w, torch.float32, (h.T, h.K), "w")
+    _req(out, y.dtype, (h.T, H), "out")
+    _check("moe_combine", lib().moe_combine(h.ptr, _ptr(y), H, _row_dtype(y), _ptr(w), _ptr(out),
+                                            _stream(stream)))
+
+
+def moe_combine_bwd(h, g, y, w, gy, gw, stream=None):
+    H = g.shape[1]
+    _req(g, None, (h.T, H), "g")
+    _req(y, g.dtype, (h.T * h.K, H), "y")
+    _req(w, torch.float32, (h.T, h.K), "w")
+    _req(gy, g.dtype, (h.T * h.K, H), "gy")
+    _req(gw, torch.float32, (h.T, h.K), "gw")
+    _check("moe_combine_bwd", lib().moe_combine_bwd(h.ptr, _ptr(g), _ptr(y), H, _row_dtype(g), _ptr(w),
+                                                    _ptr(gy), _ptr(gw), _stream(stream)))
+
+
+def moe_dispatch_bwd(h, grecv, gx, stream=None):
+    H = grecv.shape[1]
+    _req(grecv, None, (h.T * h.K, H), "grecv")
+    _req(gx, grecv.dtype, (h.T, H), "gx")
+    _check("moe_dispatch_bwd", lib().moe_dispatch_bwd(h.ptr, _ptr(grecv), H, _row_dtype(grecv),
+                                                      _ptr(gx), _stream(stream)))
+
+
+def moe_scale_rows(h, hrows, recv_w, hs, stream=None):
+    I = hrows.shape[1]
+    _req(hrows, None, (h.T * h.K, I), "h")
+    _req(recv_w, torch.float32, (h.T * h.K,), "recv_w")
+    _req(hs, hrows.dtype, (h.T * h.K, I), "hs")
+    _check("moe_scale_rows", lib().moe_scale_rows(h.ptr, _ptr(hrows), I, _row_dtype(hrows),
+                                                  _ptr(recv_w), _ptr(hs), _stream(stream)))
+
+
+def moe_scale_rows_bwd(h, ghs, hrows, recv_w, gh, gw, stream=None):
+    I = hrows.shape[1]
+    _req(ghs, None, (h.T * h.K, I), "ghs")
+    _req(hrows, ghs.dtype, (h.T * h.K, I), "h")
+    _req(recv_w, torch.float32, (h.T * h.K,), "recv_w")
+    _req(gh, ghs.dtype, (h.T * h.K, I), "gh")
+    _req(gw, torch.float32, (h.T, h.K), "gw")
+    _check("moe_scale_rows_bwd", lib().moe_scale_rows_bwd(h.ptr, _ptr(ghs), _ptr(hrows), I,
+                                                          _row_dtype(ghs), _ptr(recv_w), _ptr(gh),
+                                                          _ptr(gw), _stream(stream)))
+
+
+def moe_read_device_status(h):
+    flags = ctypes.c_uint32(0)
+    _check("moe_read_device_status", lib().moe_read_device_status(h.ptr, ctypes.byref(flags)))
+    return flags.value
+
+
+def moe_clear_device_status(h, stream=None):
+    _check("moe_clear_device_status", lib().moe_clear_device_status(h.ptr, _stream(stream)))
+
+
+def layout_tensors(h):
+    """Torch views (int32, on the handle's device) of the current layout arrays."""
+    v = moe_layout_view(h)
+    T, K, E, R = h.T, h.K, h.E, h.R
+    sizes = {"cnt_e": E, "off_e": E + 1, "cnt_send_r": R, "off_send_r": R + 1, "cnt_recv_r": R,
+             "off_recv_r": R + 1, "pos": T * K, "recv_token": T * K, "recv_k": T * K,
+             "send_token": T * min(K, R), "send_row_of": T * K, "recv_send_row": T * K, "S": 1}
+    out = {}
+    ws = h.workspace
+    base = ws.data_ptr()
+    for name, n in sizes.items():
+        off = getattr(v, name) - base
+        out[name] = ws[off:off + 4 * n].view(torch.int32)
+    out["pos"] = out["pos"].view(T, K)
+    out["send_row_of"] = out["send_row_of"].view(T, K)
+    return out
+
+
+class MoeRouter:
+    """Owns a handle; methods allocate their outputs and call the moe_* bindings."""
+
+    def __init__(self, num_experts, top_k, num_ranks, max_tokens, **kw):
+        self.cfg = make_config(num_experts, top_k, num_ranks, max_tokens, **kw)
+        self.h = Handle(self.cfg)
+
+    def route(self, logits, bias=None, stream=None):
+        T = logits.shape[0]
+        idx = torch.empty(T, self.h.K, dtype=torch.int32, device=logits.device)
+        w = torch.empty(T, self.h.K, dtype=torch.float32, device=logits.device)
+        moe_route_topk(self.h, logits, bias, idx, w, stream)
+        return idx, w
+
+    def layout(self, idx, stream=None):
+        moe_dispatch_layout(self.h, idx, stream)
+        return layout_tensors(self.h)
+
+    def dispatch(self, x, w=None, with_send=False, stream=None):
+        T, H = x.shape
+        recv = torch.empty(T * self.h.K, H, dtype=x.dtype, device=x.device)
+        recv_w = torch.empty(T * self.h.K, dtype=torch.float32, device=x.device) if w is not None else None
+        send = torch.empty(T * min(self.h.K, self.h.R), H, dtype=x.dtype, device=x.device) if with_send else None
+        moe_dispatch(self.h, x, w, recv, recv_w, send, stream)
+        return recv, recv_w, send
+
+    def combine(self, y, w=None, stream=None):
+        out = torch.empty(self.h.T, y.shape[1], dtype=y.dtype, device=y.device)
+        moe_combine(self.h, y, w, out, stream)
+        return out
+
+    def combine_bwd(self, g, y=None, w=None, stream=None):
+        gy = torch.empty(self.h.T * self.h.K, g.shape[1], dtype=g.dtype, device=g.device)
+        gw = torch.empty(self.h.T, self.h.K, dtype=torch.float32, device=g.device) if w is not None else None
+        moe_combine_bwd(self.h, g, y, w, gy, gw, stream)
+        return gy, gw
+
+    def dispatch_bwd(self, grecv, stream=None):
+        gx = torch.empty(self.h.T, grecv.shape[1], dtype=grecv.dtype, device=grecv.device)
+        moe_dispatch_bwd(self.h, grecv, gx, stream)
+        return gx
+
+    def scale_rows(self, hrows, recv_w, stream=None):
+        hs = torch.empty_like(hrows)
+        moe_scale_rows(self.h, hrows, recv_w, hs, stream)
+        return hs
+
+    def scale_rows_bwd(self, ghs, hrows, recv_w, stream=None):
+        gh = torch.empty_like(hrows)
+        gw = torch.empty(self.h.T, self.h.K, dtype=torch.float32, device=hrows.device)
+        moe_scale_rows_bwd(self.h, ghs, hrows, recv_w, gh, gw, stream)
+        return gh, gw

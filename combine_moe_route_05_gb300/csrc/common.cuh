@@ -1,0 +1,171 @@
+// Shared device helpers of the MoE routing library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_route.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// status word
+
+__device__ __forceinline__ void raise_flag(uint32_t* flags, uint32_t bit) {
+  if (flags) atomicOr(flags, bit);
+}
+
+// ---------------------------------------------------------------------------
+// 16-byte vector rows
+
+struct alignas(16) Vec16 {
+  uint32_t u[4];
+};
+
+// Streaming 16-byte load of data read once: non-coherent path, no L1
+// allocation.
+__device__ __forceinline__ Vec16 ld_stream(const void* p) {
+  Vec16 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.u[0]), "=r"(v.u[1]), "=r"(v.u[2]), "=r"(v.u[3])
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_vec(void* p, const Vec16& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.u[0]), "r"(v.u[1]),
+               "r"(v.u[2]), "r"(v.u[3])
+               : "memory");
+}
+
+// Element access of a 16-byte vector as fp32 (bf16: 8 elements, f32: 4).
+template <typename Elt>
+struct VecTraits;
+
+template <>
+struct VecTraits<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void to_f32(const Vec16& v, float* f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(v.u[i] << 16);
+      f[2 * i + 1] = __uint_as_float(v.u[i] & 0xffff0000u);
+    }
+  }
+  // round-to-nearest-even of each fp32 value
+  __device__ __forceinline__ static Vec16 from_f32(const float* f) {
+    Vec16 v;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      v.u[i] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    return v;
+  }
+};
+
+template <>
+struct VecTraits<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void to_f32(const Vec16& v, float* f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = __uint_as_float(v.u[i]);
+  }
+  __device__ __forceinline__ static Vec16 from_f32(const float* f) {
+    Vec16 v;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v.u[i] = __float_as_uint(f[i]);
+    return v;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// shared-memory addresses, mbarriers and bulk (TMA) copies
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait on an mbarrier phase: gives up after `max_tries` polls (each
+// poll itself suspends for a hardware-chosen time) and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint32_t max_tries) {
+  for (uint32_t i = 0; i < max_tries; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// Global -> shared bulk copy completing on an mbarrier (bytes % 16 == 0, both
+// addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst_smem)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Shared -> global bulk copy tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_addr(src_smem)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// warp helpers
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+}  // namespace moe

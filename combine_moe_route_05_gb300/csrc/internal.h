@@ -1,0 +1,59 @@
+// Host-side internals shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_route.h"
+
+// Tokens per layout tile (one 1024-thread block, one token per thread).
+#define MOE_LAYOUT_TILE 1024
+
+struct moe_handle {
+  moe_config cfg;
+  int device;
+  int num_sms;
+  int T;  // tokens of the current layout, -1 before the first
+  int max_tiles;
+  uint32_t* flags;   // device status word (MOE_DEVERR_* bits)
+  uint32_t* ticket;  // arrival counter of the layout's last-block scan
+  int32_t* cnt_e;
+  int32_t* off_e;
+  int32_t* cnt_send_r;
+  int32_t* off_send_r;
+  int32_t* cnt_recv_r;
+  int32_t* off_recv_r;
+  int32_t* S;
+  int32_t* pos;
+  int32_t* recv_token;
+  int32_t* recv_k;
+  int32_t* send_token;
+  int32_t* send_row_of;
+  int32_t* recv_send_row;
+  int32_t* tile_hist;  // [(E + R) columns][max_tiles], exclusive tile bases after the scan
+};
+
+namespace moe {
+
+cudaError_t launch_route_topk(const moe_handle* h, const float* logits, const float* bias, int T,
+                              int32_t* idx, float* w, cudaStream_t s);
+
+cudaError_t launch_layout(const moe_handle* h, const int32_t* idx, int T, cudaStream_t s);
+
+cudaError_t launch_dispatch(const moe_handle* h, const void* x, int64_t row_bytes, const float* w,
+                            void* recv, float* recv_w, void* send, cudaStream_t s);
+
+cudaError_t launch_combine(const moe_handle* h, const void* y, int H, int dtype, const float* w,
+                           void* out, cudaStream_t s);
+
+cudaError_t launch_combine_bwd(const moe_handle* h, const void* g, const void* y, int H, int dtype,
+                               const float* w, void* gy, float* gw, cudaStream_t s);
+
+cudaError_t launch_scale_rows(const moe_handle* h, const void* hrows, int I, int dtype,
+                              const float* recv_w, void* hs, cudaStream_t s);
+
+cudaError_t launch_scale_rows_bwd(const moe_handle* h, const void* ghs, const void* hrows, int I,
+                                  int dtype, const float* recv_w, void* gh, float* gw,
+                                  cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,522 @@
+// Row movement kernels of the MoE path (sm_103a): dispatch, combine, their
+// backward passes, and the router-score absorption scaling.
+//
+// dispatch: token-major.  Each token row of x is read from HBM once with a
+//   bulk (TMA) copy into a shared-memory slot and written from there to its K
+//   expert-grouped receive rows (and its deduplicated send rows) with bulk
+//   stores, so a row is never expanded to [T*K,H] by a separate pass
+//   (DeepSpeed "Add an opt-in DeepEP transport ...", "Why": tokens are taken
+//   before top-k expansion and replicated by the dispatch itself).
+// combine / dispatch backward: token-major gather of the K rows of a token
+//   with 16-byte streaming loads, fp32 accumulation in k order (fused
+//   multiply-add for the weighted sum), one rounding to the row dtype.
+// combine backward: reads g[t] once and each y row once; writes the K
+//   gradient rows and reduces the K router-score gradients <g_t, y[pos]> in
+//   a fixed order (deterministic).
+#include <climits>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---------------------------------------------------------------------------
+// dispatch: bulk copies through shared memory
+
+constexpr int kSlots = 4;          // shared-memory row slots per block
+constexpr int kAhead = 2;          // loads issued ahead of the one consumed
+constexpr uint32_t kChunkMax = 16384;  // bytes per bulk copy
+constexpr uint32_t kWaitPolls = 1u << 22;
+static_assert(kAhead < kSlots, "slots must outnumber loads in flight");
+
+struct DispatchArgs {
+  const uint8_t* x;
+  int64_t row_bytes;
+  int T, K;
+  uint32_t chunk;
+  int nchunk;
+  const int32_t* pos;
+  const float* w;
+  const int32_t* send_row_of;
+  uint8_t* recv;
+  float* recv_w;
+  uint8_t* send;
+  uint32_t* flags;
+};
+
+__global__ void __launch_bounds__(32) dispatch_bulk_kernel(DispatchArgs a) {
+  extern __shared__ __align__(128) uint8_t dsm[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(dsm);
+  uint8_t* slots = dsm + 128;
+  const int lane = threadIdx.x;
+  const long long units = static_cast<long long>(a.T) * a.nchunk;
+  const long long first = blockIdx.x, stride = gridDim.x;
+  const long long n_my = first < units ? (units - first + stride - 1) / stride : 0;
+  if (lane == 0) {
+    for (int s = 0; s < kSlots; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  long long issued = 0;  // lane 0: units whose load has been issued
+  auto issue = [&](long long i) {
+    const long long u = first + i * stride;
+    const long long t = u / a.nchunk;
+    const uint32_t off = static_cast<uint32_t>(u % a.nchunk) * a.chunk;
+    const uint32_t bytes = static_cast<uint32_t>(
+        a.row_bytes - off < static_cast<int64_t>(a.chunk) ? a.row_bytes - off : a.chunk);
+    uint64_t* b = &bar[i % kSlots];
+    mbar_arrive_expect_tx(b, bytes);
+    bulk_load(slots + (i % kSlots) * a.chunk, a.x + t * a.row_bytes + off, bytes, b);
+  };
+  if (lane == 0)
+    for (; issued < kAhead && issued < n_my; ++issued) issue(issued);
+
+  bool ok = true;
+  long long i = 0;
+  for (; i < n_my; ++i) {
+    const long long u = first + i * stride;
+    const long long t = u / a.nchunk;
+    const int c = static_cast<int>(u % a.nchunk);
+    const uint32_t off = static_cast<uint32_t>(c) * a.chunk;
+    const uint32_t bytes = static_cast<uint32_t>(
+        a.row_bytes - off < static_cast<int64_t>(a.chunk) ? a.row_bytes - off : a.chunk);
+
+    int p = -1, srow = -1;
+    if (lane < a.K) {
+      p = __ldg(a.pos + t * a.K + lane);
+      if (a.send) srow = __ldg(a.send_row_of + t * a.K + lane);
+      if (c == 0 && a.recv_w && p >= 0) a.recv_w[p] = __ldg(a.w + t * a.K + lane);
+    }
+    // a send row is written once, by the lowest k that maps to it
+    const uint32_t same = __match_any_sync(kFull, srow);
+    const bool send_first = a.send && lane < a.K && srow >= 0 && (__ffs(same) - 1) == lane;
+    const uint32_t send_mask = __ballot_sync(kFull, send_first);
+
+    if (lane == 0 && !mbar_wait_bounded(&bar[i % kSlots], static_cast<uint32_t>((i / kSlots) & 1),
+                                        kWaitPolls)) {
+      raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
+      ok = false;
+    }
+    ok = __shfl_sync(kFull, ok, 0);
+    if (!ok) break;
+
+    const uint8_t* src = slots + (i % kSlots) * a.chunk;
+    for (int k = 0; k < a.K; ++k) {
+      const int pk = __shfl_sync(kFull, p, k);
+      const int sk = __shfl_sync(kFull, srow, k);
+      if (lane == 0) {
+        if (pk >= 0) bulk_store(a.recv + static_cast<int64_t>(pk) * a.row_bytes + off, src, bytes);
+        if ((send_mask >> k) & 1u)
+          bulk_store(a.send + static_cast<int64_t>(sk) * a.row_bytes + off, src, bytes);
+      }
+    }
+    if (lane == 0) {
+      bulk_commit();
+      if (issued < n_my) {
+        // the slot of unit `issued` was last read by unit issued - kSlots,
+        // whose stores are among the groups older than the newest
+        // kSlots - kAhead
+        bulk_wait_read<kSlots - kAhead>();
+        issue(issued);
+        ++issued;
+      }
+    }
+  }
+  if (lane == 0) {
+    if (!ok) {
+      // drain the loads still in flight before shared memory goes away
+      for (long long q = i + 1; q < issued; ++q)
+        mbar_wait_bounded(&bar[q % kSlots], static_cast<uint32_t>((q / kSlots) & 1), kWaitPolls);
+    }
+    bulk_wait_all();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// combine / dispatch backward: out[t] = round(sum_k w_k * y[pos[t,k]])
+
+constexpr int kRowThreads = 256;
+
+template <typename Elt>
+struct RowArgs {
+  const uint8_t* y;   // [rows, H] gathered rows
+  const uint8_t* g;   // [T, H] (combine backward)
+  const float* w;     // [T, K] or NULL
+  const int32_t* pos; // [T, K]
+  uint8_t* out;       // [T, H] (combine) or [rows, H] (combine backward)
+  float* gw;          // [T, K] or NULL
+  int64_t row_bytes;
+  int nvec;           // 16-byte vectors per row
+  int T, K;
+};
+
+template <int KMAX>
+__device__ __forceinline__ void load_entries(const int32_t* pos, const float* w, int t, int K,
+                                             int (&p)[KMAX], float (&wk)[KMAX]) {
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    p[k] = -1;
+    wk[k] = 1.0f;
+    if (k < K) {
+      p[k] = __ldg(pos + static_cast<size_t>(t) * K + k);
+      if (w) wk[k] = __ldg(w + static_cast<size_t>(t) * K + k);
+    }
+  }
+}
+
+template <typename Elt, int KMAX, bool WEIGHTED>
+__global__ void __launch_bounds__(kRowThreads) combine_kernel(RowArgs<Elt> a) {
+  using VT = VecTraits<Elt>;
+  constexpr int N = VT::N;
+  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+    int p[KMAX];
+    float wk[KMAX];
+    load_entries<KMAX>(a.pos, WEIGHTED ? a.w : nullptr, t, a.K, p, wk);
+    uint8_t* orow = a.out + static_cast<int64_t>(t) * a.row_bytes;
+    for (int v = threadIdx.x; v < a.nvec; v += kRowThreads) {
+      Vec16 in[KMAX];
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if (p[k] >= 0) in[k] = ld_stream(a.y + static_cast<int64_t>(p[k]) * a.row_bytes + v * 16);
+      float acc[N];
+#pragma unroll
+      for (int i = 0; i < N; ++i) acc[i] = 0.0f;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        if (p[k] < 0) continue;
+        float f[N];
+        VT::to_f32(in[k], f);
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+          acc[i] = WEIGHTED ? __fmaf_rn(wk[k], f[i], acc[i]) : __fadd_rn(acc[i], f[i]);
+      }
+      st_vec(orow + v * 16, VT::from_f32(acc));
+    }
+  }
+}
+
+// combine backward: gy[pos[t,k]] = round(w_k * g[t]) (or g[t]), and
+// gw[t,k] = <g[t], y[pos[t,k]]> reduced over the block in a fixed order.
+template <typename Elt, int KMAX, bool WEIGHTED, bool DOT>
+__global__ void __launch_bounds__(kRowThreads) combine_bwd_kernel(RowArgs<Elt> a) {
+  using VT = VecTraits<Elt>;
+  constexpr int N = VT::N;
+  constexpr int kW = kRowThreads / 32;
+  __shared__ float red[2][kW][KMAX];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int it = 0;
+  for (int t = blockIdx.x; t < a.T; t += gridDim.x, ++it) {
+    int p[KMAX];
+    float wk[KMAX];
+    load_entries<KMAX>(a.pos, WEIGHTED ? a.w : nullptr, t, a.K, p, wk);
+    float dot[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) dot[k] = 0.0f;
+    const uint8_t* grow = a.g + static_cast<int64_t>(t) * a.row_bytes;
+    for (int v = threadIdx.x; v < a.nvec; v += kRowThreads) {
+      const Vec16 gv = ld_stream(grow + v * 16);
+      Vec16 yv[KMAX];
+      if (DOT) {
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+          if (p[k] >= 0) yv[k] = ld_stream(a.y + static_cast<int64_t>(p[k]) * a.row_bytes + v * 16);
+      }
+      float gf[N];
+      VT::to_f32(gv, gf);
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        if (p[k] < 0) continue;
+        uint8_t* dst = a.out + static_cast<int64_t>(p[k]) * a.row_bytes + v * 16;
+        if (WEIGHTED) {
+          float o[N];
+#pragma unroll
+          for (int i = 0; i < N; ++i) o[i] = __fmul_rn(wk[k], gf[i]);
+          st_vec(dst, VT::from_f32(o));
+        } else {
+          st_vec(dst, gv);
+        }
+        if (DOT) {
+          float yf[N];
+          VT::to_f32(yv[k], yf);
+#pragma unroll
+          for (int i = 0; i < N; ++i) dot[k] = __fmaf_rn(gf[i], yf[i], dot[k]);
+        }
+      }
+    }
+    if (DOT) {
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dot[k] += __shfl_xor_sync(kFull, dot[k], off);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) red[it & 1][warp][k] = dot[k];
+      }
+      __syncthreads();
+      if (threadIdx.x < a.K) {
+        float s = 0.0f;
+#pragma unroll
+        for (int wi = 0; wi < kW; ++wi) s += red[it & 1][wi][threadIdx.x];
+        int pk = __ldg(a.pos + static_cast<size_t>(t) * a.K + threadIdx.x);
+        a.gw[static_cast<size_t>(t) * a.K + threadIdx.x] = pk >= 0 ? s : 0.0f;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// absorption: hs[r] = round(h[r] * recv_w[r]) over the valid receive rows
+
+template <typename Elt>
+__global__ void __launch_bounds__(kRowThreads) scale_rows_kernel(const uint8_t* h, const float* rw,
+                                                                 uint8_t* hs, int64_t row_bytes,
+                                                                 int nvec, const int32_t* nrows_dev) {
+  using VT = VecTraits<Elt>;
+  constexpr int N = VT::N;
+  const int64_t nrows = *nrows_dev;
+  const int64_t total = nrows * nvec;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kRowThreads + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * kRowThreads) {
+    const int64_t r = i / nvec;
+    const int v = static_cast<int>(i - r * nvec);
+    const float s = __ldg(rw + r);
+    float f[N];
+    VT::to_f32(ld_stream(h + r * row_bytes + v * 16), f);
+#pragma unroll
+    for (int j = 0; j < N; ++j) f[j] = __fmul_rn(f[j], s);
+    st_vec(hs + r * row_bytes + v * 16, VT::from_f32(f));
+  }
+}
+
+// absorption backward, one warp per entry (t,k):
+//   gh[p] = round(recv_w[p] * ghs[p]),  gw[t,k] = <ghs[p], h[p]>,  p = pos[t,k]
+template <typename Elt>
+__global__ void __launch_bounds__(kRowThreads) scale_rows_bwd_kernel(
+    const uint8_t* ghs, const uint8_t* h, const float* rw, uint8_t* gh, float* gw,
+    const int32_t* pos, int64_t entries, int64_t row_bytes, int nvec) {
+  using VT = VecTraits<Elt>;
+  constexpr int N = VT::N;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kRowThreads / 32);
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * (kRowThreads / 32) + (threadIdx.x >> 5);
+       e < entries; e += nwarps) {
+    const int p = __ldg(pos + e);
+    float dot = 0.0f;
+    if (p >= 0) {
+      const float s = __ldg(rw + p);
+      const uint8_t* grow = ghs + static_cast<int64_t>(p) * row_bytes;
+      const uint8_t* hrow = h + static_cast<int64_t>(p) * row_bytes;
+      uint8_t* orow = gh + static_cast<int64_t>(p) * row_bytes;
+      for (int v = lane; v < nvec; v += 32) {
+        float gf[N], hf[N], o[N];
+        VT::to_f32(ld_stream(grow + v * 16), gf);
+        VT::to_f32(ld_stream(hrow + v * 16), hf);
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+          o[j] = __fmul_rn(s, gf[j]);
+          dot = __fmaf_rn(gf[j], hf[j], dot);
+        }
+        st_vec(orow + v * 16, VT::from_f32(o));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(kFull, dot, off);
+    }
+    if (lane == 0) gw[e] = dot;
+  }
+}
+
+// Resident blocks per SM of `kernel`, computed once per (kernel, smem) pair.
+int blocks_per_sm(const void* kernel, int threads, size_t smem) {
+  struct Entry {
+    const void* k;
+    int threads;
+    size_t smem;
+    int per_sm;
+  };
+  static Entry cache[32];
+  static int used = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].k == kernel && cache[i].threads == threads && cache[i].smem == smem)
+      return cache[i].per_sm;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess)
+    per_sm = 1;
+  if (per_sm < 1) per_sm = 1;
+  if (used < 32) cache[used++] = Entry{kernel, threads, smem, per_sm};
+  return per_sm;
+}
+
+// Persistent grid: every resident block slot of the GPU, or fewer if there is
+// less work.
+int grid_for(const void* kernel, int threads, size_t smem, int num_sms, long long work_items) {
+  long long g = static_cast<long long>(blocks_per_sm(kernel, threads, smem)) * num_sms;
+  if (work_items < g) g = work_items;
+  return static_cast<int>(g < 1 ? 1 : g);
+}
+
+template <typename Elt, int KMAX>
+cudaError_t launch_combine_t(const moe_handle* h, const void* y, int H, const float* w, void* out,
+                             cudaStream_t s) {
+  RowArgs<Elt> a{};
+  a.y = static_cast<const uint8_t*>(y);
+  a.w = w;
+  a.pos = h->pos;
+  a.out = static_cast<uint8_t*>(out);
+  a.row_bytes = static_cast<int64_t>(H) * sizeof(Elt);
+  a.nvec = static_cast<int>(a.row_bytes / 16);
+  a.T = h->T;
+  a.K = h->cfg.top_k;
+  if (a.T == 0) return cudaSuccess;
+  if (w) {
+    auto k = combine_kernel<Elt, KMAX, true>;
+    k<<<grid_for(reinterpret_cast<const void*>(k), kRowThreads, 0, h->num_sms, a.T), kRowThreads, 0, s>>>(a);
+  } else {
+    auto k = combine_kernel<Elt, KMAX, false>;
+    k<<<grid_for(reinterpret_cast<const void*>(k), kRowThreads, 0, h->num_sms, a.T), kRowThreads, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+template <typename Elt, int KMAX>
+cudaError_t launch_combine_bwd_t(const moe_handle* h, const void* g, const void* y, int H,
+                                 const float* w, void* gy, float* gw, cudaStream_t s) {
+  RowArgs<Elt> a{};
+  a.y = static_cast<const uint8_t*>(y);
+  a.g = static_cast<const uint8_t*>(g);
+  a.w = w;
+  a.pos = h->pos;
+  a.out = static_cast<uint8_t*>(gy);
+  a.gw = gw;
+  a.row_bytes = static_cast<int64_t>(H) * sizeof(Elt);
+  a.nvec = static_cast<int>(a.row_bytes / 16);
+  a.T = h->T;
+  a.K = h->cfg.top_k;
+  if (a.T == 0) return cudaSuccess;
+  const void* kp;
+  if (w && gw) {
+    auto k = combine_bwd_kernel<Elt, KMAX, true, true>;
+    kp = reinterpret_cast<const void*>(k);
+    k<<<grid_for(kp, kRowThreads, 0, h->num_sms, a.T), kRowThreads, 0, s>>>(a);
+  } else if (w) {
+    auto k = combine_bwd_kernel<Elt, KMAX, true, false>;
+    kp = reinterpret_cast<const void*>(k);
+    k<<<grid_for(kp, kRowThreads, 0, h->num_sms, a.T), kRowThreads, 0, s>>>(a);
+  } else {
+    auto k = combine_bwd_kernel<Elt, KMAX, false, false>;
+    kp = reinterpret_cast<const void*>(k);
+    k<<<grid_for(kp, kRowThreads, 0, h->num_sms, a.T), kRowThreads, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t dispatch_smem_bytes(int64_t row_bytes) {
+  const uint32_t chunk = row_bytes < kChunkMax ? static_cast<uint32_t>(row_bytes) : kChunkMax;
+  return 128 + static_cast<size_t>(kSlots) * chunk;
+}
+
+cudaError_t prepare_dispatch_kernel() {
+  return cudaFuncSetAttribute(dispatch_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(128 + kSlots * kChunkMax));
+}
+
+cudaError_t launch_dispatch(const moe_handle* h, const void* x, int64_t row_bytes, const float* w,
+                            void* recv, float* recv_w, void* send, cudaStream_t s) {
+  DispatchArgs a{};
+  a.x = static_cast<const uint8_t*>(x);
+  a.row_bytes = row_bytes;
+  a.T = h->T;
+  a.K = h->cfg.top_k;
+  a.chunk = row_bytes < kChunkMax ? static_cast<uint32_t>(row_bytes) : kChunkMax;
+  a.nchunk = static_cast<int>((row_bytes + a.chunk - 1) / a.chunk);
+  a.pos = h->pos;
+  a.w = w;
+  a.send_row_of = h->send_row_of;
+  a.recv = static_cast<uint8_t*>(recv);
+  a.recv_w = recv_w;
+  a.send = static_cast<uint8_t*>(send);
+  a.flags = h->flags;
+  if (a.T == 0) return cudaSuccess;
+  const size_t smem = dispatch_smem_bytes(row_bytes);
+  const int grid = grid_for(reinterpret_cast<const void*>(dispatch_bulk_kernel), 32, smem,
+                            h->num_sms, static_cast<long long>(a.T) * a.nchunk);
+  dispatch_bulk_kernel<<<grid, 32, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const moe_handle* h, const void* y, int H, int dtype, const float* w,
+                           void* out, cudaStream_t s) {
+  const bool k8 = h->cfg.top_k <= 8;
+  if (dtype == MOE_BF16)
+    return k8 ? launch_combine_t<__nv_bfloat16, 8>(h, y, H, w, out, s)
+              : launch_combine_t<__nv_bfloat16, 16>(h, y, H, w, out, s);
+  return k8 ? launch_combine_t<float, 8>(h, y, H, w, out, s)
+            : launch_combine_t<float, 16>(h, y, H, w, out, s);
+}
+
+cudaError_t launch_combine_bwd(const moe_handle* h, const void* g, const void* y, int H, int dtype,
+                               const float* w, void* gy, float* gw, cudaStream_t s) {
+  const bool k8 = h->cfg.top_k <= 8;
+  if (dtype == MOE_BF16)
+    return k8 ? launch_combine_bwd_t<__nv_bfloat16, 8>(h, g, y, H, w, gy, gw, s)
+              : launch_combine_bwd_t<__nv_bfloat16, 16>(h, g, y, H, w, gy, gw, s);
+  return k8 ? launch_combine_bwd_t<float, 8>(h, g, y, H, w, gy, gw, s)
+            : launch_combine_bwd_t<float, 16>(h, g, y, H, w, gy, gw, s);
+}
+
+cudaError_t launch_scale_rows(const moe_handle* h, const void* hrows, int I, int dtype,
+                              const float* recv_w, void* hs, cudaStream_t s) {
+  const int64_t row_bytes = static_cast<int64_t>(I) * (dtype == MOE_BF16 ? 2 : 4);
+  const int nvec = static_cast<int>(row_bytes / 16);
+  if (h->T == 0) return cudaSuccess;
+  const long long items = static_cast<long long>(h->T) * h->cfg.top_k * nvec;
+  const long long blocks = (items + kRowThreads - 1) / kRowThreads;
+  const int32_t* nrows = h->off_e + h->cfg.num_experts;
+  if (dtype == MOE_BF16) {
+    auto k = scale_rows_kernel<__nv_bfloat16>;
+    const int grid = grid_for(reinterpret_cast<const void*>(k), kRowThreads, 0, h->num_sms, blocks);
+    k<<<grid, kRowThreads, 0, s>>>(static_cast<const uint8_t*>(hrows), recv_w,
+                                   static_cast<uint8_t*>(hs), row_bytes, nvec, nrows);
+  } else {
+    auto k = scale_rows_kernel<float>;
+    const int grid = grid_for(reinterpret_cast<const void*>(k), kRowThreads, 0, h->num_sms, blocks);
+    k<<<grid, kRowThreads, 0, s>>>(static_cast<const uint8_t*>(hrows), recv_w,
+                                   static_cast<uint8_t*>(hs), row_bytes, nvec, nrows);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_rows_bwd(const moe_handle* h, const void* ghs, const void* hrows, int I,
+                                  int dtype, const float* recv_w, void* gh, float* gw,
+                                  cudaStream_t s) {
+  const int64_t row_bytes = static_cast<int64_t>(I) * (dtype == MOE_BF16 ? 2 : 4);
+  const int nvec = static_cast<int>(row_bytes / 16);
+  const int64_t entries = static_cast<int64_t>(h->T) * h->cfg.top_k;
+  if (entries == 0) return cudaSuccess;
+  const long long blocks = (entries + kRowThreads / 32 - 1) / (kRowThreads / 32);
+  if (dtype == MOE_BF16) {
+    auto k = scale_rows_bwd_kernel<__nv_bfloat16>;
+    const int grid = grid_for(reinterpret_cast<const void*>(k), kRowThreads, 0, h->num_sms, blocks);
+    k<<<grid, kRowThreads, 0, s>>>(static_cast<const uint8_t*>(ghs),
+                                   static_cast<const uint8_t*>(hrows), recv_w,
+                                   static_cast<uint8_t*>(gh), gw, h->pos, entries, row_bytes, nvec);
+  } else {
+    auto k = scale_rows_bwd_kernel<float>;
+    const int grid = grid_for(reinterpret_cast<const void*>(k), kRowThreads, 0, h->num_sms, blocks);
+    k<<<grid, kRowThreads, 0, s>>>(static_cast<const uint8_t*>(ghs),
+                                   static_cast<const uint8_t*>(hrows), recv_w,
+                                   static_cast<uint8_t*>(gh), gw, h->pos, entries, row_bytes, nvec);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

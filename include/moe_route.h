@@ -1,0 +1,264 @@
+/*
+ * moe_route.h -- C ABI of the MoE token routing / dispatch / combine library
+ * (one GPU, sm_103a).
+ *
+ * The operations follow these web pages on DeepEP-style token dispatchers:
+ *   [AutoEP-DeepEP]  DeepSpeed PR "Add an opt-in DeepEP transport for the AutoEP
+ *                    expert all-to-all": section "Why" (dedup once per
+ *                    destination rank, tokens taken before top-k expansion,
+ *                    arrivals grouped by expert, weighted combine, backward =
+ *                    dispatch/combine replayed on the forward handle) and the
+ *                    review-fix commit text (router-score gradient must be
+ *                    returned; capacity must grow or fail, not fault).
+ *   [AutoEP-prep]    DeepSpeed PR "Avoid collective token preparation for
+ *                    AutoEP DeepEP": "Summary" (no argsort, no [T*K,H]
+ *                    expansion pass, no split-count exchange, no device-to-host
+ *                    split materialisation), "Testing Done" (score-correction
+ *                    bias, skewed routing, empty expert).
+ *   [Titan-absorb]   torchtitan issue "[MoE] Apply router scores before W2
+ *                    projection": "Motivation" and "Implementation" (scores
+ *                    applied in fp32 to the W2 input, combine becomes a plain
+ *                    sum; scores gathered expert-major as routed_scores_R).
+ *   [NeMo-DeepEPv2]  NeMo Automodel PR "DeepEP v2 dispatcher ...":
+ *                    "Performance" (one handle shared by dispatch and combine).
+ *
+ * Conventions for every entry point:
+ *   - Every pointer named d_* is a DEVICE pointer on the device that was
+ *     current when the handle was created; the caller owns all memory
+ *     (tensors and workspace).  Row tensors must be 16-byte aligned and their
+ *     row size (H or I times the element size) a multiple of 16 bytes.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
+ *     compute calls are asynchronous on it: none synchronises the host,
+ *     allocates memory or copies device -> host.
+ *   - Row dtype: MOE_BF16 (bfloat16) or MOE_F32.  Index tensors are int32,
+ *     router weights fp32, row-major.
+ *   - Return value: MOE_OK, or an error detected on the host before anything
+ *     is launched (MOE_ERR_INVALID, MOE_ERR_CAPACITY, MOE_ERR_STATE), or
+ *     MOE_ERR_CUDA if a launch failed.  Errors in the DATA (an expert index out
+ *     of range, a repeated expert, a non-finite logit, a bounded wait that gave
+ *     up) are found on the device: the kernel sets a bit of the handle's
+ *     device status word (MOE_DEVERR_*) and skips the offending entry; read it
+ *     with moe_read_device_status (which synchronises; not for the hot path).
+ */
+#ifndef MOE_ROUTE_H_
+#define MOE_ROUTE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = 1,  /* null / misaligned pointer, bad size or config     */
+  MOE_ERR_CAPACITY = 2, /* T larger than the handle's max_tokens             */
+  MOE_ERR_CUDA = 3,     /* a CUDA call or kernel launch failed               */
+  MOE_ERR_STATE = 4     /* a row operation called before moe_dispatch_layout */
+} moe_status;
+
+typedef enum moe_dtype { MOE_BF16 = 0, MOE_F32 = 1 } moe_dtype;
+
+typedef enum moe_score_fn { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
+
+/* Device status bits (sticky until moe_clear_device_status). */
+#define MOE_DEVERR_BAD_EXPERT 0x1u /* idx entry outside [0,E): entry dropped      */
+#define MOE_DEVERR_DUP_EXPERT 0x2u /* expert repeated in a token: later dropped   */
+#define MOE_DEVERR_NONFINITE 0x4u  /* NaN/Inf router logit: token's route unspecified */
+#define MOE_DEVERR_TIMEOUT 0x8u    /* a bounded wait inside a kernel gave up      */
+
+/* Limits checked by moe_handle_create. */
+#define MOE_MAX_EXPERTS 512
+#define MOE_MAX_TOPK 16
+
+/*
+ * Router and layout configuration, fixed for the life of a handle.
+ *   num_experts E (1..512), top_k K (1..min(E,16)), num_ranks R (virtual
+ *   destination ranks; E % R == 0; rank(e) = e / (E/R)).
+ *   score_fn: MOE_SCORE_SOFTMAX selects the top-K logits (softmax is strictly
+ *     increasing) and weights them by softmax; MOE_SCORE_SIGMOID selects on
+ *     key_e = sigmoid(l_e) + bias_e in fp64 and weights by the unbiased
+ *     sigmoid ([AutoEP-prep] "score-correction bias").
+ *   num_groups / topk_groups / group_score_topk: group-limited selection
+ *     (sigmoid only): experts form num_groups contiguous groups; a group's
+ *     score is the sum of its top group_score_topk keys; only the best
+ *     topk_groups groups are eligible.  num_groups = 1 disables it.
+ *   renorm: 1 = divide the K selected weights by their sum.
+ *   route_scale: multiplies the weights (1.0 = none).
+ *   max_tokens: capacity T_max; a larger batch is rejected with
+ *     MOE_ERR_CAPACITY ([AutoEP-DeepEP] review fix: a batch that outgrows the
+ *     buffer must not fault).
+ */
+typedef struct moe_config {
+  int32_t num_experts;
+  int32_t top_k;
+  int32_t num_ranks;
+  int32_t score_fn;
+  int32_t num_groups;
+  int32_t topk_groups;
+  int32_t group_score_topk;
+  int32_t renorm;
+  double route_scale;
+  int32_t max_tokens;
+  int32_t reserved;
+} moe_config;
+
+/*
+ * Device pointers into the handle's workspace, filled by moe_dispatch_layout
+ * for the last layout's T tokens (all int32):
+ *   cnt_e[E], off_e[E+1]              per-expert counts, exclusive offsets
+ *   cnt_send_r[R], off_send_r[R+1]    token-deduplicated rows per rank
+ *   cnt_recv_r[R], off_recv_r[R+1]    expert rows per rank
+ *   pos[T*K]          receive row of entry (t,k), -1 if dropped
+ *   recv_token[T*K]   token of receive row p, recv_k[T*K] its k (tail: -1)
+ *   send_token[T*min(K,R)]  token of send row s (tail beyond S: -1)
+ *   send_row_of[T*K]  send row of entry (t,k), -1 if dropped
+ *   recv_send_row[T*K] send row that receive row p expands from (tail: -1)
+ *   S[1]              number of send rows (device scalar)
+ */
+typedef struct moe_layout {
+  int32_t* cnt_e;
+  int32_t* off_e;
+  int32_t* cnt_send_r;
+  int32_t* off_send_r;
+  int32_t* cnt_recv_r;
+  int32_t* off_recv_r;
+  int32_t* pos;
+  int32_t* recv_token;
+  int32_t* recv_k;
+  int32_t* send_token;
+  int32_t* send_row_of;
+  int32_t* recv_send_row;
+  int32_t* S;
+  int32_t num_tokens; /* T of the last layout, -1 before the first */
+  int32_t reserved;
+} moe_layout;
+
+typedef struct moe_handle moe_handle;
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status s);
+
+/*
+ * Bytes of device workspace a handle with configuration `c` needs (0 if the
+ * configuration is invalid).  The workspace holds the layout arrays above
+ * plus per-tile histograms; allocate it 256-byte aligned.
+ */
+size_t moe_workspace_bytes(const moe_config* c);
+
+/*
+ * Creates a handle over caller-owned device workspace `d_workspace`
+ * (`workspace_bytes` >= moe_workspace_bytes(c)) on the current device.  The
+ * handle is a small host object holding the configuration and pointers into
+ * the workspace; it is the "handle the forward dispatch produced" that the
+ * combine and both backward passes replay ([AutoEP-DeepEP] "Why";
+ * [NeMo-DeepEPv2] paired handle).  Set-up call: it clears the workspace's
+ * status word synchronously.  Not thread-safe: use one handle per stream.
+ */
+moe_status moe_handle_create(const moe_config* c, void* d_workspace, size_t workspace_bytes,
+                             moe_handle** out);
+moe_status moe_handle_destroy(moe_handle* h);
+
+/*
+ * Routing: per token, the top-K experts and their weights.
+ *   d_logits [T,E] fp32 router logits; d_bias [E] fp32 score-correction bias
+ *   (sigmoid only; NULL = none).  Outputs d_idx [T,K] int32 in descending key
+ *   order, equal keys to the lower expert index; d_w [T,K] fp32.
+ *   Weights are computed in fp64 and rounded once to fp32.
+ */
+moe_status moe_route_topk(moe_handle* h, const float* d_logits, const float* d_bias, int32_t T,
+                          int32_t* d_idx, float* d_w, void* stream);
+
+/*
+ * Dispatch layout ([AutoEP-DeepEP] "Why"; [AutoEP-prep] "Summary"): from
+ * d_idx [T,K] computes every array of moe_layout on the device, with no host
+ * synchronisation.  Receive rows are grouped by expert, stable by token then
+ * k; send rows by rank, one per (token, rank), stable by token.  The result
+ * depends only on d_idx (bit-identical on replay).  Records T in the handle.
+ * Returns MOE_ERR_CAPACITY if T > max_tokens.
+ */
+moe_status moe_dispatch_layout(moe_handle* h, const int32_t* d_idx, int32_t T, void* stream);
+
+/* Device pointers of the current layout (no device access). */
+moe_status moe_layout_view(const moe_handle* h, moe_layout* out);
+
+/*
+ * Dispatch: permute token rows to expert-grouped receive rows
+ * ([AutoEP-DeepEP] "Why": tokens taken before top-k expansion and replicated
+ * by the dispatch itself).
+ *   d_x [T,H] rows -> d_recv [T*K,H]: d_recv[pos[t,k]] = d_x[t] (bit copy).
+ *   d_w [T,K] and d_recv_w [T*K] (both NULL or both set):
+ *     d_recv_w[pos[t,k]] = d_w[t,k]   ([Titan-absorb] routed_scores_R).
+ *   d_send [T*min(K,R),H] or NULL: d_send[send_row_of[t,k]] = d_x[t], the
+ *     token-deduplicated rank-major rows.
+ * Rows of d_recv beyond off_e[E] (only when entries were dropped) are not
+ * written.
+ */
+moe_status moe_dispatch(const moe_handle* h, const void* d_x, int32_t H, int32_t dtype,
+                        const float* d_w, void* d_recv, float* d_recv_w, void* d_send,
+                        void* stream);
+
+/*
+ * Combine ([AutoEP-DeepEP] "Why": reduces the weighted sum back to token
+ * order; [Titan-absorb]: a plain sum when scores are absorbed):
+ *   d_out[t] = round( sum_k w[t,k] * d_y[pos[t,k]] ), accumulated in fp32 in
+ *   k order with fused multiply-add, rounded once to the row dtype.
+ *   d_w [T,K] fp32, or NULL for the plain sum.
+ */
+moe_status moe_combine(const moe_handle* h, const void* d_y, int32_t H, int32_t dtype,
+                       const float* d_w, void* d_out, void* stream);
+
+/*
+ * Combine backward = a dispatch of the output gradient, plus the router-score
+ * gradient ([AutoEP-DeepEP] "Why" and review fix):
+ *   d_gy[pos[t,k]] = round(w[t,k] * d_g[t])   (fp32 product; d_w NULL: copy)
+ *   d_gw[t,k] = <d_g[t], d_y[pos[t,k]]>       (fp32 accumulation; 0 for a
+ *                                             dropped entry; skipped if d_gw
+ *                                             or d_w is NULL)
+ *   d_g [T,H], d_y [T*K,H] (the forward's expert output), d_gy [T*K,H].
+ */
+moe_status moe_combine_bwd(const moe_handle* h, const void* d_g, const void* d_y, int32_t H,
+                           int32_t dtype, const float* d_w, void* d_gy, float* d_gw,
+                           void* stream);
+
+/*
+ * Dispatch backward = a unit-weight combine ([AutoEP-DeepEP] "Why"):
+ *   d_gx[t] = round( sum_k d_grecv[pos[t,k]] ), fp32 in k order.
+ */
+moe_status moe_dispatch_bwd(const moe_handle* h, const void* d_grecv, int32_t H, int32_t dtype,
+                            void* d_gx, void* stream);
+
+/*
+ * Router-score absorption ([Titan-absorb] "Implementation": the W2 input is
+ * scaled in float32 and restored to its dtype before the grouped GEMM):
+ *   d_hs[r] = round(d_h[r] * d_recv_w[r]) for the T*K receive rows r of the
+ *   current layout.  d_h, d_hs [T*K, I].
+ */
+moe_status moe_scale_rows(const moe_handle* h, const void* d_h, int32_t I, int32_t dtype,
+                          const float* d_recv_w, void* d_hs, void* stream);
+
+/*
+ * Backward of moe_scale_rows:
+ *   d_gh[r] = round(d_recv_w[r] * d_ghs[r])
+ *   d_gw[t,k] = <d_ghs[pos[t,k]], d_h[pos[t,k]]>  (fp32 accumulation; 0 if
+ *   the entry was dropped).
+ */
+moe_status moe_scale_rows_bwd(const moe_handle* h, const void* d_ghs, const void* d_h, int32_t I,
+                              int32_t dtype, const float* d_recv_w, void* d_gh, float* d_gw,
+                              void* stream);
+
+/*
+ * Copies the device status word to *host_flags (MOE_DEVERR_* bits).  This
+ * SYNCHRONISES the handle's device; keep it off the hot path.
+ */
+moe_status moe_read_device_status(const moe_handle* h, uint32_t* host_flags);
+
+/* Clears the device status word (asynchronous on `stream`). */
+moe_status moe_clear_device_status(moe_handle* h, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTE_H_ */

@@ -75,25 +75,37 @@ def _child(seed, name):
     return np.random.SeedSequence(seed).spawn(len(STREAMS))[STREAMS.index(name)]
 
 
-def normal_f32(seed, name, shape, threads=None):
-    """fp32 N(0,1) array of `shape` from stream `name`, drawn chunk by chunk."""
-    n = int(np.prod(shape))
-    out = np.empty(n, np.float32)
+def _fill_chunks(seed, name, n, out, convert, threads):
     nchunks = (n + CHUNK - 1) // CHUNK
     seqs = _child(seed, name).spawn(nchunks)
 
     def fill(c):
         lo, hi = c * CHUNK, min(n, (c + 1) * CHUNK)
-        np.random.Generator(np.random.PCG64(seqs[c])).standard_normal(
-            hi - lo, dtype=np.float32, out=out[lo:hi])
+        a = np.random.Generator(np.random.PCG64(seqs[c])).standard_normal(hi - lo, dtype=np.float32)
+        out[lo:hi] = convert(a)
 
     threads = threads or min(16, os.cpu_count() or 1)
-    if nchunks == 1 or threads == 1:
+    if nchunks <= 1 or threads == 1:
         for c in range(nchunks):
             fill(c)
     else:
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(fill, range(nchunks)))
+
+
+def normal_f32(seed, name, shape, threads=None):
+    """fp32 N(0,1) array of `shape` from stream `name`, drawn chunk by chunk."""
+    n = int(np.prod(shape))
+    out = np.empty(n, np.float32)
+    _fill_chunks(seed, name, n, out, lambda a: a, threads)
+    return out.reshape(shape)
+
+
+def normal_bf16(seed, name, shape, threads=None):
+    """bf16 bits of the same fp32 draws as normal_f32(seed, name, shape)."""
+    n = int(np.prod(shape))
+    out = np.empty(n, np.uint16)
+    _fill_chunks(seed, name, n, out, to_bf16_bits, threads)
     return out.reshape(shape)
 
 
@@ -101,15 +113,14 @@ def to_bf16_bits(a):
     """Round fp32 -> bf16 to nearest even; returns np.uint16 bit patterns."""
     u = np.ascontiguousarray(a, np.float32).view(np.uint32)
     out = np.empty(u.shape, np.uint16)
-    step = CHUNK
     flat_u = u.reshape(-1)
     flat_o = out.reshape(-1)
-    for lo in range(0, flat_u.size, step):
-        v = flat_u[lo:lo + step]
+    for lo in range(0, flat_u.size, CHUNK):
+        v = flat_u[lo:lo + CHUNK]
         r = (v + np.uint32(0x7FFF) + ((v >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
         nan = (v & np.uint32(0x7FFFFFFF)) > np.uint32(0x7F800000)
         r = np.where(nan, (v >> np.uint32(16)) | np.uint32(0x40), r)
-        flat_o[lo:lo + step] = r.astype(np.uint16)
+        flat_o[lo:lo + CHUNK] = r.astype(np.uint16)
     return out
 
 
@@ -119,8 +130,9 @@ def bf16_bits_to_f32(a):
 
 def rows(wl, seed, name, nrows, width):
     """A [nrows, width] row tensor in the workload's row dtype (bf16 bits or fp32)."""
-    a = normal_f32(seed, name, (nrows, width))
-    return to_bf16_bits(a) if wl.dtype == "bf16" else a
+    if wl.dtype == "bf16":
+        return normal_bf16(seed, name, (nrows, width))
+    return normal_f32(seed, name, (nrows, width))
 
 
 def router_logits(wl, seed=None):
@@ -167,9 +179,9 @@ def make_inputs(wl, seed=None, want=("logits", "bias", "x", "y", "g")):
         elif k == "grecv":
             out[k] = rows(wl, seed, "grecv", wl.T * wl.K, wl.H)
         elif k == "h":
-            out[k] = to_bf16_bits(normal_f32(seed, "h", (wl.T * wl.K, wl.I)))
+            out[k] = normal_bf16(seed, "h", (wl.T * wl.K, wl.I))
         elif k == "ghs":
-            out[k] = to_bf16_bits(normal_f32(seed, "ghs", (wl.T * wl.K, wl.I)))
+            out[k] = normal_bf16(seed, "ghs", (wl.T * wl.K, wl.I))
         elif k == "w2":
             w2 = normal_f32(seed, "w2", (wl.E, wl.I, wl.H)) * np.float32(1.0 / np.sqrt(wl.I))
             out[k] = to_bf16_bits(w2)
