@@ -25,6 +25,7 @@ MOE_OK, MOE_ERR_INVALID, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_STATE = range(5
 MOE_BF16, MOE_F32 = 0, 1
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_DEVERR_BAD_EXPERT, MOE_DEVERR_DUP_EXPERT, MOE_DEVERR_NONFINITE, MOE_DEVERR_TIMEOUT = 1, 2, 4, 8
+MOE_DEVERR_INTERNAL = 16
 MOE_MAX_EXPERTS, MOE_MAX_TOPK = 512, 16
 
 EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_handle_create", "moe_handle_destroy",

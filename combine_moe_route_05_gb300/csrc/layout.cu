@@ -204,6 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   }
   __syncthreads();
 
+  const int n_recv_rows = a.T * a.K;
+  const int n_send_rows = a.T * (a.K < a.R ? a.K : a.R);
   if (t < a.T) {
     const uint32_t lt = lanemask_lt();
     const int32_t* off_e = off;
@@ -223,6 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
       const int r = e / a.epr;
       const int cr = (a.E + r) * kWords + warp;
       const int srow = off_s[r] + base[a.E + r] + pre[cr] + __popc(masks[cr] & lt);
+      // the scan guarantees p < T*K and srow < S; a violation (inconsistent
+      // counts) is reported instead of written
+      if (p < 0 || p >= n_recv_rows || srow < 0 || srow >= n_send_rows) {
+        raise_flag(a.flags, MOE_DEVERR_INTERNAL);
+        a.pos[tk] = -1;
+        a.send_row_of[tk] = -1;
+        continue;
+      }
       a.pos[tk] = p;
       a.recv_token[p] = t;
       a.recv_k[p] = k;

@@ -67,6 +67,7 @@ typedef enum moe_score_fn { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_s
 #define MOE_DEVERR_DUP_EXPERT 0x2u /* expert repeated in a token: later dropped   */
 #define MOE_DEVERR_NONFINITE 0x4u  /* NaN/Inf router logit: token's route unspecified */
 #define MOE_DEVERR_TIMEOUT 0x8u    /* a bounded wait inside a kernel gave up      */
+#define MOE_DEVERR_INTERNAL 0x10u  /* layout counts inconsistent: writes skipped  */
 
 /* Limits checked by moe_handle_create. */
 #define MOE_MAX_EXPERTS 512
@@ -151,9 +152,9 @@ size_t moe_workspace_bytes(const moe_config* c);
  * Creates a handle over caller-owned device workspace `d_workspace`
  * (`workspace_bytes` >= moe_workspace_bytes(c)) on the current device.  The
  * handle is a small host object holding the configuration and pointers into
- * the workspace; it is the "handle the forward dispatch produced" that the
- * combine and both backward passes replay ([AutoEP-DeepEP] "Why";
- * [NeMo-DeepEPv2] paired handle).  Set-up call: it clears the workspace's
+ * the workspace.  The layout it holds is the state that the combine and both
+ * backward passes reuse, so the backward never recomputes the layout
+ * ([AutoEP-DeepEP] "Why"; [NeMo-DeepEPv2] "Performance", the paired handle).  Set-up call: it clears the workspace's
  * status word synchronously.  Not thread-safe: use one handle per stream.
  */
 moe_status moe_handle_create(const moe_config* c, void* d_workspace, size_t workspace_bytes,
