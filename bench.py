@@ -421,6 +421,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", type=int, default=3)
+    ap.add_argument("--tokens", type=int, default=0, help="override T (small profiling cases)")
     ap.add_argument("--cpu-tokens", type=int, default=1024)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-e2e", action="store_true")
@@ -429,6 +430,8 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     wl = synth.WORKLOADS[args.workload]
+    if args.tokens:
+        wl = wl.with_tokens(args.tokens)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

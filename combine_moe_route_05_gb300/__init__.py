@@ -122,6 +122,8 @@ def _row_dtype(t):
 def _req(t, dtype=None, shape=None, name="tensor"):
     if t is None:
         return
+    if shape is not None and any(d < 0 for d in shape):
+        shape = None  # no layout yet: the library itself reports MOE_ERR_STATE
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
     if not t.is_contiguous():
@@ -327,18 +329,18 @@ class MoeRouter:
         return recv, recv_w, send
 
     def combine(self, y, w=None, stream=None):
-        out = torch.empty(self.h.T, y.shape[1], dtype=y.dtype, device=y.device)
+        out = torch.empty(max(self.h.T, 0), y.shape[1], dtype=y.dtype, device=y.device)
         moe_combine(self.h, y, w, out, stream)
         return out
 
     def combine_bwd(self, g, y=None, w=None, stream=None):
-        gy = torch.empty(self.h.T * self.h.K, g.shape[1], dtype=g.dtype, device=g.device)
-        gw = torch.empty(self.h.T, self.h.K, dtype=torch.float32, device=g.device) if w is not None else None
+        gy = torch.empty(max(self.h.T, 0) * self.h.K, g.shape[1], dtype=g.dtype, device=g.device)
+        gw = torch.empty(max(self.h.T, 0), self.h.K, dtype=torch.float32, device=g.device) if w is not None else None
         moe_combine_bwd(self.h, g, y, w, gy, gw, stream)
         return gy, gw
 
     def dispatch_bwd(self, grecv, stream=None):
-        gx = torch.empty(self.h.T, grecv.shape[1], dtype=grecv.dtype, device=grecv.device)
+        gx = torch.empty(max(self.h.T, 0), grecv.shape[1], dtype=grecv.dtype, device=grecv.device)
         moe_dispatch_bwd(self.h, grecv, gx, stream)
         return gx
 
@@ -349,6 +351,6 @@ class MoeRouter:
 
     def scale_rows_bwd(self, ghs, hrows, recv_w, stream=None):
         gh = torch.empty_like(hrows)
-        gw = torch.empty(self.h.T, self.h.K, dtype=torch.float32, device=hrows.device)
+        gw = torch.empty(max(self.h.T, 0), self.h.K, dtype=torch.float32, device=hrows.device)
         moe_scale_rows_bwd(self.h, ghs, hrows, recv_w, gh, gw, stream)
         return gh, gw
