@@ -31,7 +31,9 @@ MOE_MAX_EXPERTS, MOE_MAX_TOPK = 512, 16
 EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_handle_create", "moe_handle_destroy",
            "moe_route_topk", "moe_dispatch_layout", "moe_layout_view", "moe_dispatch",
            "moe_combine", "moe_combine_bwd", "moe_dispatch_bwd", "moe_scale_rows",
-           "moe_scale_rows_bwd", "moe_read_device_status", "moe_clear_device_status")
+           "moe_scale_rows_bwd", "moe_read_device_status", "moe_clear_device_status",
+           "moe_dispatch_layout_static")
+MOE_LAYOUT_STATIC_COUNTERS = 65536
 
 
 class MoeConfig(ctypes.Structure):
@@ -84,6 +86,7 @@ def lib():
             "moe_scale_rows_bwd": ([P, P, P, i32, i32, P, P, P, P], st),
             "moe_read_device_status": ([P, P], st),
             "moe_clear_device_status": ([P, P], st),
+            "moe_dispatch_layout_static": ([P, P, i32, P, P, P], st),
         }
         for name, (args, res) in sigs.items():
             f = getattr(L, name)
@@ -282,6 +285,38 @@ def moe_read_device_status(h):
 
 def moe_clear_device_status(h, stream=None):
     _check("moe_clear_device_status", lib().moe_clear_device_status(h.ptr, _stream(stream)))
+
+
+LAYOUT_FIELDS = ("cnt_e", "off_e", "cnt_send_r", "off_send_r", "cnt_recv_r", "off_recv_r", "pos",
+                 "recv_token", "recv_k", "send_token", "send_row_of", "recv_send_row", "S")
+
+
+def layout_sizes(T, K, E, R):
+    """Element counts (int32) of the layout arrays for T tokens."""
+    return {"cnt_e": E, "off_e": E + 1, "cnt_send_r": R, "off_send_r": R + 1, "cnt_recv_r": R,
+            "off_recv_r": R + 1, "pos": T * K, "recv_token": T * K, "recv_k": T * K,
+            "send_token": T * min(K, R), "send_row_of": T * K, "recv_send_row": T * K, "S": 1}
+
+
+def moe_dispatch_layout_static(cfg, idx, out, status=None, stream=None):
+    """Allocation-free layout into caller-owned int32 tensors `out` (a dict
+    keyed like LAYOUT_FIELDS, sized by layout_sizes); `status` an optional
+    one-element int32 CUDA tensor that collects MOE_DEVERR_* bits."""
+    T = idx.shape[0]
+    _req(idx, torch.int32, (T, cfg.top_k), "idx")
+    sizes = layout_sizes(T, cfg.top_k, cfg.num_experts, cfg.num_ranks)
+    v = MoeLayout()
+    for name in LAYOUT_FIELDS:
+        t = out[name]
+        _req(t, torch.int32, None, name)
+        if t.numel() != sizes[name]:
+            raise ValueError("%s must have %d elements, got %d" % (name, sizes[name], t.numel()))
+        setattr(v, name, t.data_ptr() if t.numel() else None)
+    v.num_tokens = T
+    _req(status, torch.int32, (1,), "status")
+    _check("moe_dispatch_layout_static",
+           lib().moe_dispatch_layout_static(ctypes.byref(cfg), _ptr(idx), T, ctypes.byref(v),
+                                            _ptr(status), _stream(stream)))
 
 
 def layout_tensors(h):

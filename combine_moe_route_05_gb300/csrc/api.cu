@@ -101,6 +101,10 @@ cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 }  // namespace
 
+namespace moe {
+bool valid_config(const moe_config* c) { return config_valid(c); }
+}  // namespace moe
+
 extern "C" {
 
 const char* moe_status_string(moe_status s) {

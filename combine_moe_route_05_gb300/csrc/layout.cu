@@ -320,4 +320,45 @@ cudaError_t launch_layout(const moe_handle* h, const int32_t* idx, int T, cudaSt
   return cudaGetLastError();
 }
 
+int layout_tiles(int T) { return T > 0 ? (T + kTile - 1) / kTile : 1; }
+
+// The same two launches as launch_layout, over caller-chosen buffers: the
+// outputs in `out`, the status word `flags` (may be null), and the scratch
+// (arrival ticket, zero on entry, and max_tiles * (E + R) tile counters).
+cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T,
+                                  const moe_layout& out, uint32_t* flags, uint32_t* ticket,
+                                  int32_t* tile_hist, int max_tiles, cudaStream_t s) {
+  LayoutArgs a;
+  a.idx = idx;
+  a.T = T;
+  a.K = c.top_k;
+  a.E = c.num_experts;
+  a.R = c.num_ranks;
+  a.epr = c.num_experts / c.num_ranks;
+  a.ntiles = layout_tiles(T);
+  a.max_tiles = max_tiles;
+  a.flags = flags;
+  a.ticket = ticket;
+  a.cnt_e = out.cnt_e;
+  a.off_e = out.off_e;
+  a.cnt_send_r = out.cnt_send_r;
+  a.off_send_r = out.off_send_r;
+  a.cnt_recv_r = out.cnt_recv_r;
+  a.off_recv_r = out.off_recv_r;
+  a.S = out.S;
+  a.pos = out.pos;
+  a.recv_token = out.recv_token;
+  a.recv_k = out.recv_k;
+  a.send_token = out.send_token;
+  a.send_row_of = out.send_row_of;
+  a.recv_send_row = out.recv_send_row;
+  a.tile_hist = tile_hist;
+  const int cols = a.E + a.R;
+  layout_count_kernel<<<a.ntiles, kThreads, count_smem(cols), s>>>(a);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  layout_scatter_kernel<<<a.ntiles, kThreads, scatter_smem(cols), s>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace moe

@@ -181,6 +181,38 @@ moe_status moe_route_topk(moe_handle* h, const float* d_logits, const float* d_b
  */
 moe_status moe_dispatch_layout(moe_handle* h, const int32_t* d_idx, int32_t T, void* stream);
 
+/*
+ * Allocation-free dispatch layout.  The web pages have no counterpart: this
+ * entry point exists for callers that are not allowed to allocate device
+ * memory, for example a plugin whose host framework hands it only its input
+ * and output buffers and forbids cudaMalloc on the execution path (a
+ * cudaMalloc there would synchronise the device and is illegal while the
+ * framework captures the stream), so it cannot own the workspace that
+ * moe_handle_create needs.
+ *
+ * Computes exactly what moe_dispatch_layout computes, for configuration `c`
+ * (validated as in moe_workspace_bytes; max_tokens is not used) and the T
+ * rows of d_idx [T,K], into the caller's arrays named in `out` (the layout of
+ * moe_layout: counts and offsets always; pos, recv_token, recv_k,
+ * send_row_of, recv_send_row [T*K] and send_token [T*min(K,R)] when T > 0;
+ * out->num_tokens is ignored).  Data errors set bits in *d_status
+ * (MOE_DEVERR_*) when d_status is not NULL.
+ *
+ * It allocates nothing: its scratch (an arrival counter and per-tile
+ * counters) is a static device array of MOE_LAYOUT_STATIC_COUNTERS + 64
+ * int32 (about 256 KiB), which every GPU that loads the library holds until
+ * the process exits.  Limit: (E + R) * ceil(T / 1024) must not exceed
+ * MOE_LAYOUT_STATIC_COUNTERS, else MOE_ERR_CAPACITY (for E = 256, R = 64:
+ * T up to 208896).  The first call on a device looks up the array's device
+ * address and sets kernel attributes for that device, so make that first
+ * call outside any stream capture.  All calls share the one array: calls
+ * that overlap on the GPU (on different streams without ordering) race and
+ * give wrong layouts; order them on one stream.  Asynchronous on `stream`.
+ */
+#define MOE_LAYOUT_STATIC_COUNTERS 65536
+moe_status moe_dispatch_layout_static(const moe_config* c, const int32_t* d_idx, int32_t T,
+                                      const moe_layout* out, uint32_t* d_status, void* stream);
+
 /* Device pointers of the current layout (no device access). */
 moe_status moe_layout_view(const moe_handle* h, moe_layout* out);
 
