@@ -34,6 +34,7 @@ EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_handle_create", "moe
            "moe_scale_rows_bwd", "moe_read_device_status", "moe_clear_device_status",
            "moe_dispatch_layout_static")
 MOE_LAYOUT_STATIC_COUNTERS = 65536
+MOE_LAYOUT_TILE_TOKENS = 512
 
 
 class MoeConfig(ctypes.Structure):

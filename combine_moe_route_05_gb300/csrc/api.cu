@@ -49,7 +49,7 @@ Plan plan(const moe_config* c) {
   const size_t E = c->num_experts, R = c->num_ranks, K = c->top_k;
   const size_t T = c->max_tokens;
   const size_t i4 = sizeof(int32_t);
-  p.max_tiles = static_cast<int>(T > 0 ? (T + MOE_LAYOUT_TILE - 1) / MOE_LAYOUT_TILE : 1);
+  p.max_tiles = static_cast<int>(T > 0 ? (T + MOE_LAYOUT_TILE_TOKENS - 1) / MOE_LAYOUT_TILE_TOKENS : 1);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;

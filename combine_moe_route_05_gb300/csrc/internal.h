@@ -6,8 +6,6 @@
 
 #include "moe_route.h"
 
-// Tokens per layout tile (one 1024-thread block, one token per thread).
-#define MOE_LAYOUT_TILE 1024
 
 struct moe_handle {
   moe_config cfg;

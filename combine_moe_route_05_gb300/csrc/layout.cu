@@ -7,30 +7,39 @@
 // grouped by expert; "Avoid collective token preparation for AutoEP DeepEP",
 // "Summary": no argsort and no device-to-host split materialisation.
 //
-// Two launches over tiles of 1024 tokens (one token per thread):
+// Two launches over tiles of MOE_LAYOUT_TILE_TOKENS tokens (one per thread):
 //   1. count: each block marks, in shared-memory bitmasks, which of its
 //      tokens use each expert and each rank (atomicOr is order-free, so the
 //      result does not depend on thread timing), writes per-tile column
 //      counts, and the block that arrives last (an atomic ticket, no
 //      waiting) scans them into per-tile bases, counts and offsets;
-//   2. scatter: each block rebuilds its bitmasks; the rank of a token among
-//      the tile's users of an expert is a popcount of the mask words before
-//      it, so every position is a pure function of idx (bit-identical on
-//      replay).
+//   2. scatter: each block rebuilds its bitmasks.  The rank of a token among
+//      the tile's users of a column (expert or rank) is a popcount of the mask
+//      bits before it, so every position is a pure function of idx
+//      (bit-identical on replay).  Token-major outputs (pos, send_row_of) are
+//      staged in shared memory and written as one contiguous run per tile;
+//      receive-row and send-row outputs are written column by column, the
+//      j-th set bit of a column going to its j-th row, so those writes are
+//      contiguous runs as well.
+//
+// Masks are stored word-major with an odd row stride ([word][col], stride
+// cols | 1) so that the lanes of a warp, which share a word index and differ in
+// column, hit different shared-memory banks.
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 namespace {
 
-constexpr int kTile = MOE_LAYOUT_TILE;
+constexpr int kTile = MOE_LAYOUT_TILE_TOKENS;
 constexpr int kWords = kTile / 32;  // mask words per column
 constexpr int kThreads = kTile;
 constexpr int kWarps = kThreads / 32;
+static_assert(kTile % 32 == 0 && kTile <= 1024, "tile must be whole warps of one block");
 
 struct LayoutArgs {
   const int32_t* idx;
-  int T, K, E, R, epr, ntiles, max_tiles;
+  int T, K, E, R, epr, ntiles;
   uint32_t* flags;
   uint32_t* ticket;
   int32_t* cnt_e;
@@ -46,14 +55,16 @@ struct LayoutArgs {
   int32_t* send_token;
   int32_t* send_row_of;
   int32_t* recv_send_row;
-  int32_t* tile_hist;
+  int32_t* tile_hist;  // [ntiles][cols], exclusive tile bases after the scan
 };
 
-// Loads this thread's token (if any), validates it and sets its bits in the
-// tile's expert and rank masks.  Returns the valid-entry bitmask; ek holds the
-// expert of each entry.
-__device__ __forceinline__ uint32_t mark_token(const LayoutArgs& a, int t, uint32_t* masks,
-                                               int (&ek)[MOE_MAX_TOPK]) {
+__host__ __device__ constexpr int col_stride(int cols) { return cols | 1; }
+
+// Loads this thread's token (if any), validates it, keeps its row in
+// `idx_s` (if not null) and sets its bits in the tile's expert and rank masks.
+// Returns the valid-entry bitmask; ek holds the expert of each entry.
+__device__ __forceinline__ uint32_t mark_token(const LayoutArgs& a, int t, uint32_t* masks, int cp,
+                                               int* idx_s, int (&ek)[MOE_MAX_TOPK]) {
   uint32_t valid = 0;
   if (t >= a.T) return 0;
   const int word = threadIdx.x >> 5;
@@ -65,6 +76,7 @@ __device__ __forceinline__ uint32_t mark_token(const LayoutArgs& a, int t, uint3
     if (k >= a.K) break;
     const int e = __ldg(row + k);
     ek[k] = e;
+    if (idx_s) idx_s[threadIdx.x * a.K + k] = e;
     bool ok = e >= 0 && e < a.E;
     if (!ok) bad |= MOE_DEVERR_BAD_EXPERT;
 #pragma unroll
@@ -77,8 +89,8 @@ __device__ __forceinline__ uint32_t mark_token(const LayoutArgs& a, int t, uint3
     }
     if (ok) {
       valid |= 1u << k;
-      atomicOr(&masks[e * kWords + word], bit);
-      atomicOr(&masks[(a.E + e / a.epr) * kWords + word], bit);
+      atomicOr(&masks[word * cp + e], bit);
+      atomicOr(&masks[word * cp + a.E + e / a.epr], bit);
     }
   }
   if (bad) raise_flag(a.flags, bad);
@@ -87,18 +99,20 @@ __device__ __forceinline__ uint32_t mark_token(const LayoutArgs& a, int t, uint3
 
 __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a) {
   extern __shared__ uint32_t lsm[];
-  uint32_t* masks = lsm;  // [(E+R) * kWords]
   const int cols = a.E + a.R;
+  const int cp = col_stride(cols);
+  uint32_t* masks = lsm;  // [kWords][cp]
   const int tile = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < cols * kWords; i += kThreads) masks[i] = 0;
+  for (int i = threadIdx.x; i < kWords * cp; i += kThreads) masks[i] = 0;
   __syncthreads();
   int ek[MOE_MAX_TOPK];
-  mark_token(a, tile * kTile + threadIdx.x, masks, ek);
+  mark_token(a, tile * kTile + threadIdx.x, masks, cp, nullptr, ek);
   __syncthreads();
-  for (int col = warp; col < cols; col += kWarps) {
-    const int c = __reduce_add_sync(0xffffffffu, __popc(masks[col * kWords + lane]));
-    if (lane == 0) a.tile_hist[static_cast<size_t>(col) * a.max_tiles + tile] = c;
+  for (int col = threadIdx.x; col < cols; col += kThreads) {
+    int c = 0;
+#pragma unroll 8
+    for (int w = 0; w < kWords; ++w) c += __popc(masks[w * cp + col]);
+    a.tile_hist[static_cast<size_t>(tile) * cols + col] = c;
   }
   __threadfence();
   __syncthreads();
@@ -112,21 +126,22 @@ __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a)
   // exclusive scans over experts and over ranks.
   int32_t* tot = reinterpret_cast<int32_t*>(masks);  // [cols], masks are dead now
   for (int col = threadIdx.x; col < cols; col += kThreads) {
-    int32_t* base = a.tile_hist + static_cast<size_t>(col) * a.max_tiles;
     int run = 0;
     for (int t0 = 0; t0 < a.ntiles; t0 += 16) {
       int v[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = t0 + i < a.ntiles ? __ldcg(base + t0 + i) : 0;
+      for (int i = 0; i < 16; ++i)
+        v[i] = t0 + i < a.ntiles ? __ldcg(a.tile_hist + static_cast<size_t>(t0 + i) * cols + col) : 0;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        if (t0 + i < a.ntiles) base[t0 + i] = run;
+        if (t0 + i < a.ntiles) a.tile_hist[static_cast<size_t>(t0 + i) * cols + col] = run;
         run += v[i];
       }
     }
     tot[col] = run;
   }
   __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp < 2) {
     // warp 0 scans the E expert totals, warp 1 the R rank totals
     const int n = warp == 0 ? a.E : a.R;
@@ -156,7 +171,6 @@ __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a)
     }
   }
   __syncthreads();
-  __threadfence_block();
   for (int r = threadIdx.x; r < a.R; r += kThreads) {
     const int lo = a.off_e[r * a.epr], hi = a.off_e[(r + 1) * a.epr];
     a.off_recv_r[r] = lo;
@@ -168,19 +182,39 @@ __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a)
   }
 }
 
+// shared memory of the scatter kernel, in order
+struct ScatterSmem {
+  int cols, cp, K;
+  __host__ __device__ size_t masks() const { return 0; }
+  __host__ __device__ size_t pre() const { return masks() + sizeof(uint32_t) * kWords * cp; }
+  __host__ __device__ size_t idx() const { return align(pre() + sizeof(uint16_t) * kWords * cp); }
+  __host__ __device__ size_t stage() const { return idx() + sizeof(int32_t) * kTile * K; }
+  __host__ __device__ size_t base() const { return stage() + 2 * sizeof(int32_t) * kTile * K; }
+  __host__ __device__ size_t off() const { return base() + sizeof(int32_t) * cols; }
+  __host__ __device__ size_t bytes() const { return off() + sizeof(int32_t) * (cols + 2); }
+  __host__ __device__ static size_t align(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
+};
+
 __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs a) {
-  extern __shared__ uint32_t lsm[];
+  extern __shared__ __align__(16) uint8_t ssm[];
   const int cols = a.E + a.R;
-  uint32_t* masks = lsm;                                                  // [cols * kWords]
-  uint16_t* pre = reinterpret_cast<uint16_t*>(masks + cols * kWords);     // [cols * kWords]
-  int32_t* base = reinterpret_cast<int32_t*>(pre + cols * kWords);        // [cols] tile bases
-  int32_t* off = base + cols;                                             // [E+1 | R+1]
+  const int cp = col_stride(cols);
+  const ScatterSmem L{cols, cp, a.K};
+  uint32_t* masks = reinterpret_cast<uint32_t*>(ssm + L.masks());  // [kWords][cp]
+  uint16_t* pre = reinterpret_cast<uint16_t*>(ssm + L.pre());      // [kWords][cp]
+  int32_t* idx_s = reinterpret_cast<int32_t*>(ssm + L.idx());      // [kTile][K]
+  int32_t* pos_s = reinterpret_cast<int32_t*>(ssm + L.stage());    // [kTile][K]
+  int32_t* srow_s = pos_s + kTile * a.K;                           // [kTile][K]
+  int32_t* base = reinterpret_cast<int32_t*>(ssm + L.base());      // [cols] tile bases
+  int32_t* off = reinterpret_cast<int32_t*>(ssm + L.off());        // off_e[E+1], off_s[R+1]
   const int tile = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile_t0 = tile * kTile;
+  const int tile_n = max(0, min(kTile, a.T - tile_t0));  // tokens in this tile
 
-  for (int i = threadIdx.x; i < cols * kWords; i += kThreads) masks[i] = 0;
+  for (int i = threadIdx.x; i < kWords * cp; i += kThreads) masks[i] = 0;
   for (int c = threadIdx.x; c < cols; c += kThreads) {
-    base[c] = a.tile_hist[static_cast<size_t>(c) * a.max_tiles + tile];
+    base[c] = a.tile_hist[static_cast<size_t>(tile) * cols + c];
     off[c + (c >= a.E ? 1 : 0)] = c < a.E ? a.off_e[c] : a.off_send_r[c - a.E];
   }
   if (threadIdx.x == 0) {
@@ -188,90 +222,123 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
     off[cols + 1] = a.off_send_r[a.R];
   }
   __syncthreads();
-  const int t = tile * kTile + threadIdx.x;
+  const int t = tile_t0 + threadIdx.x;
   int ek[MOE_MAX_TOPK];
-  const uint32_t valid = mark_token(a, t, masks, ek);
+  const uint32_t valid = mark_token(a, t, masks, cp, idx_s, ek);
   __syncthreads();
-  for (int col = warp; col < cols; col += kWarps) {
-    const int c = __popc(masks[col * kWords + lane]);
-    int incl = c;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += o;
+  // exclusive prefix of the popcounts over the words of each column
+  for (int col = threadIdx.x; col < cols; col += kThreads) {
+    int run = 0;
+#pragma unroll 8
+    for (int w = 0; w < kWords; ++w) {
+      pre[w * cp + col] = static_cast<uint16_t>(run);
+      run += __popc(masks[w * cp + col]);
     }
-    pre[col * kWords + lane] = static_cast<uint16_t>(incl - c);
   }
   __syncthreads();
 
+  const int32_t* off_e = off;
+  const int32_t* off_s = off + a.E + 1;
   const int n_recv_rows = a.T * a.K;
   const int n_send_rows = a.T * (a.K < a.R ? a.K : a.R);
+  const uint32_t lt = lanemask_lt();
+
+  // token-major: pos[t,k] and send_row_of[t,k], staged then written as one run
   if (t < a.T) {
-    const uint32_t lt = lanemask_lt();
-    const int32_t* off_e = off;
-    const int32_t* off_s = off + a.E + 1;
 #pragma unroll
     for (int k = 0; k < MOE_MAX_TOPK; ++k) {
       if (k >= a.K) break;
-      const size_t tk = static_cast<size_t>(t) * a.K + k;
-      if (!((valid >> k) & 1u)) {
-        a.pos[tk] = -1;
-        a.send_row_of[tk] = -1;
-        continue;
+      int p = -1, srow = -1;
+      if ((valid >> k) & 1u) {
+        const int e = ek[k];
+        const int r = e / a.epr;
+        const int ce = warp * cp + e;
+        const int cr = warp * cp + a.E + r;
+        p = off_e[e] + base[e] + pre[ce] + __popc(masks[ce] & lt);
+        srow = off_s[r] + base[a.E + r] + pre[cr] + __popc(masks[cr] & lt);
+        // the scan guarantees p < T*K and srow < S; a violation (inconsistent
+        // counts) is reported and the entry dropped instead of written
+        if (p < 0 || p >= n_recv_rows || srow < 0 || srow >= n_send_rows) {
+          raise_flag(a.flags, MOE_DEVERR_INTERNAL);
+          p = -1;
+          srow = -1;
+        }
       }
-      const int e = ek[k];
-      const int ce = e * kWords + warp;
-      const int p = off_e[e] + base[e] + pre[ce] + __popc(masks[ce] & lt);
-      const int r = e / a.epr;
-      const int cr = (a.E + r) * kWords + warp;
-      const int srow = off_s[r] + base[a.E + r] + pre[cr] + __popc(masks[cr] & lt);
-      // the scan guarantees p < T*K and srow < S; a violation (inconsistent
-      // counts) is reported instead of written
-      if (p < 0 || p >= n_recv_rows || srow < 0 || srow >= n_send_rows) {
+      pos_s[threadIdx.x * a.K + k] = p;
+      srow_s[threadIdx.x * a.K + k] = srow;
+    }
+  }
+  __syncthreads();
+  {
+    const int n = tile_n * a.K;
+    int32_t* pos_g = a.pos + static_cast<size_t>(tile_t0) * a.K;
+    int32_t* srow_g = a.send_row_of + static_cast<size_t>(tile_t0) * a.K;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      pos_g[i] = pos_s[i];
+      srow_g[i] = srow_s[i];
+    }
+  }
+
+  // column-major: the j-th token of a column within the tile goes to the
+  // column's j-th row of this tile
+  for (int col = warp; col < cols; col += kWarps) {
+    const int last = (kWords - 1) * cp + col;
+    const int n = pre[last] + __popc(masks[last]);
+    const bool is_rank = col >= a.E;
+    const int row0 = (is_rank ? off_s[col - a.E] : off_e[col]) + base[col];
+    for (int j0 = 0; j0 < n; j0 += 32) {
+      const int j = j0 + lane;
+      if (j >= n) break;
+      int lo = 0, hi = kWords - 1;  // largest word w with pre[w] <= j
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid * cp + col] <= j) lo = mid; else hi = mid - 1;
+      }
+      const uint32_t m = masks[lo * cp + col];
+      const int bit = static_cast<int>(__fns(m, 0, j - pre[lo * cp + col] + 1));
+      if (bit < 0) {  // cannot happen for j < n; reported rather than used
         raise_flag(a.flags, MOE_DEVERR_INTERNAL);
-        a.pos[tk] = -1;
-        a.send_row_of[tk] = -1;
         continue;
       }
-      a.pos[tk] = p;
-      a.recv_token[p] = t;
-      a.recv_k[p] = k;
-      a.send_row_of[tk] = srow;
-      a.recv_send_row[p] = srow;
-      bool first = true;
-#pragma unroll
-      for (int j = 0; j < MOE_MAX_TOPK; ++j) {
-        if (j >= k) break;
-        if (((valid >> j) & 1u) && ek[j] / a.epr == r) first = false;
+      const int tl = lo * 32 + bit;
+      const int row = row0 + j;
+      if (is_rank) {
+        if (row >= 0 && row < n_send_rows) a.send_token[row] = tile_t0 + tl;
+        else raise_flag(a.flags, MOE_DEVERR_INTERNAL);
+        continue;
       }
-      if (first) a.send_token[srow] = t;
+      if (row < 0 || row >= n_recv_rows) {
+        raise_flag(a.flags, MOE_DEVERR_INTERNAL);
+        continue;
+      }
+      int k = 0;
+      for (int kk = a.K - 1; kk >= 0; --kk)  // first (valid) entry of this expert
+        if (idx_s[tl * a.K + kk] == col) k = kk;
+      a.recv_token[row] = tile_t0 + tl;
+      a.recv_k[row] = k;
+      a.recv_send_row[row] = srow_s[tl * a.K + k];
     }
   }
 
   // tails: receive rows past off_e[E] and send rows past S
   const long long gtid = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
   const long long gsize = static_cast<long long>(gridDim.x) * kThreads;
-  const long long n_recv = static_cast<long long>(a.T) * a.K;
-  for (long long p = off[a.E] + gtid; p < n_recv; p += gsize) {
+  for (long long p = off[a.E] + gtid; p < n_recv_rows; p += gsize) {
     a.recv_token[p] = -1;
     a.recv_k[p] = -1;
     a.recv_send_row[p] = -1;
   }
-  const long long n_send = static_cast<long long>(a.T) * (a.K < a.R ? a.K : a.R);
-  for (long long s = off[cols + 1] + gtid; s < n_send; s += gsize) a.send_token[s] = -1;
+  for (long long s = off[cols + 1] + gtid; s < n_send_rows; s += gsize) a.send_token[s] = -1;
 }
 
-size_t count_smem(int cols) { return static_cast<size_t>(cols) * kWords * sizeof(uint32_t); }
+size_t count_smem(int cols) { return static_cast<size_t>(kWords) * col_stride(cols) * sizeof(uint32_t); }
 
-size_t scatter_smem(int cols) {
-  return static_cast<size_t>(cols) * kWords * (sizeof(uint32_t) + sizeof(uint16_t)) +
-         static_cast<size_t>(cols) * sizeof(int32_t) + static_cast<size_t>(cols + 2) * sizeof(int32_t);
-}
+size_t scatter_smem(int cols, int K) { return ScatterSmem{cols, col_stride(cols), K}.bytes(); }
 
 }  // namespace
 
 size_t layout_smem_bytes(int E, int R) {
-  const size_t a = count_smem(E + R), b = scatter_smem(E + R);
+  const size_t a = count_smem(E + R), b = scatter_smem(E + R, MOE_MAX_TOPK);
   return a > b ? a : b;
 }
 
@@ -284,47 +351,11 @@ cudaError_t prepare_layout_kernels() {
                               max_smem);
 }
 
-cudaError_t launch_layout(const moe_handle* h, const int32_t* idx, int T, cudaStream_t s) {
-  const moe_config& c = h->cfg;
-  LayoutArgs a;
-  a.idx = idx;
-  a.T = T;
-  a.K = c.top_k;
-  a.E = c.num_experts;
-  a.R = c.num_ranks;
-  a.epr = c.num_experts / c.num_ranks;
-  a.ntiles = T > 0 ? (T + kTile - 1) / kTile : 1;
-  a.max_tiles = h->max_tiles;
-  a.flags = h->flags;
-  a.ticket = h->ticket;
-  a.cnt_e = h->cnt_e;
-  a.off_e = h->off_e;
-  a.cnt_send_r = h->cnt_send_r;
-  a.off_send_r = h->off_send_r;
-  a.cnt_recv_r = h->cnt_recv_r;
-  a.off_recv_r = h->off_recv_r;
-  a.S = h->S;
-  a.pos = h->pos;
-  a.recv_token = h->recv_token;
-  a.recv_k = h->recv_k;
-  a.send_token = h->send_token;
-  a.send_row_of = h->send_row_of;
-  a.recv_send_row = h->recv_send_row;
-  a.tile_hist = h->tile_hist;
-
-  const int cols = a.E + a.R;
-  layout_count_kernel<<<a.ntiles, kThreads, count_smem(cols), s>>>(a);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  layout_scatter_kernel<<<a.ntiles, kThreads, scatter_smem(cols), s>>>(a);
-  return cudaGetLastError();
-}
-
 int layout_tiles(int T) { return T > 0 ? (T + kTile - 1) / kTile : 1; }
 
-// The same two launches as launch_layout, over caller-chosen buffers: the
-// outputs in `out`, the status word `flags` (may be null), and the scratch
-// (arrival ticket, zero on entry, and max_tiles * (E + R) tile counters).
+// The two launches over caller-chosen buffers: the outputs in `out`, the
+// status word `flags` (may be null), and the scratch (arrival ticket, zero on
+// entry, and tiles * (E + R) tile counters).
 cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T,
                                   const moe_layout& out, uint32_t* flags, uint32_t* ticket,
                                   int32_t* tile_hist, int max_tiles, cudaStream_t s) {
@@ -336,7 +367,7 @@ cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T
   a.R = c.num_ranks;
   a.epr = c.num_experts / c.num_ranks;
   a.ntiles = layout_tiles(T);
-  a.max_tiles = max_tiles;
+  if (a.ntiles > max_tiles) return cudaErrorInvalidValue;
   a.flags = flags;
   a.ticket = ticket;
   a.cnt_e = out.cnt_e;
@@ -357,8 +388,27 @@ cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T
   layout_count_kernel<<<a.ntiles, kThreads, count_smem(cols), s>>>(a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  layout_scatter_kernel<<<a.ntiles, kThreads, scatter_smem(cols), s>>>(a);
+  layout_scatter_kernel<<<a.ntiles, kThreads, scatter_smem(cols, a.K), s>>>(a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_layout(const moe_handle* h, const int32_t* idx, int T, cudaStream_t s) {
+  moe_layout out{};
+  out.cnt_e = h->cnt_e;
+  out.off_e = h->off_e;
+  out.cnt_send_r = h->cnt_send_r;
+  out.off_send_r = h->off_send_r;
+  out.cnt_recv_r = h->cnt_recv_r;
+  out.off_recv_r = h->off_recv_r;
+  out.S = h->S;
+  out.pos = h->pos;
+  out.recv_token = h->recv_token;
+  out.recv_k = h->recv_k;
+  out.send_token = h->send_token;
+  out.send_row_of = h->send_row_of;
+  out.recv_send_row = h->recv_send_row;
+  return launch_layout_buffers(h->cfg, idx, T, out, h->flags, h->ticket, h->tile_hist,
+                               h->max_tiles, s);
 }
 
 }  // namespace moe

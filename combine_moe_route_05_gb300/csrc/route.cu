@@ -3,16 +3,31 @@
 // Softmax routing selects the K largest logits (softmax is strictly
 // increasing, so the set and order equal those of the probabilities) and
 // weights them by softmax; group-limited sigmoid routing selects on
-// key = sigmoid(logit) + score-correction bias in fp64 and weights by the
-// unbiased sigmoid (DeepSpeed "Avoid collective token preparation for AutoEP
-// DeepEP", "Testing Done": exact routes, score-correction bias).  Selection
-// order is descending key; equal keys go to the lower expert index.  Weights
-// are computed in fp64 and rounded once to fp32.
+// key = sigmoid(logit) + score-correction bias and weights by the unbiased
+// sigmoid (DeepSpeed "Avoid collective token preparation for AutoEP DeepEP",
+// "Testing Done": exact routes, score-correction bias).  Selection order is
+// descending key, equal keys to the lower expert index.  Weights are computed
+// in fp64 and rounded once to fp32.
 //
-// Each lane holds VPL consecutive experts (e = lane*VPL + j).  A selection
-// round takes the best entry strictly after the previous pick in the total
-// order (key descending, index ascending), reduced across the warp with
-// shuffles, so no per-entry "taken" state is needed.
+// The sigmoid selection is defined on fp64 keys, but fp64 arithmetic is slow
+// on this GPU, so the kernel first selects on fp32 keys and keeps that result
+// only when it provably equals the fp64 one:
+//   |key32 - key64| <= DELTA = 5e-7 + 1.25e-7 * max|key32| for every expert
+// (expf is accurate to 2 ulp, i.e. 2^-22 relative; 1 + e and the reciprocal
+// are each rounded once, 2^-24; so the sigmoid is within 1.5 * 2^-22 of its
+// value, at most 3.6e-7 since it is <= 1; adding the bias rounds once more,
+// 2^-24 |key|; fp64 keys are exact to 1e-15).  A group score (sum of the
+// group's top GK keys) is then within GK * (DELTA + 1.25e-7 * max|gs|) of the
+// fp64 one, since a top-m sum moves by at most m times the largest change of
+// its inputs.  If the fp32 gap between the last kept and the first dropped
+// group exceeds twice that bound, and the gap between each of the K + 1 best
+// eligible experts and the next exceeds 2 * DELTA, the fp64 selection is the
+// same set in the same order; otherwise the token is recomputed in fp64.
+//
+// Each lane holds VPL consecutive experts (e = lane*VPL + j).  The fp64
+// weights of the K selected experts of TB = 32 / K tokens are computed
+// together, one (token, k) per lane, so each fp64 instruction serves TB
+// tokens.
 #include <cfloat>
 #include <climits>
 
@@ -22,8 +37,10 @@
 namespace moe {
 namespace {
 
-constexpr int kRouteWarps = 8;  // tokens in flight per block
+constexpr int kRouteWarps = 8;  // warps per block
 constexpr unsigned kFull = 0xffffffffu;
+constexpr float kDeltaAbs = 5e-7f;
+constexpr float kDeltaRel = 1.25e-7f;
 
 struct RouteArgs {
   const float* logits;
@@ -32,6 +49,7 @@ struct RouteArgs {
   int G, TG, GK;
   int renorm;
   int vec4;
+  int fast;  // the fp32 selection applies to this configuration
   double scale;
   int32_t* idx;
   float* w;
@@ -62,7 +80,14 @@ __device__ __forceinline__ void warp_best(V& v, int& i) {
   }
 }
 
-// Loads the lane's VPL logits of row t; entries past E read as -inf.
+// fp32 -> uint32 with the same order (for -inf..+inf; no NaN reaches here)
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Loads the lane's VPL logits of row t; entries past E read as -inf, NaN as
+// -inf (flagged with the other non-finite values).
 template <int VPL>
 __device__ __forceinline__ bool load_logits(const RouteArgs& a, int t, int lane, float (&v)[VPL]) {
   const float* row = a.logits + static_cast<size_t>(t) * a.E;
@@ -96,163 +121,363 @@ __device__ __forceinline__ bool load_logits(const RouteArgs& a, int t, int lane,
   return bad;
 }
 
-template <int VPL>
-__global__ void __launch_bounds__(kRouteWarps * 32) route_softmax_kernel(RouteArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int nwarps = gridDim.x * kRouteWarps;
-  for (int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5); t < a.T; t += nwarps) {
-    float v[VPL];
-    const bool bad = load_logits<VPL>(a, t, lane, v);
-    if (__any_sync(kFull, bad) && lane == 0) raise_flag(a.flags, MOE_DEVERR_NONFINITE);
+// ---------------------------------------------------------------------------
+// reference-precision paths, one token at a time (all lanes take part)
 
-    float pv = INFINITY, myv = 0.f;
-    int pi = -1, myi = 0;
-    for (int k = 0; k < a.K; ++k) {
-      float bv = -INFINITY;
-      int bi = INT_MAX;
+// Sigmoid routing of token t entirely in fp64 (keys, group scores,
+// selection and weights); writes idx and w.  wkeys: E doubles of shared
+// memory owned by this warp.
+template <int VPL>
+__device__ void sigmoid_token_fp64(const RouteArgs& a, int t, int lane, const float (&v)[VPL],
+                                   double* wkeys) {
+  const int gsz = a.E / a.G;
+  double s[VPL], key[VPL];
 #pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const int e = lane * VPL + j;
-        if (comes_after(v[j], e, pv, pi) && ranks_before(v[j], e, bv, bi)) {
-          bv = v[j];
-          bi = e;
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane * VPL + j;
+    if (e < a.E) {
+      s[j] = 1.0 / (1.0 + exp(-static_cast<double>(v[j])));
+      key[j] = s[j] + (a.bias ? static_cast<double>(__ldg(a.bias + e)) : 0.0);
+    } else {
+      s[j] = 0.0;
+      key[j] = -INFINITY;
+    }
+  }
+  uint32_t keep = 0xffffffffu;
+  if (a.G > 1) {
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+      if (lane * VPL + j < a.E) wkeys[lane * VPL + j] = key[j];
+    __syncwarp();
+    double gscore = -INFINITY;
+    if (lane < a.G) {
+      const int base = lane * gsz;
+      double sum = 0.0, qv = INFINITY;
+      int qi = -1;
+      for (int r = 0; r < a.GK; ++r) {
+        double bv = -INFINITY;
+        int bi = INT_MAX;
+        for (int i = 0; i < gsz; ++i) {
+          const double kv = wkeys[base + i];
+          if (comes_after(kv, base + i, qv, qi) && ranks_before(kv, base + i, bv, bi)) {
+            bv = kv;
+            bi = base + i;
+          }
         }
+        sum += bv;
+        qv = bv;
+        qi = bi;
+      }
+      gscore = sum;
+    }
+    __syncwarp();
+    keep = 0;
+    double pv = INFINITY;
+    int pi = -1;
+    for (int r = 0; r < a.TG; ++r) {
+      double bv = -INFINITY;
+      int bi = INT_MAX;
+      if (lane < a.G && comes_after(gscore, lane, pv, pi)) {
+        bv = gscore;
+        bi = lane;
       }
       warp_best(bv, bi);
+      if (bi < 32) keep |= 1u << bi;
       pv = bv;
       pi = bi;
-      if (lane == k) {
-        myv = bv;
-        myi = bi;
+    }
+  }
+  double pv = INFINITY, mys = 0.0;
+  int pi = -1, myi = 0;
+  for (int k = 0; k < a.K; ++k) {
+    double bv = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane * VPL + j;
+      const bool eligible = e < a.E && ((keep >> (e / gsz)) & 1u);
+      if (eligible && comes_after(key[j], e, pv, pi) && ranks_before(key[j], e, bv, bi)) {
+        bv = key[j];
+        bi = e;
       }
     }
-
-    const double lmax = static_cast<double>(__shfl_sync(kFull, myv, 0));
-    const double ex = lane < a.K ? exp(static_cast<double>(myv) - lmax) : 0.0;
-    double den = 0.0;
-    if (a.renorm) {
-      for (int k = 0; k < a.K; ++k) den += __shfl_sync(kFull, ex, k);
-    } else {
-      double part = 0.0;
+    warp_best(bv, bi);
+    pv = bv;
+    pi = bi;
+    double sv = 0.0;
 #pragma unroll
-      for (int j = 0; j < VPL; ++j)
-        if (lane * VPL + j < a.E) part += exp(static_cast<double>(v[j]) - lmax);
-      for (int l = 0; l < 32; ++l) den += __shfl_sync(kFull, part, l);
+    for (int j = 0; j < VPL; ++j)
+      if (lane * VPL + j == bi) sv = s[j];
+    sv = __shfl_sync(kFull, sv, bi / VPL);
+    if (lane == k) {
+      mys = sv;
+      myi = bi;
     }
-    if (lane < a.K) {
-      a.idx[static_cast<size_t>(t) * a.K + lane] = myi;
-      a.w[static_cast<size_t>(t) * a.K + lane] = static_cast<float>((ex / den) * a.scale);
-    }
+  }
+  double den = 0.0;
+  for (int k = 0; k < a.K; ++k) den += __shfl_sync(kFull, mys, k);
+  if (lane < a.K) {
+    const double p = a.renorm ? mys / den : mys;
+    a.idx[static_cast<size_t>(t) * a.K + lane] = myi;
+    a.w[static_cast<size_t>(t) * a.K + lane] = static_cast<float>(p * a.scale);
   }
 }
 
+// Softmax routing of token t without renormalisation (the denominator runs
+// over all E experts); writes idx and w.
 template <int VPL>
-__global__ void __launch_bounds__(kRouteWarps * 32) route_sigmoid_kernel(RouteArgs a) {
-  extern __shared__ double route_smem[];
-  double* wkeys = route_smem + (threadIdx.x >> 5) * a.E;
-  const int lane = threadIdx.x & 31;
-  const int nwarps = gridDim.x * kRouteWarps;
-  const int gsz = a.E / a.G;
-  for (int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5); t < a.T; t += nwarps) {
-    float v[VPL];
-    const bool bad = load_logits<VPL>(a, t, lane, v);
-    if (__any_sync(kFull, bad) && lane == 0) raise_flag(a.flags, MOE_DEVERR_NONFINITE);
+__device__ void softmax_token_full(const RouteArgs& a, int t, int lane, const float (&v)[VPL]) {
+  uint32_t taken = 0;
+  float myv = 0.f;
+  int myi = 0;
+  for (int k = 0; k < a.K; ++k) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane * VPL + j;
+      if (!((taken >> j) & 1u) && ranks_before(v[j], e, bv, bi)) {
+        bv = v[j];
+        bi = e;
+      }
+    }
+    warp_best(bv, bi);
+    if (bi / VPL == lane) taken |= 1u << (bi % VPL);
+    if (lane == k) {
+      myv = bv;
+      myi = bi;
+    }
+  }
+  const double lmax = static_cast<double>(__shfl_sync(kFull, myv, 0));
+  double part = 0.0;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j)
+    if (lane * VPL + j < a.E) part += exp(static_cast<double>(v[j]) - lmax);
+  double den = 0.0;
+  for (int l = 0; l < 32; ++l) den += __shfl_sync(kFull, part, l);
+  if (lane < a.K) {
+    const double ex = exp(static_cast<double>(myv) - lmax);
+    a.idx[static_cast<size_t>(t) * a.K + lane] = myi;
+    a.w[static_cast<size_t>(t) * a.K + lane] = static_cast<float>((ex / den) * a.scale);
+  }
+}
 
-    double s[VPL], key[VPL];
+// ---------------------------------------------------------------------------
+// fp32 selection of one token; returns false if it cannot be trusted (the
+// caller then recomputes the token in fp64).  On success, lane base + k holds
+// the k-th selected expert and its logit.
+
+// Top-GK values of a lane's VPL values, merged across the L lanes of a group
+// (butterfly over lane bits 1..L/2), summed in descending order.
+template <int VPL, int GKMAX>
+__device__ __forceinline__ float group_score_fp32(const float (&key)[VPL], int gk, int lanes) {
+  float top[GKMAX];
+#pragma unroll
+  for (int i = 0; i < GKMAX; ++i) top[i] = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    float x = key[j];
+#pragma unroll
+    for (int i = 0; i < GKMAX; ++i) {
+      if (x > top[i]) {
+        const float y = top[i];
+        top[i] = x;
+        x = y;
+      }
+    }
+  }
+  for (int off = 1; off < lanes; off <<= 1) {
+    float other[GKMAX];
+#pragma unroll
+    for (int i = 0; i < GKMAX; ++i) other[i] = __shfl_xor_sync(kFull, top[i], off);
+#pragma unroll
+    for (int i2 = 0; i2 < GKMAX; ++i2) {
+      float x = other[i2];
+#pragma unroll
+      for (int i = 0; i < GKMAX; ++i) {
+        if (x > top[i]) {
+          const float y = top[i];
+          top[i] = x;
+          x = y;
+        }
+      }
+    }
+  }
+  float sum = 0.0f;
+#pragma unroll
+  for (int i = 0; i < GKMAX; ++i)
+    if (i < gk) sum = __fadd_rn(sum, top[i]);
+  return sum;
+}
+
+template <int VPL, bool SIGMOID>
+__device__ __forceinline__ bool select_fp32(const RouteArgs& a, int lane, const float (&v)[VPL],
+                                            int base, int& my_idx, float& my_logit) {
+  float key[VPL];
+  float maxabs = 0.0f;
+  if (SIGMOID) {
 #pragma unroll
     for (int j = 0; j < VPL; ++j) {
       const int e = lane * VPL + j;
       if (e < a.E) {
-        s[j] = 1.0 / (1.0 + exp(-static_cast<double>(v[j])));
-        key[j] = s[j] + (a.bias ? static_cast<double>(__ldg(a.bias + e)) : 0.0);
+        const float s = __frcp_rn(__fadd_rn(1.0f, expf(-v[j])));
+        key[j] = __fadd_rn(s, a.bias ? __ldg(a.bias + e) : 0.0f);
+        maxabs = fmaxf(maxabs, fabsf(key[j]));
       } else {
-        s[j] = 0.0;
         key[j] = -INFINITY;
       }
     }
-
-    uint32_t keep = 0xffffffffu;  // eligible groups
-    if (a.G > 1) {
+  } else {
 #pragma unroll
-      for (int j = 0; j < VPL; ++j)
-        if (lane * VPL + j < a.E) wkeys[lane * VPL + j] = key[j];
-      __syncwarp();
-      double gscore = -INFINITY;
-      if (lane < a.G) {
-        // sum of the group's top-GK keys, added in descending order
-        const int base = lane * gsz;
-        double sum = 0.0, qv = INFINITY;
-        int qi = -1;
-        for (int r = 0; r < a.GK; ++r) {
-          double bv = -INFINITY;
-          int bi = INT_MAX;
-          for (int i = 0; i < gsz; ++i) {
-            const double kv = wkeys[base + i];
-            if (comes_after(kv, base + i, qv, qi) && ranks_before(kv, base + i, bv, bi)) {
-              bv = kv;
-              bi = base + i;
-            }
-          }
-          sum += bv;
-          qv = bv;
-          qi = bi;
-        }
-        gscore = sum;
-      }
-      __syncwarp();
-      keep = 0;
-      double pv = INFINITY;
-      int pi = -1;
-      for (int r = 0; r < a.TG; ++r) {
-        double bv = -INFINITY;
-        int bi = INT_MAX;
-        if (lane < a.G && comes_after(gscore, lane, pv, pi)) {
-          bv = gscore;
-          bi = lane;
-        }
-        warp_best(bv, bi);
-        if (bi < 32) keep |= 1u << bi;
-        pv = bv;
-        pi = bi;
+    for (int j = 0; j < VPL; ++j) key[j] = v[j];
+  }
+  float delta = 0.0f;
+  if (SIGMOID) {
+    // non-negative floats order like their bit patterns
+    maxabs = __uint_as_float(__reduce_max_sync(kFull, __float_as_uint(maxabs)));
+    delta = kDeltaAbs + kDeltaRel * maxabs;
+    if (!(delta < 1e-3f)) return false;  // huge or non-finite keys
+  }
+
+  // groups (sigmoid only): lanes of a group are contiguous and L = gsz / VPL
+  bool eligible_lane = lane * VPL < a.E;
+  if (SIGMOID && a.G > 1) {
+    const int gsz = a.E / a.G;
+    const int L = gsz / VPL;
+    const float gs = group_score_fp32<VPL, 4>(key, a.GK, L);
+    float gsv[32];
+    float gmax = 0.0f;
+#pragma unroll
+    for (int g = 0; g < 32; ++g) {
+      gsv[g] = -INFINITY;
+      if (g < a.G) {  // uniform across the warp
+        gsv[g] = __shfl_sync(kFull, gs, (g * L) & 31);
+        gmax = fmaxf(gmax, fabsf(gsv[g]));
       }
     }
-
-    double pv = INFINITY, mys = 0.0;
-    int pi = -1, myi = 0;
-    for (int k = 0; k < a.K; ++k) {
-      double bv = -INFINITY;
-      int bi = INT_MAX;
+    // the TG best groups, ties to the lower group, and the gap to the next
+    uint32_t keep = 0;
+    float last = 0.0f, next = -INFINITY;
+    for (int r = 0; r <= a.TG && r < a.G; ++r) {
+      float bv = -INFINITY;
+      int bg = -1;
 #pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const int e = lane * VPL + j;
-        const bool eligible = e < a.E && ((keep >> (e / gsz)) & 1u);
-        if (eligible && comes_after(key[j], e, pv, pi) && ranks_before(key[j], e, bv, bi)) {
+      for (int g = 0; g < 32; ++g)
+        if (g < a.G && !((keep >> g) & 1u) && (bg < 0 || gsv[g] > bv)) {
+          bv = gsv[g];
+          bg = g;
+        }
+      if (r < a.TG) {
+        keep |= 1u << bg;
+        last = bv;
+      } else {
+        next = bv;
+      }
+    }
+    const float dg = a.GK * (delta + kDeltaRel * gmax);
+    if (a.TG < a.G && !(last - next > 2.0f * dg)) return false;
+    eligible_lane = eligible_lane && ((keep >> ((lane * VPL) / gsz)) & 1u);
+  }
+
+  // K + 1 rounds of warp arg-max over the eligible keys
+  uint32_t taken = 0;
+  float prev = 0.0f;
+  const int n_elig = SIGMOID && a.G > 1 ? a.TG * (a.E / a.G) : a.E;
+  const int rounds = SIGMOID ? (a.K < n_elig ? a.K + 1 : a.K) : a.K;
+  for (int k = 0; k < rounds; ++k) {
+    float bv = -INFINITY;
+    int bj = -1;
+    if (eligible_lane) {
+#pragma unroll
+      for (int j = 0; j < VPL; ++j)
+        if (!((taken >> j) & 1u) && lane * VPL + j < a.E && (bj < 0 || key[j] > bv)) {
           bv = key[j];
-          bi = e;
+          bj = j;
         }
-      }
-      warp_best(bv, bi);
-      pv = bv;
-      pi = bi;
-      double sv = 0.0;
+    }
+    const uint32_t ok_bits = bj >= 0 ? order_key(bv) : 0u;
+    const uint32_t best = __reduce_max_sync(kFull, ok_bits);
+    const uint32_t who = __ballot_sync(kFull, bj >= 0 && ok_bits == best);
+    const int wl = __ffs(who) - 1;
+    const int wj = __shfl_sync(kFull, bj, wl);
+    const float wv = __shfl_sync(kFull, bv, wl);
+    if (lane == wl) taken |= 1u << wj;
+    if (SIGMOID && k > 0 && !(prev - wv > 2.0f * delta)) return false;
+    prev = wv;
+    if (k < a.K) {
+      // the selected expert's logit, from its owner lane
+      float lg = 0.0f;
 #pragma unroll
       for (int j = 0; j < VPL; ++j)
-        if (lane * VPL + j == bi) sv = s[j];
-      sv = __shfl_sync(kFull, sv, bi / VPL);
-      if (lane == k) {
-        mys = sv;
-        myi = bi;
+        if (j == wj) lg = v[j];
+      lg = __shfl_sync(kFull, lg, wl);
+      if (lane == base + k) {
+        my_idx = wl * VPL + wj;
+        my_logit = lg;
       }
-    }
-
-    double den = 0.0;
-    for (int k = 0; k < a.K; ++k) den += __shfl_sync(kFull, mys, k);
-    if (lane < a.K) {
-      const double p = a.renorm ? mys / den : mys;
-      a.idx[static_cast<size_t>(t) * a.K + lane] = myi;
-      a.w[static_cast<size_t>(t) * a.K + lane] = static_cast<float>(p * a.scale);
     }
   }
+  return true;
+}
+
+template <int VPL, bool SIGMOID>
+__global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
+  extern __shared__ double route_smem[];
+  double* wkeys = route_smem + (threadIdx.x >> 5) * a.E;
+  const int lane = threadIdx.x & 31;
+  const int TB = 32 / a.K;  // tokens per fp64 weight pass
+  const int nwarps = gridDim.x * kRouteWarps;
+  const int j_of_lane = lane / a.K, k_of_lane = lane % a.K;
+  for (int t0 = (blockIdx.x * kRouteWarps + (threadIdx.x >> 5)) * TB; t0 < a.T; t0 += nwarps * TB) {
+    int my_idx = 0;
+    float my_logit = 0.0f;
+    bool my_fast = false;
+    for (int j = 0; j < TB; ++j) {
+      const int t = t0 + j;
+      if (t >= a.T) break;
+      float v[VPL];
+      const bool bad = load_logits<VPL>(a, t, lane, v);
+      if (__any_sync(kFull, bad) && lane == 0) raise_flag(a.flags, MOE_DEVERR_NONFINITE);
+      // a softmax selection on fp32 logits is exact even with infinities; a
+      // sigmoid token with a non-finite logit goes to the fp64 path
+      const bool use_fast = a.fast && !(SIGMOID && __any_sync(kFull, bad));
+      int sel_idx = 0;
+      float sel_logit = 0.0f;
+      const bool ok = use_fast && select_fp32<VPL, SIGMOID>(a, lane, v, j * a.K, sel_idx, sel_logit);
+      if (ok) {
+        if (j_of_lane == j) {
+          my_idx = sel_idx;
+          my_logit = sel_logit;
+          my_fast = true;
+        }
+      } else if (SIGMOID) {
+        sigmoid_token_fp64<VPL>(a, t, lane, v, wkeys);
+      } else {
+        softmax_token_full<VPL>(a, t, lane, v);
+      }
+    }
+    // fp64 weights of the tokens selected in fp32: lane = (token j, rank k)
+    const int t = t0 + j_of_lane;
+    double val;
+    if (SIGMOID) {
+      val = 1.0 / (1.0 + exp(-static_cast<double>(my_logit)));
+    } else {
+      const float top = __shfl_sync(kFull, my_logit, (j_of_lane * a.K) & 31);
+      val = exp(static_cast<double>(my_logit) - static_cast<double>(top));
+    }
+    double den = 0.0;
+    for (int k = 0; k < a.K; ++k) den += __shfl_sync(kFull, val, (j_of_lane * a.K + k) & 31);
+    if (my_fast && j_of_lane < TB && t < a.T) {
+      const double p = (SIGMOID && !a.renorm) ? val : val / den;
+      a.idx[static_cast<size_t>(t) * a.K + k_of_lane] = my_idx;
+      a.w[static_cast<size_t>(t) * a.K + k_of_lane] = static_cast<float>(p * a.scale);
+    }
+  }
+}
+
+template <int VPL, bool SIGMOID>
+void launch_one(const RouteArgs& a, int grid, size_t smem, cudaStream_t s) {
+  route_kernel<VPL, SIGMOID><<<grid, kRouteWarps * 32, smem, s>>>(a);
 }
 
 }  // namespace
@@ -277,28 +502,29 @@ cudaError_t launch_route_topk(const moe_handle* h, const float* logits, const fl
   a.flags = h->flags;
   if (T == 0) return cudaSuccess;
 
-  const int blocks_needed = (T + kRouteWarps - 1) / kRouteWarps;
+  const int vpl = a.E <= 32 ? 1 : a.E <= 64 ? 2 : a.E <= 128 ? 4 : a.E <= 256 ? 8 : 16;
+  const bool sigmoid = c.score_fn == MOE_SCORE_SIGMOID;
+  if (sigmoid) {
+    // fp32 pre-selection needs whole lanes per group, a power-of-two lane
+    // count per group, and at most 4 keys per group score
+    const int gsz = a.E / a.G;
+    const int L = gsz / vpl;
+    a.fast = a.G == 1 || (gsz % vpl == 0 && L >= 1 && (L & (L - 1)) == 0 && a.GK <= 4);
+  } else {
+    a.fast = a.renorm;  // without renormalisation the weights need all E exponentials
+  }
+  const int TB = 32 / a.K;
+  const int warps_needed = (T + TB - 1) / TB;
+  const int blocks_needed = (warps_needed + kRouteWarps - 1) / kRouteWarps;
   const int cap = h->num_sms * 16;
   const int grid = blocks_needed < cap ? blocks_needed : cap;
-  const int vpl = a.E <= 32 ? 1 : a.E <= 64 ? 2 : a.E <= 128 ? 4 : a.E <= 256 ? 8 : 16;
-  const dim3 block(kRouteWarps * 32);
-  if (c.score_fn == MOE_SCORE_SOFTMAX) {
-    switch (vpl) {
-      case 1: route_softmax_kernel<1><<<grid, block, 0, s>>>(a); break;
-      case 2: route_softmax_kernel<2><<<grid, block, 0, s>>>(a); break;
-      case 4: route_softmax_kernel<4><<<grid, block, 0, s>>>(a); break;
-      case 8: route_softmax_kernel<8><<<grid, block, 0, s>>>(a); break;
-      default: route_softmax_kernel<16><<<grid, block, 0, s>>>(a); break;
-    }
-  } else {
-    const size_t smem = a.G > 1 ? static_cast<size_t>(kRouteWarps) * a.E * sizeof(double) : 0;
-    switch (vpl) {
-      case 1: route_sigmoid_kernel<1><<<grid, block, smem, s>>>(a); break;
-      case 2: route_sigmoid_kernel<2><<<grid, block, smem, s>>>(a); break;
-      case 4: route_sigmoid_kernel<4><<<grid, block, smem, s>>>(a); break;
-      case 8: route_sigmoid_kernel<8><<<grid, block, smem, s>>>(a); break;
-      default: route_sigmoid_kernel<16><<<grid, block, smem, s>>>(a); break;
-    }
+  const size_t smem = sigmoid && a.G > 1 ? static_cast<size_t>(kRouteWarps) * a.E * sizeof(double) : 0;
+  switch (vpl) {
+    case 1: sigmoid ? launch_one<1, true>(a, grid, smem, s) : launch_one<1, false>(a, grid, smem, s); break;
+    case 2: sigmoid ? launch_one<2, true>(a, grid, smem, s) : launch_one<2, false>(a, grid, smem, s); break;
+    case 4: sigmoid ? launch_one<4, true>(a, grid, smem, s) : launch_one<4, false>(a, grid, smem, s); break;
+    case 8: sigmoid ? launch_one<8, true>(a, grid, smem, s) : launch_one<8, false>(a, grid, smem, s); break;
+    default: sigmoid ? launch_one<16, true>(a, grid, smem, s) : launch_one<16, false>(a, grid, smem, s); break;
   }
   return cudaGetLastError();
 }

@@ -73,6 +73,9 @@ typedef enum moe_score_fn { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_s
 #define MOE_MAX_EXPERTS 512
 #define MOE_MAX_TOPK 16
 
+/* Tokens per tile of the layout kernels (one thread block per tile). */
+#define MOE_LAYOUT_TILE_TOKENS 512
+
 /*
  * Router and layout configuration, fixed for the life of a handle.
  *   num_experts E (1..512), top_k K (1..min(E,16)), num_ranks R (virtual
@@ -201,9 +204,9 @@ moe_status moe_dispatch_layout(moe_handle* h, const int32_t* d_idx, int32_t T, v
  * It allocates nothing: its scratch (an arrival counter and per-tile
  * counters) is a static device array of MOE_LAYOUT_STATIC_COUNTERS + 64
  * int32 (about 256 KiB), which every GPU that loads the library holds until
- * the process exits.  Limit: (E + R) * ceil(T / 1024) must not exceed
- * MOE_LAYOUT_STATIC_COUNTERS, else MOE_ERR_CAPACITY (for E = 256, R = 64:
- * T up to 208896).  The first call on a device looks up the array's device
+ * the process exits.  Limit: (E + R) * ceil(T / MOE_LAYOUT_TILE_TOKENS) must
+ * not exceed MOE_LAYOUT_STATIC_COUNTERS, else MOE_ERR_CAPACITY (for E = 256,
+ * R = 64: T up to 104448).  The first call on a device looks up the array's device
  * address and sets kernel attributes for that device, so make that first
  * call outside any stream capture.  All calls share the one array: calls
  * that overlap on the GPU (on different streams without ordering) race and

@@ -169,3 +169,56 @@ def test_fp32_rows_and_large_rows():
         g = mk(rng.standard_normal((T, H)).astype(np.float32))
         idx, w = oracle.route_softmax(logits, K)
         check_chain(router(wl), wl, idx, w, x, y, g)
+
+
+def near_tie_logits(rng, T, E):
+    """Logits from a few values nudged by a few fp32 ulps, so that many keys
+    are closer than the fp32 selection's error bound and the kernel must decide
+    those tokens in fp64."""
+    base = rng.choice(np.float32([-1.0, 0.0, 0.25, 0.5, 1.0, 2.0]), size=(T, E))
+    ulps = rng.integers(-3, 4, size=(T, E)).astype(np.int32)
+    return (base.view(np.int32) + ulps).view(np.float32)
+
+
+@pytest.mark.parametrize("grouped", [False, True])
+def test_near_tie_sigmoid_routing_matches_fp64_oracle(grouped):
+    rng = np.random.default_rng(21 + grouped)
+    T, E, K = 3000, 256, 8
+    logits = near_tie_logits(rng, T, E)
+    bias = (rng.integers(-2, 3, size=E) * np.float32(1e-7)).astype(np.float32)
+    G, TG, GK = (8, 4, 2) if grouped else (1, 1, 1)
+    wl = synth.Workload("neartie", T=T, H=16, E=E, K=K, R=64, score_fn="sigmoid", n_groups=G,
+                        topk_groups=TG, group_score_topk=GK)
+    r = router(wl)
+    gi, gw_ = r.route(to_dev(logits), to_dev(bias))
+    idx, w = oracle.route_sigmoid_grouped(logits, bias, K, G, TG, GK)
+    assert np.array_equal(to_host(gi), idx)
+    assert_ulp(to_host(gw_), w, 1, "w")
+
+
+def test_near_tie_softmax_routing_is_exact():
+    rng = np.random.default_rng(23)
+    T, E, K = 3000, 128, 8
+    logits = near_tie_logits(rng, T, E)
+    wl = synth.Workload("neartie", T=T, H=16, E=E, K=K, R=8)
+    gi, gw_ = router(wl).route(to_dev(logits))
+    idx, w = oracle.route_softmax(logits, K)
+    assert np.array_equal(to_host(gi), idx)
+    assert_ulp(to_host(gw_), w, 1, "w")
+
+
+@pytest.mark.parametrize("bias_std", [0.01, 0.3])
+def test_large_random_grouped_routing_matches_fp64_oracle(bias_std):
+    """131072 DeepSeek-V3-shaped tokens: any case where the fp32 selection's
+    error bound were wrong would show up as an index mismatch."""
+    T, E = 131072, 256
+    rng = np.random.default_rng(int(bias_std * 1000))
+    logits = (rng.standard_normal((T, E)) * 2).astype(np.float32)
+    bias = (rng.standard_normal(E) * bias_std).astype(np.float32)
+    wl = synth.Workload("big", T=T, H=16, E=E, K=8, R=64, score_fn="sigmoid", n_groups=8,
+                        topk_groups=4, group_score_topk=2)
+    gi, gw_ = router(wl).route(to_dev(logits), to_dev(bias))
+    idx, w = oracle.route_sigmoid_grouped(logits, bias, 8, 8, 4, 2)
+    gi = to_host(gi)
+    assert np.array_equal(gi, idx), "%d tokens differ" % int((gi != idx).any(1).sum())
+    assert_ulp(to_host(gw_), w, 1, "w")

@@ -66,7 +66,7 @@ def test_static_layout_rejects_sizes_beyond_its_scratch():
     cfg = moe.make_config(wl.E, wl.K, wl.R, 16, score_fn="sigmoid", num_groups=8, topk_groups=4,
                           group_score_topk=2)
     tiles_max = moe.MOE_LAYOUT_STATIC_COUNTERS // (wl.E + wl.R)
-    T = tiles_max * 1024 + 1
+    T = tiles_max * moe.MOE_LAYOUT_TILE_TOKENS + 1
     v = moe.MoeLayout()
     st = moe.lib().moe_dispatch_layout_static(
         __import__("ctypes").byref(cfg), None, T, __import__("ctypes").byref(v), None, None)
