@@ -175,9 +175,12 @@ def near_tie_logits(rng, T, E):
     """Logits from a few values nudged by a few fp32 ulps, so that many keys
     are closer than the fp32 selection's error bound and the kernel must decide
     those tokens in fp64."""
-    base = rng.choice(np.float32([-1.0, 0.0, 0.25, 0.5, 1.0, 2.0]), size=(T, E))
+    # no zero base: a bit-pattern nudge below +0 would make a NaN
+    base = rng.choice(np.float32([-1.0, -0.125, 0.25, 0.5, 1.0, 2.0]), size=(T, E))
     ulps = rng.integers(-3, 4, size=(T, E)).astype(np.int32)
-    return (base.view(np.int32) + ulps).view(np.float32)
+    out = (base.view(np.int32) + ulps).view(np.float32)
+    assert np.isfinite(out).all()
+    return out
 
 
 @pytest.mark.parametrize("grouped", [False, True])
