@@ -344,34 +344,26 @@ __device__ __forceinline__ bool select_fp32(const RouteArgs& a, int lane, const 
   if (SIGMOID && a.G > 1) {
     const int gsz = a.E / a.G;
     const int L = gsz / VPL;
-    const float gs = group_score_fp32<VPL, 4>(key, a.GK, L);
-    float gsv[32];
-    float gmax = 0.0f;
-#pragma unroll
-    for (int g = 0; g < 32; ++g) {
-      gsv[g] = -INFINITY;
-      if (g < a.G) {  // uniform across the warp
-        gsv[g] = __shfl_sync(kFull, gs, (g * L) & 31);
-        gmax = fmaxf(gmax, fabsf(gsv[g]));
-      }
-    }
-    // the TG best groups, ties to the lower group, and the gap to the next
+    const float gs = group_score_fp32<VPL, 2>(key, a.GK, L);
+    // lane g < G holds group g's score; TG + 1 rounds of warp arg-max, ties
+    // to the lower group
+    const bool glane = lane < a.G;
+    const float my_gs = __shfl_sync(kFull, gs, (lane * L) & 31);
+    const float gmax = __uint_as_float(__reduce_max_sync(kFull, glane ? __float_as_uint(fabsf(my_gs)) : 0u));
     uint32_t keep = 0;
     float last = 0.0f, next = -INFINITY;
-    for (int r = 0; r <= a.TG && r < a.G; ++r) {
-      float bv = -INFINITY;
-      int bg = -1;
-#pragma unroll
-      for (int g = 0; g < 32; ++g)
-        if (g < a.G && !((keep >> g) & 1u) && (bg < 0 || gsv[g] > bv)) {
-          bv = gsv[g];
-          bg = g;
-        }
+    const int rounds = a.TG < a.G ? a.TG + 1 : a.TG;
+    for (int r = 0; r < rounds; ++r) {
+      const bool cand = glane && !((keep >> lane) & 1u);
+      const uint32_t bits = cand ? order_key(my_gs) : 0u;
+      const uint32_t best = __reduce_max_sync(kFull, bits);
+      const int wl = __ffs(__ballot_sync(kFull, cand && bits == best)) - 1;
+      const float val = __shfl_sync(kFull, my_gs, wl & 31);
       if (r < a.TG) {
-        keep |= 1u << bg;
-        last = bv;
+        keep |= 1u << wl;
+        last = val;
       } else {
-        next = bv;
+        next = val;
       }
     }
     const float dg = a.GK * (delta + kDeltaRel * gmax);
@@ -506,10 +498,10 @@ cudaError_t launch_route_topk(const moe_handle* h, const float* logits, const fl
   const bool sigmoid = c.score_fn == MOE_SCORE_SIGMOID;
   if (sigmoid) {
     // fp32 pre-selection needs whole lanes per group, a power-of-two lane
-    // count per group, and at most 4 keys per group score
+    // count per group, and at most 2 keys per group score
     const int gsz = a.E / a.G;
     const int L = gsz / vpl;
-    a.fast = a.G == 1 || (gsz % vpl == 0 && L >= 1 && (L & (L - 1)) == 0 && a.GK <= 4);
+    a.fast = a.G == 1 || (gsz % vpl == 0 && L >= 1 && (L & (L - 1)) == 0 && a.GK <= 2);
   } else {
     a.fast = a.renorm;  // without renormalisation the weights need all E exponentials
   }
