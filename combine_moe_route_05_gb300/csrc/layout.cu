@@ -16,11 +16,10 @@
 //   2. scatter: each block rebuilds its bitmasks.  The rank of a token among
 //      the tile's users of a column (expert or rank) is a popcount of the mask
 //      bits before it, so every position is a pure function of idx
-//      (bit-identical on replay).  Token-major outputs (pos, send_row_of) are
-//      staged in shared memory and written as one contiguous run per tile;
-//      receive-row and send-row outputs are written column by column, the
-//      j-th set bit of a column going to its j-th row, so those writes are
-//      contiguous runs as well.
+//      (bit-identical on replay).  The tile's entries are counting-sorted in
+//      shared memory by column (slot = the column's segment start in the
+//      tile + the entry's rank), and the receive-row and send-row outputs are
+//      then copied out as one contiguous run of rows per column.
 //
 // Masks are stored word-major with an odd row stride ([word][col], stride
 // cols | 1) so that the lanes of a warp, which share a word index and differ in
@@ -184,29 +183,41 @@ __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a)
 
 // shared memory of the scatter kernel, in order
 struct ScatterSmem {
-  int cols, cp, K;
+  int cols, cp, K, KR;  // KR = min(K, R): send entries per token at most
   __host__ __device__ size_t masks() const { return 0; }
   __host__ __device__ size_t pre() const { return masks() + sizeof(uint32_t) * kWords * cp; }
-  __host__ __device__ size_t idx() const { return align(pre() + sizeof(uint16_t) * kWords * cp); }
-  __host__ __device__ size_t stage() const { return idx() + sizeof(int32_t) * kTile * K; }
-  __host__ __device__ size_t base() const { return stage() + 2 * sizeof(int32_t) * kTile * K; }
+  __host__ __device__ size_t seg() const { return align(pre() + sizeof(uint16_t) * kWords * cp); }
+  __host__ __device__ size_t srow() const { return seg() + sizeof(int32_t) * (cols + 2); }
+  __host__ __device__ size_t rst() const { return srow() + sizeof(int32_t) * kTile * K; }
+  __host__ __device__ size_t sst() const { return rst() + sizeof(uint32_t) * kTile * K; }
+  __host__ __device__ size_t base() const { return sst() + sizeof(uint32_t) * kTile * KR; }
   __host__ __device__ size_t off() const { return base() + sizeof(int32_t) * cols; }
   __host__ __device__ size_t bytes() const { return off() + sizeof(int32_t) * (cols + 2); }
   __host__ __device__ static size_t align(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
 };
 
+// packed staging entries (expert < 512, k < 16, token in tile < 1024)
+__device__ __forceinline__ uint32_t pack_recv(int e, int k, int tl) {
+  return static_cast<uint32_t>(e) | (static_cast<uint32_t>(k) << 9) | (static_cast<uint32_t>(tl) << 13);
+}
+__device__ __forceinline__ uint32_t pack_send(int r, int tl) {
+  return static_cast<uint32_t>(r) | (static_cast<uint32_t>(tl) << 9);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs a) {
   extern __shared__ __align__(16) uint8_t ssm[];
   const int cols = a.E + a.R;
   const int cp = col_stride(cols);
-  const ScatterSmem L{cols, cp, a.K};
+  const int KR = a.K < a.R ? a.K : a.R;
+  const ScatterSmem L{cols, cp, a.K, KR};
   uint32_t* masks = reinterpret_cast<uint32_t*>(ssm + L.masks());  // [kWords][cp]
   uint16_t* pre = reinterpret_cast<uint16_t*>(ssm + L.pre());      // [kWords][cp]
-  int32_t* idx_s = reinterpret_cast<int32_t*>(ssm + L.idx());      // [kTile][K]
-  int32_t* pos_s = reinterpret_cast<int32_t*>(ssm + L.stage());    // [kTile][K]
-  int32_t* srow_s = pos_s + kTile * a.K;                           // [kTile][K]
+  int32_t* seg = reinterpret_cast<int32_t*>(ssm + L.seg());        // seg_e[E+1] | seg_r[R+1]
+  int32_t* srow_s = reinterpret_cast<int32_t*>(ssm + L.srow());    // [kTile][K]
+  uint32_t* rst = reinterpret_cast<uint32_t*>(ssm + L.rst());      // receive entries, by column
+  uint32_t* sst = reinterpret_cast<uint32_t*>(ssm + L.sst());      // send entries, by column
   int32_t* base = reinterpret_cast<int32_t*>(ssm + L.base());      // [cols] tile bases
-  int32_t* off = reinterpret_cast<int32_t*>(ssm + L.off());        // off_e[E+1], off_s[R+1]
+  int32_t* off = reinterpret_cast<int32_t*>(ssm + L.off());        // off_e[E+1] | off_s[R+1]
   const int tile = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_t0 = tile * kTile;
@@ -224,9 +235,10 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   __syncthreads();
   const int t = tile_t0 + threadIdx.x;
   int ek[MOE_MAX_TOPK];
-  const uint32_t valid = mark_token(a, t, masks, cp, idx_s, ek);
+  const uint32_t valid = mark_token(a, t, masks, cp, nullptr, ek);
   __syncthreads();
-  // exclusive prefix of the popcounts over the words of each column
+  // exclusive prefix of the popcounts over the words of each column; the
+  // column's count in this tile goes to seg (scanned below)
   for (int col = threadIdx.x; col < cols; col += kThreads) {
     int run = 0;
 #pragma unroll 8
@@ -234,17 +246,45 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
       pre[w * cp + col] = static_cast<uint16_t>(run);
       run += __popc(masks[w * cp + col]);
     }
+    seg[col + (col >= a.E ? 1 : 0)] = run;
+  }
+  __syncthreads();
+  if (warp < 2) {
+    // exclusive scan of the tile's column counts: warp 0 experts, warp 1 ranks
+    const int n = warp == 0 ? a.E : a.R;
+    int32_t* v = seg + (warp == 0 ? 0 : a.E + 1);
+    const int per = (n + 31) / 32;
+    const int lo = lane * per, hi = min(n, lo + per);
+    int local = 0;
+    for (int i = lo; i < hi; ++i) local += v[i];
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    int run = incl - local;
+    for (int i = lo; i < hi; ++i) {
+      const int c = v[i];
+      v[i] = run;
+      run += c;
+    }
+    if (lane == 31) v[n] = incl;
   }
   __syncthreads();
 
   const int32_t* off_e = off;
   const int32_t* off_s = off + a.E + 1;
+  const int32_t* seg_e = seg;
+  const int32_t* seg_r = seg + a.E + 1;
   const int n_recv_rows = a.T * a.K;
-  const int n_send_rows = a.T * (a.K < a.R ? a.K : a.R);
+  const int n_send_rows = a.T * KR;
   const uint32_t lt = lanemask_lt();
 
-  // token-major: pos[t,k] and send_row_of[t,k], staged then written as one run
+  // token pass: positions, and the tile's counting sort into the staging
+  // arrays (an entry's slot is its column's segment start plus its rank)
   if (t < a.T) {
+    int32_t* pos_g = a.pos + static_cast<size_t>(t) * a.K;
 #pragma unroll
     for (int k = 0; k < MOE_MAX_TOPK; ++k) {
       if (k >= a.K) break;
@@ -254,70 +294,66 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
         const int r = e / a.epr;
         const int ce = warp * cp + e;
         const int cr = warp * cp + a.E + r;
-        p = off_e[e] + base[e] + pre[ce] + __popc(masks[ce] & lt);
-        srow = off_s[r] + base[a.E + r] + pre[cr] + __popc(masks[cr] & lt);
+        const int rank_e = pre[ce] + __popc(masks[ce] & lt);
+        const int rank_r = pre[cr] + __popc(masks[cr] & lt);
+        p = off_e[e] + base[e] + rank_e;
+        srow = off_s[r] + base[a.E + r] + rank_r;
         // the scan guarantees p < T*K and srow < S; a violation (inconsistent
         // counts) is reported and the entry dropped instead of written
         if (p < 0 || p >= n_recv_rows || srow < 0 || srow >= n_send_rows) {
           raise_flag(a.flags, MOE_DEVERR_INTERNAL);
           p = -1;
           srow = -1;
+        } else {
+          rst[seg_e[e] + rank_e] = pack_recv(e, k, threadIdx.x);
+          bool first = true;
+#pragma unroll
+          for (int j = 0; j < MOE_MAX_TOPK; ++j) {
+            if (j >= k) break;
+            if (((valid >> j) & 1u) && ek[j] / a.epr == r) first = false;
+          }
+          if (first) sst[seg_r[r] + rank_r] = pack_send(r, threadIdx.x);
         }
       }
-      pos_s[threadIdx.x * a.K + k] = p;
+      pos_g[k] = p;
       srow_s[threadIdx.x * a.K + k] = srow;
     }
   }
   __syncthreads();
+
+  // copy-out: send_row_of (token-major), then receive and send entries, each
+  // a run of consecutive rows per column
   {
     const int n = tile_n * a.K;
-    int32_t* pos_g = a.pos + static_cast<size_t>(tile_t0) * a.K;
     int32_t* srow_g = a.send_row_of + static_cast<size_t>(tile_t0) * a.K;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      pos_g[i] = pos_s[i];
-      srow_g[i] = srow_s[i];
-    }
+    for (int i = threadIdx.x; i < n; i += kThreads) srow_g[i] = srow_s[i];
   }
-
-  // column-major: the j-th token of a column within the tile goes to the
-  // column's j-th row of this tile
-  for (int col = warp; col < cols; col += kWarps) {
-    const int last = (kWords - 1) * cp + col;
-    const int n = pre[last] + __popc(masks[last]);
-    const bool is_rank = col >= a.E;
-    const int row0 = (is_rank ? off_s[col - a.E] : off_e[col]) + base[col];
-    for (int j0 = 0; j0 < n; j0 += 32) {
-      const int j = j0 + lane;
-      if (j >= n) break;
-      int lo = 0, hi = kWords - 1;  // largest word w with pre[w] <= j
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (pre[mid * cp + col] <= j) lo = mid; else hi = mid - 1;
-      }
-      const uint32_t m = masks[lo * cp + col];
-      const int bit = static_cast<int>(__fns(m, 0, j - pre[lo * cp + col] + 1));
-      if (bit < 0) {  // cannot happen for j < n; reported rather than used
-        raise_flag(a.flags, MOE_DEVERR_INTERNAL);
-        continue;
-      }
-      const int tl = lo * 32 + bit;
-      const int row = row0 + j;
-      if (is_rank) {
-        if (row >= 0 && row < n_send_rows) a.send_token[row] = tile_t0 + tl;
-        else raise_flag(a.flags, MOE_DEVERR_INTERNAL);
-        continue;
-      }
-      if (row < 0 || row >= n_recv_rows) {
-        raise_flag(a.flags, MOE_DEVERR_INTERNAL);
-        continue;
-      }
-      int k = 0;
-      for (int kk = a.K - 1; kk >= 0; --kk)  // first (valid) entry of this expert
-        if (idx_s[tl * a.K + kk] == col) k = kk;
-      a.recv_token[row] = tile_t0 + tl;
-      a.recv_k[row] = k;
-      a.recv_send_row[row] = srow_s[tl * a.K + k];
+  for (int i = threadIdx.x; i < seg_e[a.E]; i += kThreads) {
+    const uint32_t u = rst[i];
+    const int e = u & 511u, k = (u >> 9) & 15u, tl = u >> 13;
+    // a slot left empty by a dropped inconsistent entry holds stale data
+    if (e >= a.E || k >= a.K || tl >= tile_n) {
+      raise_flag(a.flags, MOE_DEVERR_INTERNAL);
+      continue;
     }
+    const int row = off_e[e] + base[e] + (i - seg_e[e]);
+    if (row < 0 || row >= n_recv_rows) {
+      raise_flag(a.flags, MOE_DEVERR_INTERNAL);
+      continue;
+    }
+    a.recv_token[row] = tile_t0 + tl;
+    a.recv_k[row] = k;
+    a.recv_send_row[row] = srow_s[tl * a.K + k];
+  }
+  for (int i = threadIdx.x; i < seg_r[a.R]; i += kThreads) {
+    const uint32_t u = sst[i];
+    const int r = u & 511u, tl = u >> 9;
+    const int row = r < a.R ? off_s[r] + base[a.E + r] + (i - seg_r[r]) : -1;
+    if (tl >= tile_n || row < 0 || row >= n_send_rows) {
+      raise_flag(a.flags, MOE_DEVERR_INTERNAL);
+      continue;
+    }
+    a.send_token[row] = tile_t0 + tl;
   }
 
   // tails: receive rows past off_e[E] and send rows past S
@@ -333,12 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
 
 size_t count_smem(int cols) { return static_cast<size_t>(kWords) * col_stride(cols) * sizeof(uint32_t); }
 
-size_t scatter_smem(int cols, int K) { return ScatterSmem{cols, col_stride(cols), K}.bytes(); }
+size_t scatter_smem(int cols, int K, int R) {
+  return ScatterSmem{cols, col_stride(cols), K, K < R ? K : R}.bytes();
+}
 
 }  // namespace
 
 size_t layout_smem_bytes(int E, int R) {
-  const size_t a = count_smem(E + R), b = scatter_smem(E + R, MOE_MAX_TOPK);
+  const size_t a = count_smem(E + R), b = scatter_smem(E + R, MOE_MAX_TOPK, R);
   return a > b ? a : b;
 }
 
@@ -388,7 +426,7 @@ cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T
   layout_count_kernel<<<a.ntiles, kThreads, count_smem(cols), s>>>(a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  layout_scatter_kernel<<<a.ntiles, kThreads, scatter_smem(cols, a.K), s>>>(a);
+  layout_scatter_kernel<<<a.ntiles, kThreads, scatter_smem(cols, a.K, a.R), s>>>(a);
   return cudaGetLastError();
 }
 

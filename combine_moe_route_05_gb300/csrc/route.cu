@@ -265,71 +265,72 @@ __device__ void softmax_token_full(const RouteArgs& a, int t, int lane, const fl
 // ---------------------------------------------------------------------------
 // fp32 selection of one token; returns false if it cannot be trusted (the
 // caller then recomputes the token in fp64).  On success, lane base + k holds
-// the k-th selected expert and its logit.
+// the k-th selected expert.
+//
+// Each lane first sorts its VPL (key, j) pairs by key, descending, with a
+// stable odd-even transposition network (equal keys keep ascending j), so a
+// selection round only compares the lanes' heads: the largest head wins,
+// equal heads go to the lowest lane, which holds the lower expert indices.
 
-// Top-GK values of a lane's VPL values, merged across the L lanes of a group
-// (butterfly over lane bits 1..L/2), summed in descending order.
-template <int VPL, int GKMAX>
-__device__ __forceinline__ float group_score_fp32(const float (&key)[VPL], int gk, int lanes) {
-  float top[GKMAX];
+__device__ __forceinline__ float unorder_key(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
+template <int VPL>
+__device__ __forceinline__ void sort_desc(float (&k)[VPL], int (&j)[VPL]) {
 #pragma unroll
-  for (int i = 0; i < GKMAX; ++i) top[i] = -INFINITY;
+  for (int pass = 0; pass < VPL; ++pass) {
 #pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    float x = key[j];
-#pragma unroll
-    for (int i = 0; i < GKMAX; ++i) {
-      if (x > top[i]) {
-        const float y = top[i];
-        top[i] = x;
-        x = y;
+    for (int i = pass & 1; i + 1 < VPL; i += 2) {
+      if (k[i] < k[i + 1]) {
+        const float tk = k[i];
+        k[i] = k[i + 1];
+        k[i + 1] = tk;
+        const int tj = j[i];
+        j[i] = j[i + 1];
+        j[i + 1] = tj;
       }
     }
   }
+}
+
+// Sum of the top two (or top one) keys of a group whose keys are spread over
+// L lanes (each lane's list sorted), merged over lane bits 1..L/2.
+__device__ __forceinline__ float group_top2_fp32(float t0, float t1, int gk, int lanes) {
   for (int off = 1; off < lanes; off <<= 1) {
-    float other[GKMAX];
-#pragma unroll
-    for (int i = 0; i < GKMAX; ++i) other[i] = __shfl_xor_sync(kFull, top[i], off);
-#pragma unroll
-    for (int i2 = 0; i2 < GKMAX; ++i2) {
-      float x = other[i2];
-#pragma unroll
-      for (int i = 0; i < GKMAX; ++i) {
-        if (x > top[i]) {
-          const float y = top[i];
-          top[i] = x;
-          x = y;
-        }
-      }
-    }
+    const float o0 = __shfl_xor_sync(kFull, t0, off);
+    const float o1 = __shfl_xor_sync(kFull, t1, off);
+    const float n0 = fmaxf(t0, o0);
+    const float n1 = fmaxf(fminf(t0, o0), fmaxf(t1, o1));
+    t0 = n0;
+    t1 = n1;
   }
-  float sum = 0.0f;
-#pragma unroll
-  for (int i = 0; i < GKMAX; ++i)
-    if (i < gk) sum = __fadd_rn(sum, top[i]);
-  return sum;
+  return gk >= 2 ? __fadd_rn(__fadd_rn(0.0f, t0), t1) : t0;
 }
 
 template <int VPL, bool SIGMOID>
 __device__ __forceinline__ bool select_fp32(const RouteArgs& a, int lane, const float (&v)[VPL],
-                                            int base, int& my_idx, float& my_logit) {
-  float key[VPL];
+                                            int base, int& my_idx) {
+  float sk[VPL];
+  int sj[VPL];
   float maxabs = 0.0f;
-  if (SIGMOID) {
+  int n_valid = 0;  // experts of this lane below E
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int e = lane * VPL + j;
-      if (e < a.E) {
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane * VPL + j;
+    sj[j] = j;
+    if (e < a.E) {
+      ++n_valid;
+      if (SIGMOID) {
         const float s = __frcp_rn(__fadd_rn(1.0f, expf(-v[j])));
-        key[j] = __fadd_rn(s, a.bias ? __ldg(a.bias + e) : 0.0f);
-        maxabs = fmaxf(maxabs, fabsf(key[j]));
+        sk[j] = __fadd_rn(s, a.bias ? __ldg(a.bias + e) : 0.0f);
+        maxabs = fmaxf(maxabs, fabsf(sk[j]));
       } else {
-        key[j] = -INFINITY;
+        sk[j] = v[j];
       }
+    } else {
+      sk[j] = -INFINITY;
     }
-  } else {
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) key[j] = v[j];
   }
   float delta = 0.0f;
   if (SIGMOID) {
@@ -338,18 +339,20 @@ __device__ __forceinline__ bool select_fp32(const RouteArgs& a, int lane, const 
     delta = kDeltaAbs + kDeltaRel * maxabs;
     if (!(delta < 1e-3f)) return false;  // huge or non-finite keys
   }
+  sort_desc<VPL>(sk, sj);
 
   // groups (sigmoid only): lanes of a group are contiguous and L = gsz / VPL
   bool eligible_lane = lane * VPL < a.E;
   if (SIGMOID && a.G > 1) {
     const int gsz = a.E / a.G;
     const int L = gsz / VPL;
-    const float gs = group_score_fp32<VPL, 2>(key, a.GK, L);
+    const float gs = group_top2_fp32(sk[0], VPL > 1 ? sk[VPL > 1 ? 1 : 0] : -INFINITY, a.GK, L);
     // lane g < G holds group g's score; TG + 1 rounds of warp arg-max, ties
     // to the lower group
     const bool glane = lane < a.G;
     const float my_gs = __shfl_sync(kFull, gs, (lane * L) & 31);
-    const float gmax = __uint_as_float(__reduce_max_sync(kFull, glane ? __float_as_uint(fabsf(my_gs)) : 0u));
+    const float gmax =
+        __uint_as_float(__reduce_max_sync(kFull, glane ? __float_as_uint(fabsf(my_gs)) : 0u));
     uint32_t keep = 0;
     float last = 0.0f, next = -INFINITY;
     const int rounds = a.TG < a.G ? a.TG + 1 : a.TG;
@@ -358,7 +361,7 @@ __device__ __forceinline__ bool select_fp32(const RouteArgs& a, int lane, const 
       const uint32_t bits = cand ? order_key(my_gs) : 0u;
       const uint32_t best = __reduce_max_sync(kFull, bits);
       const int wl = __ffs(__ballot_sync(kFull, cand && bits == best)) - 1;
-      const float val = __shfl_sync(kFull, my_gs, wl & 31);
+      const float val = unorder_key(best);
       if (r < a.TG) {
         keep |= 1u << wl;
         last = val;
@@ -371,43 +374,30 @@ __device__ __forceinline__ bool select_fp32(const RouteArgs& a, int lane, const 
     eligible_lane = eligible_lane && ((keep >> ((lane * VPL) / gsz)) & 1u);
   }
 
-  // K + 1 rounds of warp arg-max over the eligible keys
-  uint32_t taken = 0;
+  // K (+1 for the gap check) rounds over the lanes' heads
+  int consumed = 0;
   float prev = 0.0f;
   const int n_elig = SIGMOID && a.G > 1 ? a.TG * (a.E / a.G) : a.E;
   const int rounds = SIGMOID ? (a.K < n_elig ? a.K + 1 : a.K) : a.K;
   for (int k = 0; k < rounds; ++k) {
-    float bv = -INFINITY;
-    int bj = -1;
-    if (eligible_lane) {
+    const bool have = eligible_lane && consumed < n_valid;
+    const uint32_t bits = have ? order_key(sk[0]) : 0u;
+    const uint32_t best = __reduce_max_sync(kFull, bits);
+    const int wl = __ffs(__ballot_sync(kFull, have && bits == best)) - 1;
+    const int wj = __shfl_sync(kFull, sj[0], wl & 31);
+    const float wv = unorder_key(best);
+    if (lane == wl) {
 #pragma unroll
-      for (int j = 0; j < VPL; ++j)
-        if (!((taken >> j) & 1u) && lane * VPL + j < a.E && (bj < 0 || key[j] > bv)) {
-          bv = key[j];
-          bj = j;
-        }
+      for (int i = 0; i + 1 < VPL; ++i) {
+        sk[i] = sk[i + 1];
+        sj[i] = sj[i + 1];
+      }
+      sk[VPL - 1] = -INFINITY;
+      ++consumed;
     }
-    const uint32_t ok_bits = bj >= 0 ? order_key(bv) : 0u;
-    const uint32_t best = __reduce_max_sync(kFull, ok_bits);
-    const uint32_t who = __ballot_sync(kFull, bj >= 0 && ok_bits == best);
-    const int wl = __ffs(who) - 1;
-    const int wj = __shfl_sync(kFull, bj, wl);
-    const float wv = __shfl_sync(kFull, bv, wl);
-    if (lane == wl) taken |= 1u << wj;
     if (SIGMOID && k > 0 && !(prev - wv > 2.0f * delta)) return false;
     prev = wv;
-    if (k < a.K) {
-      // the selected expert's logit, from its owner lane
-      float lg = 0.0f;
-#pragma unroll
-      for (int j = 0; j < VPL; ++j)
-        if (j == wj) lg = v[j];
-      lg = __shfl_sync(kFull, lg, wl);
-      if (lane == base + k) {
-        my_idx = wl * VPL + wj;
-        my_logit = lg;
-      }
-    }
+    if (k < a.K && lane == base + k) my_idx = wl * VPL + wj;
   }
   return true;
 }
@@ -434,12 +424,11 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
       // sigmoid token with a non-finite logit goes to the fp64 path
       const bool use_fast = a.fast && !(SIGMOID && __any_sync(kFull, bad));
       int sel_idx = 0;
-      float sel_logit = 0.0f;
-      const bool ok = use_fast && select_fp32<VPL, SIGMOID>(a, lane, v, j * a.K, sel_idx, sel_logit);
+      const bool ok = use_fast && select_fp32<VPL, SIGMOID>(a, lane, v, j * a.K, sel_idx);
       if (ok) {
         if (j_of_lane == j) {
           my_idx = sel_idx;
-          my_logit = sel_logit;
+          my_logit = __ldg(a.logits + static_cast<size_t>(t) * a.E + sel_idx);
           my_fast = true;
         }
       } else if (SIGMOID) {
