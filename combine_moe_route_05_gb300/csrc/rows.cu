@@ -1,12 +1,14 @@
 // Row movement kernels of the MoE path (sm_103a): dispatch, combine, their
 // backward passes, and the router-score absorption scaling.
 //
-// dispatch: token-major.  Each token row of x is read from HBM once with a
-//   bulk (TMA) copy into a shared-memory slot and written from there to its K
-//   expert-grouped receive rows (and its deduplicated send rows) with bulk
-//   stores, so a row is never expanded to [T*K,H] by a separate pass
-//   (DeepSpeed "Add an opt-in DeepEP transport ...", "Why": tokens are taken
-//   before top-k expansion and replicated by the dispatch itself).
+// dispatch: token-major, one block per token.  Each 16-byte vector of a
+//   token row is read from HBM once and stored to the token's K
+//   expert-grouped receive rows (and its deduplicated send rows), so a row is
+//   never expanded to [T*K,H] by a separate pass (DeepSpeed "Add an opt-in
+//   DeepEP transport ...", "Why": tokens are taken before top-k expansion and
+//   replicated by the dispatch itself).  Plain vector stores from many warps
+//   keep more writes in flight than bulk (TMA) stores from shared memory did
+//   for this one-read, K-write pattern.
 // combine / dispatch backward: token-major gather of the K rows of a token
 //   with 16-byte streaming loads, fp32 accumulation in k order (fused
 //   multiply-add for the weighted sum), one rounding to the row dtype.
@@ -25,122 +27,64 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 
 // ---------------------------------------------------------------------------
-// dispatch: bulk copies through shared memory
-
-constexpr int kSlots = 4;          // shared-memory row slots per block
-constexpr int kAhead = 2;          // loads issued ahead of the one consumed
-constexpr uint32_t kChunkMax = 16384;  // bytes per bulk copy
-constexpr uint32_t kWaitPolls = 1u << 22;
-static_assert(kAhead < kSlots, "slots must outnumber loads in flight");
+// dispatch: one block per token, 16-byte vectors, each row vector read once
+// and stored to the token's K receive rows (and its deduplicated send rows)
 
 struct DispatchArgs {
   const uint8_t* x;
   int64_t row_bytes;
+  int nvec;
   int T, K;
-  uint32_t chunk;
-  int nchunk;
   const int32_t* pos;
   const float* w;
   const int32_t* send_row_of;
   uint8_t* recv;
   float* recv_w;
   uint8_t* send;
-  uint32_t* flags;
 };
 
-__global__ void __launch_bounds__(32) dispatch_bulk_kernel(DispatchArgs a) {
-  extern __shared__ __align__(128) uint8_t dsm[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(dsm);
-  uint8_t* slots = dsm + 128;
-  const int lane = threadIdx.x;
-  const long long units = static_cast<long long>(a.T) * a.nchunk;
-  const long long first = blockIdx.x, stride = gridDim.x;
-  const long long n_my = first < units ? (units - first + stride - 1) / stride : 0;
-  if (lane == 0) {
-    for (int s = 0; s < kSlots; ++s) mbar_init(&bar[s], 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-
-  long long issued = 0;  // lane 0: units whose load has been issued
-  auto issue = [&](long long i) {
-    const long long u = first + i * stride;
-    const long long t = u / a.nchunk;
-    const uint32_t off = static_cast<uint32_t>(u % a.nchunk) * a.chunk;
-    const uint32_t bytes = static_cast<uint32_t>(
-        a.row_bytes - off < static_cast<int64_t>(a.chunk) ? a.row_bytes - off : a.chunk);
-    uint64_t* b = &bar[i % kSlots];
-    mbar_arrive_expect_tx(b, bytes);
-    bulk_load(slots + (i % kSlots) * a.chunk, a.x + t * a.row_bytes + off, bytes, b);
-  };
-  if (lane == 0)
-    for (; issued < kAhead && issued < n_my; ++issued) issue(issued);
-
-  bool ok = true;
-  long long i = 0;
-  for (; i < n_my; ++i) {
-    const long long u = first + i * stride;
-    const long long t = u / a.nchunk;
-    const int c = static_cast<int>(u % a.nchunk);
-    const uint32_t off = static_cast<uint32_t>(c) * a.chunk;
-    const uint32_t bytes = static_cast<uint32_t>(
-        a.row_bytes - off < static_cast<int64_t>(a.chunk) ? a.row_bytes - off : a.chunk);
-
-    int p = -1, srow = -1;
-    if (lane < a.K) {
-      p = __ldg(a.pos + t * a.K + lane);
-      if (a.send) srow = __ldg(a.send_row_of + t * a.K + lane);
-      if (c == 0 && a.recv_w && p >= 0) a.recv_w[p] = __ldg(a.w + t * a.K + lane);
-    }
-    // a send row is written once, by the lowest k that maps to it
-    const uint32_t same = __match_any_sync(kFull, srow);
-    const bool send_first = a.send && lane < a.K && srow >= 0 && (__ffs(same) - 1) == lane;
-    const uint32_t send_mask = __ballot_sync(kFull, send_first);
-
-    if (lane == 0 && !mbar_wait_bounded(&bar[i % kSlots], static_cast<uint32_t>((i / kSlots) & 1),
-                                        kWaitPolls)) {
-      raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
-      ok = false;
-    }
-    ok = __shfl_sync(kFull, ok, 0);
-    if (!ok) break;
-
-    const uint8_t* src = slots + (i % kSlots) * a.chunk;
-    for (int k = 0; k < a.K; ++k) {
-      const int pk = __shfl_sync(kFull, p, k);
-      const int sk = __shfl_sync(kFull, srow, k);
-      if (lane == 0) {
-        if (pk >= 0) bulk_store(a.recv + static_cast<int64_t>(pk) * a.row_bytes + off, src, bytes);
-        if ((send_mask >> k) & 1u)
-          bulk_store(a.send + static_cast<int64_t>(sk) * a.row_bytes + off, src, bytes);
+template <int KMAX>
+__global__ void __launch_bounds__(1024) dispatch_kernel(DispatchArgs a) {
+  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+    int p[KMAX], srow[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      p[k] = -1;
+      srow[k] = -1;
+      if (k < a.K) {
+        p[k] = __ldg(a.pos + static_cast<size_t>(t) * a.K + k);
+        if (a.send) srow[k] = __ldg(a.send_row_of + static_cast<size_t>(t) * a.K + k);
       }
     }
-    if (lane == 0) {
-      bulk_commit();
-      if (issued < n_my) {
-        // the slot of unit `issued` was last read by unit issued - kSlots,
-        // whose stores are among the groups older than the newest
-        // kSlots - kAhead
-        bulk_wait_read<kSlots - kAhead>();
-        issue(issued);
-        ++issued;
+    if (a.send) {
+      // a send row is written once, by the lowest k that maps to it
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+#pragma unroll
+        for (int j = 0; j < k; ++j)
+          if (srow[j] == srow[k]) srow[k] = -1;
+    }
+    if (a.recv_w && threadIdx.x < a.K) {
+      const int pk = __ldg(a.pos + static_cast<size_t>(t) * a.K + threadIdx.x);
+      if (pk >= 0) a.recv_w[pk] = __ldg(a.w + static_cast<size_t>(t) * a.K + threadIdx.x);
+    }
+    const uint8_t* xrow = a.x + static_cast<int64_t>(t) * a.row_bytes;
+    for (int v = threadIdx.x; v < a.nvec; v += blockDim.x) {
+      const Vec16 val = ld_stream(xrow + v * 16);
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        if (p[k] >= 0) st_vec(a.recv + static_cast<int64_t>(p[k]) * a.row_bytes + v * 16, val);
+        if (srow[k] >= 0) st_vec(a.send + static_cast<int64_t>(srow[k]) * a.row_bytes + v * 16, val);
       }
     }
-  }
-  if (lane == 0) {
-    if (!ok) {
-      // drain the loads still in flight before shared memory goes away
-      for (long long q = i + 1; q < issued; ++q)
-        mbar_wait_bounded(&bar[q % kSlots], static_cast<uint32_t>((q / kSlots) & 1), kWaitPolls);
-    }
-    bulk_wait_all();
   }
 }
 
 // ---------------------------------------------------------------------------
 // combine / dispatch backward: out[t] = round(sum_k w_k * y[pos[t,k]])
 
-constexpr int kRowThreads = 256;
+constexpr int kRowThreads = 256;      // elementwise and per-entry kernels
+constexpr int kGatherMaxThreads = 512; // combine-type kernels: about 2 vectors per thread
 
 template <typename Elt>
 struct RowArgs {
@@ -170,7 +114,7 @@ __device__ __forceinline__ void load_entries(const int32_t* pos, const float* w,
 }
 
 template <typename Elt, int KMAX, bool WEIGHTED>
-__global__ void __launch_bounds__(kRowThreads) combine_kernel(RowArgs<Elt> a) {
+__global__ void __launch_bounds__(kGatherMaxThreads) combine_kernel(RowArgs<Elt> a) {
   using VT = VecTraits<Elt>;
   constexpr int N = VT::N;
   for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
@@ -178,7 +122,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(RowArgs<Elt> a) {
     float wk[KMAX];
     load_entries<KMAX>(a.pos, WEIGHTED ? a.w : nullptr, t, a.K, p, wk);
     uint8_t* orow = a.out + static_cast<int64_t>(t) * a.row_bytes;
-    for (int v = threadIdx.x; v < a.nvec; v += kRowThreads) {
+    for (int v = threadIdx.x; v < a.nvec; v += blockDim.x) {
       Vec16 in[KMAX];
 #pragma unroll
       for (int k = 0; k < KMAX; ++k)
@@ -203,11 +147,11 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(RowArgs<Elt> a) {
 // combine backward: gy[pos[t,k]] = round(w_k * g[t]) (or g[t]), and
 // gw[t,k] = <g[t], y[pos[t,k]]> reduced over the block in a fixed order.
 template <typename Elt, int KMAX, bool WEIGHTED, bool DOT>
-__global__ void __launch_bounds__(kRowThreads) combine_bwd_kernel(RowArgs<Elt> a) {
+__global__ void __launch_bounds__(kGatherMaxThreads, 2) combine_bwd_kernel(RowArgs<Elt> a) {
   using VT = VecTraits<Elt>;
   constexpr int N = VT::N;
-  constexpr int kW = kRowThreads / 32;
-  __shared__ float red[2][kW][KMAX];
+  __shared__ float red[2][kGatherMaxThreads / 32][KMAX];
+  const int nw = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int it = 0;
   for (int t = blockIdx.x; t < a.T; t += gridDim.x, ++it) {
@@ -218,7 +162,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_bwd_kernel(RowArgs<Elt> a
 #pragma unroll
     for (int k = 0; k < KMAX; ++k) dot[k] = 0.0f;
     const uint8_t* grow = a.g + static_cast<int64_t>(t) * a.row_bytes;
-    for (int v = threadIdx.x; v < a.nvec; v += kRowThreads) {
+    for (int v = threadIdx.x; v < a.nvec; v += blockDim.x) {
       const Vec16 gv = ld_stream(grow + v * 16);
       Vec16 yv[KMAX];
       if (DOT) {
@@ -261,8 +205,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_bwd_kernel(RowArgs<Elt> a
       __syncthreads();
       if (threadIdx.x < a.K) {
         float s = 0.0f;
-#pragma unroll
-        for (int wi = 0; wi < kW; ++wi) s += red[it & 1][wi][threadIdx.x];
+        for (int wi = 0; wi < nw; ++wi) s += red[it & 1][wi][threadIdx.x];
         int pk = __ldg(a.pos + static_cast<size_t>(t) * a.K + threadIdx.x);
         a.gw[static_cast<size_t>(t) * a.K + threadIdx.x] = pk >= 0 ? s : 0.0f;
       }
@@ -331,6 +274,14 @@ __global__ void __launch_bounds__(kRowThreads) scale_rows_bwd_kernel(
   }
 }
 
+// Threads per block for rows of nvec 16-byte vectors, `per` vectors per
+// thread: whole warps, at most 1024.
+int threads_for(int nvec, int per) {
+  int t = (nvec + per - 1) / per;
+  t = (t + 31) / 32 * 32;
+  return t < 32 ? 32 : (t > 1024 ? 1024 : t);
+}
+
 // Resident blocks per SM of `kernel`, computed once per (kernel, smem) pair.
 int blocks_per_sm(const void* kernel, int threads, size_t smem) {
   struct Entry {
@@ -362,6 +313,11 @@ int grid_for(const void* kernel, int threads, size_t smem, int num_sms, long lon
   return static_cast<int>(g < 1 ? 1 : g);
 }
 
+int gather_threads(int nvec) {
+  const int t = threads_for(nvec, 2);
+  return t > kGatherMaxThreads ? kGatherMaxThreads : t;
+}
+
 template <typename Elt, int KMAX>
 cudaError_t launch_combine_t(const moe_handle* h, const void* y, int H, const float* w, void* out,
                              cudaStream_t s) {
@@ -375,12 +331,13 @@ cudaError_t launch_combine_t(const moe_handle* h, const void* y, int H, const fl
   a.T = h->T;
   a.K = h->cfg.top_k;
   if (a.T == 0) return cudaSuccess;
+  const int block = gather_threads(a.nvec);
   if (w) {
     auto k = combine_kernel<Elt, KMAX, true>;
-    k<<<grid_for(reinterpret_cast<const void*>(k), kRowThreads, 0, h->num_sms, a.T), kRowThreads, 0, s>>>(a);
+    k<<<grid_for(reinterpret_cast<const void*>(k), block, 0, h->num_sms, a.T), block, 0, s>>>(a);
   } else {
     auto k = combine_kernel<Elt, KMAX, false>;
-    k<<<grid_for(reinterpret_cast<const void*>(k), kRowThreads, 0, h->num_sms, a.T), kRowThreads, 0, s>>>(a);
+    k<<<grid_for(reinterpret_cast<const void*>(k), block, 0, h->num_sms, a.T), block, 0, s>>>(a);
   }
   return cudaGetLastError();
 }
@@ -400,56 +357,52 @@ cudaError_t launch_combine_bwd_t(const moe_handle* h, const void* g, const void*
   a.T = h->T;
   a.K = h->cfg.top_k;
   if (a.T == 0) return cudaSuccess;
+  const int block = gather_threads(a.nvec);
   const void* kp;
   if (w && gw) {
     auto k = combine_bwd_kernel<Elt, KMAX, true, true>;
     kp = reinterpret_cast<const void*>(k);
-    k<<<grid_for(kp, kRowThreads, 0, h->num_sms, a.T), kRowThreads, 0, s>>>(a);
+    k<<<grid_for(kp, block, 0, h->num_sms, a.T), block, 0, s>>>(a);
   } else if (w) {
     auto k = combine_bwd_kernel<Elt, KMAX, true, false>;
     kp = reinterpret_cast<const void*>(k);
-    k<<<grid_for(kp, kRowThreads, 0, h->num_sms, a.T), kRowThreads, 0, s>>>(a);
+    k<<<grid_for(kp, block, 0, h->num_sms, a.T), block, 0, s>>>(a);
   } else {
     auto k = combine_bwd_kernel<Elt, KMAX, false, false>;
     kp = reinterpret_cast<const void*>(k);
-    k<<<grid_for(kp, kRowThreads, 0, h->num_sms, a.T), kRowThreads, 0, s>>>(a);
+    k<<<grid_for(kp, block, 0, h->num_sms, a.T), block, 0, s>>>(a);
   }
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t dispatch_smem_bytes(int64_t row_bytes) {
-  const uint32_t chunk = row_bytes < kChunkMax ? static_cast<uint32_t>(row_bytes) : kChunkMax;
-  return 128 + static_cast<size_t>(kSlots) * chunk;
-}
-
-cudaError_t prepare_dispatch_kernel() {
-  return cudaFuncSetAttribute(dispatch_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(128 + kSlots * kChunkMax));
-}
+cudaError_t prepare_dispatch_kernel() { return cudaSuccess; }
 
 cudaError_t launch_dispatch(const moe_handle* h, const void* x, int64_t row_bytes, const float* w,
                             void* recv, float* recv_w, void* send, cudaStream_t s) {
   DispatchArgs a{};
   a.x = static_cast<const uint8_t*>(x);
   a.row_bytes = row_bytes;
+  a.nvec = static_cast<int>(row_bytes / 16);
   a.T = h->T;
   a.K = h->cfg.top_k;
-  a.chunk = row_bytes < kChunkMax ? static_cast<uint32_t>(row_bytes) : kChunkMax;
-  a.nchunk = static_cast<int>((row_bytes + a.chunk - 1) / a.chunk);
   a.pos = h->pos;
   a.w = w;
   a.send_row_of = h->send_row_of;
   a.recv = static_cast<uint8_t*>(recv);
   a.recv_w = recv_w;
   a.send = static_cast<uint8_t*>(send);
-  a.flags = h->flags;
   if (a.T == 0) return cudaSuccess;
-  const size_t smem = dispatch_smem_bytes(row_bytes);
-  const int grid = grid_for(reinterpret_cast<const void*>(dispatch_bulk_kernel), 32, smem,
-                            h->num_sms, static_cast<long long>(a.T) * a.nchunk);
-  dispatch_bulk_kernel<<<grid, 32, smem, s>>>(a);
+  // one block per token, a thread per 16-byte vector of the row (many
+  // independent stores in flight; measured faster than bulk copies through
+  // shared memory for this 1-read / K-write pattern)
+  const int block = threads_for(a.nvec, 1);
+  const int grid = a.T < 1048576 ? a.T : 1048576;
+  if (a.K <= 8)
+    dispatch_kernel<8><<<grid, block, 0, s>>>(a);
+  else
+    dispatch_kernel<16><<<grid, block, 0, s>>>(a);
   return cudaGetLastError();
 }
 
