@@ -33,6 +33,10 @@ struct moe_handle {
 
 namespace moe {
 
+// Resident blocks per SM of `kernel` at `threads` threads and `smem` dynamic
+// shared memory (cached per kernel).
+int resident_blocks(const void* kernel, int threads, size_t smem);
+
 cudaError_t launch_route_topk(const moe_handle* h, const float* logits, const float* bias, int T,
                               int32_t* idx, float* w, cudaStream_t s);
 

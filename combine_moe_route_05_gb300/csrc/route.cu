@@ -121,6 +121,21 @@ __device__ __forceinline__ bool load_logits(const RouteArgs& a, int t, int lane,
   return bad;
 }
 
+// One logit of row t as the selection sees it (NaN as -inf).
+__device__ __forceinline__ float logit_at(const RouteArgs& a, int t, int e) {
+  const float x = __ldg(a.logits + static_cast<size_t>(t) * a.E + e);
+  return isnan(x) ? -INFINITY : x;
+}
+
+template <int VPL>
+__device__ __forceinline__ void reload_logits(const RouteArgs& a, int t, int lane, float (&v)[VPL]) {
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const int e = lane * VPL + j;
+    v[j] = e < a.E ? logit_at(a, t, e) : -INFINITY;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // reference-precision paths, one token at a time (all lanes take part)
 
@@ -128,8 +143,9 @@ __device__ __forceinline__ bool load_logits(const RouteArgs& a, int t, int lane,
 // selection and weights); writes idx and w.  wkeys: E doubles of shared
 // memory owned by this warp.
 template <int VPL>
-__device__ void sigmoid_token_fp64(const RouteArgs& a, int t, int lane, const float (&v)[VPL],
-                                   double* wkeys) {
+__device__ void sigmoid_token_fp64(const RouteArgs& a, int t, int lane, double* wkeys) {
+  float v[VPL];
+  reload_logits<VPL>(a, t, lane, v);
   const int gsz = a.E / a.G;
   double s[VPL], key[VPL];
 #pragma unroll
@@ -226,7 +242,9 @@ __device__ void sigmoid_token_fp64(const RouteArgs& a, int t, int lane, const fl
 // Softmax routing of token t without renormalisation (the denominator runs
 // over all E experts); writes idx and w.
 template <int VPL>
-__device__ void softmax_token_full(const RouteArgs& a, int t, int lane, const float (&v)[VPL]) {
+__device__ void softmax_token_full(const RouteArgs& a, int t, int lane) {
+  float v[VPL];
+  reload_logits<VPL>(a, t, lane, v);
   uint32_t taken = 0;
   float myv = 0.f;
   int myi = 0;
@@ -294,9 +312,9 @@ __device__ __forceinline__ void sort_desc(float (&k)[VPL], int (&j)[VPL]) {
   }
 }
 
-// Sum of the top two (or top one) keys of a group whose keys are spread over
-// L lanes (each lane's list sorted), merged over lane bits 1..L/2.
-__device__ __forceinline__ float group_top2_fp32(float t0, float t1, int gk, int lanes) {
+// The top two keys of a group whose keys are spread over L lanes (each
+// lane's list sorted), merged over lane bits 1..L/2.
+__device__ __forceinline__ void group_top2_fp32(float& t0, float& t1, int lanes) {
   for (int off = 1; off < lanes; off <<= 1) {
     const float o0 = __shfl_xor_sync(kFull, t0, off);
     const float o1 = __shfl_xor_sync(kFull, t1, off);
@@ -305,13 +323,82 @@ __device__ __forceinline__ float group_top2_fp32(float t0, float t1, int gk, int
     t0 = n0;
     t1 = n1;
   }
-  return gk >= 2 ? __fadd_rn(__fadd_rn(0.0f, t0), t1) : t0;
 }
 
+// fp64 -> uint64 with the same order (no NaN reaches here)
+__device__ __forceinline__ uint64_t order_key64(double d) {
+  const uint64_t u = static_cast<uint64_t>(__double_as_longlong(d));
+  return (u & 0x8000000000000000ull) ? ~u : (u | 0x8000000000000000ull);
+}
+
+// Lane holding the largest key among the lanes where `valid` is set, the
+// lowest such lane on ties; -1 if no lane is valid.  Integer reductions only.
+__device__ __forceinline__ int warp_argmax_u64(bool valid, uint64_t key) {
+  const uint32_t hi = valid ? static_cast<uint32_t>(key >> 32) : 0u;
+  const uint32_t mhi = __reduce_max_sync(kFull, hi);
+  const bool c1 = valid && hi == mhi;
+  const uint32_t lo = c1 ? static_cast<uint32_t>(key) : 0u;
+  const uint32_t mlo = __reduce_max_sync(kFull, lo);
+  const uint32_t who = __ballot_sync(kFull, c1 && static_cast<uint32_t>(key) == mlo);
+  return who ? __ffs(who) - 1 : -1;
+}
+
+// The fp64 selection key of expert e with logit l (the reference definition).
+__device__ __forceinline__ double key_fp64(const RouteArgs& a, int e, float l) {
+  const double s = 1.0 / (1.0 + exp(-static_cast<double>(l)));
+  return s + (a.bias ? static_cast<double>(__ldg(a.bias + e)) : 0.0);
+}
+
+// The fp32 selection key (sigmoid + bias), the same expression everywhere.
+__device__ __forceinline__ float key_fp32(const RouteArgs& a, int e, float l) {
+  const float s = __frcp_rn(__fadd_rn(1.0f, expf(-l)));
+  return __fadd_rn(s, a.bias ? __ldg(a.bias + e) : 0.0f);
+}
+
+// Gathers the lanes' candidate experts (bit j of `mask`: expert lane*VPL + j)
+// into the warp's list in expert order and hands candidate i to lane i.
+// Returns the count (the same in every lane), or -1 if it exceeds 32.
+template <int VPL>
+__device__ __forceinline__ int compact_candidates(const RouteArgs& a, int t, uint32_t mask, int lane,
+                                                  int2* list, int2& mine) {
+  const int c = __popc(mask);
+  int incl = c;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(kFull, incl, d);
+    if (lane >= d) incl += o;
+  }
+  const int total = __shfl_sync(kFull, incl, 31);
+  if (total > 32) return -1;
+  int o = incl - c;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j)
+    if ((mask >> j) & 1u) {
+      const int e = lane * VPL + j;
+      list[o++] = make_int2(e, __float_as_int(logit_at(a, t, e)));
+    }
+  __syncwarp();
+  mine = lane < total ? list[lane] : make_int2(0, 0);
+  __syncwarp();
+  return total;
+}
+
+// Selection of one token from fp32 keys.  Returns true with the k-th
+// selected expert in lane base + k, or false if the token needs the full fp64
+// path.  Where an fp32 decision is closer than its error bound, only the
+// candidates that can cross it get fp64 keys:
+//   experts: an eligible expert whose fp32 key is more than 2 * DELTA below
+//     the K-th pick's has an fp64 key below those of all K picks, so the fp64
+//     top-K lies among the experts within 2 * DELTA of the K-th pick or above;
+//   groups: likewise a group more than 2 * DG below the TG-th group score is
+//     out, and a group's fp64 score only involves its experts within 2 * DELTA
+//     of its GK-th fp32 key or above.
+// The candidates (at most 32) get one fp64 key each, one per lane, and the
+// selection among them uses the exact fp64 order (ties to the lower index).
 template <int VPL, bool SIGMOID>
-__device__ __forceinline__ bool select_fp32(const RouteArgs& a, int lane, const float (&v)[VPL],
-                                            int base, int& my_idx) {
-  float sk[VPL];
+__device__ __forceinline__ bool select_fp32(const RouteArgs& a, int t, int lane, float (&sk)[VPL],
+                                            int base, int& my_idx, int2* list) {
+  // sk holds the lane's logits on entry and becomes its sorted keys
   int sj[VPL];
   float maxabs = 0.0f;
   int n_valid = 0;  // experts of this lane below E
@@ -322,11 +409,8 @@ __device__ __forceinline__ bool select_fp32(const RouteArgs& a, int lane, const 
     if (e < a.E) {
       ++n_valid;
       if (SIGMOID) {
-        const float s = __frcp_rn(__fadd_rn(1.0f, expf(-v[j])));
-        sk[j] = __fadd_rn(s, a.bias ? __ldg(a.bias + e) : 0.0f);
+        sk[j] = key_fp32(a, e, sk[j]);
         maxabs = fmaxf(maxabs, fabsf(sk[j]));
-      } else {
-        sk[j] = v[j];
       }
     } else {
       sk[j] = -INFINITY;
@@ -346,7 +430,9 @@ __device__ __forceinline__ bool select_fp32(const RouteArgs& a, int lane, const 
   if (SIGMOID && a.G > 1) {
     const int gsz = a.E / a.G;
     const int L = gsz / VPL;
-    const float gs = group_top2_fp32(sk[0], VPL > 1 ? sk[VPL > 1 ? 1 : 0] : -INFINITY, a.GK, L);
+    float t0 = sk[0], t1 = VPL > 1 ? sk[VPL > 1 ? 1 : 0] : -INFINITY;
+    group_top2_fp32(t0, t1, L);
+    const float gs = a.GK >= 2 ? __fadd_rn(__fadd_rn(0.0f, t0), t1) : t0;
     // lane g < G holds group g's score; TG + 1 rounds of warp arg-max, ties
     // to the lower group
     const bool glane = lane < a.G;
@@ -370,13 +456,47 @@ __device__ __forceinline__ bool select_fp32(const RouteArgs& a, int lane, const 
       }
     }
     const float dg = a.GK * (delta + kDeltaRel * gmax);
-    if (a.TG < a.G && !(last - next > 2.0f * dg)) return false;
+    if (a.TG < a.G && !(last - next > 2.0f * dg)) {
+      // refine the group choice with fp64 group scores of the candidate groups
+      const uint32_t cg = __ballot_sync(kFull, glane && my_gs >= last - 2.0f * dg);
+      uint32_t mask = 0;
+      if (lane * VPL < a.E && ((cg >> ((lane * VPL) / gsz)) & 1u)) {
+        const float thr = (a.GK >= 2 ? t1 : t0) - 2.0f * delta;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i)
+          if (sk[i] >= thr && lane * VPL + sj[i] < a.E) mask |= 1u << sj[i];
+      }
+      int2 c;
+      const int n = compact_candidates<VPL>(a, t, mask, lane, list, c);
+      if (n < 0) return false;
+      const bool have = lane < n;
+      const double kd = have ? key_fp64(a, c.x, __int_as_float(c.y)) : 0.0;
+      const uint64_t ok = order_key64(kd);
+      const int cgrp = c.x / gsz;
+      uint64_t my_gs64 = 0;
+      for (uint32_t rem = cg; rem; rem &= rem - 1) {
+        const int g = __ffs(rem) - 1;
+        const int w1 = warp_argmax_u64(have && cgrp == g, ok);
+        double sum = __shfl_sync(kFull, kd, w1 & 31);
+        if (a.GK >= 2) {
+          const int w2 = warp_argmax_u64(have && cgrp == g && lane != w1, ok);
+          sum = sum + __shfl_sync(kFull, kd, w2 & 31);
+        }
+        if (lane == g) my_gs64 = order_key64(sum);
+      }
+      keep = 0;
+      for (int r = 0; r < a.TG; ++r) {
+        const int wg = warp_argmax_u64(glane && ((cg >> lane) & 1u) && !((keep >> lane) & 1u), my_gs64);
+        keep |= 1u << (wg & 31);
+      }
+    }
     eligible_lane = eligible_lane && ((keep >> ((lane * VPL) / gsz)) & 1u);
   }
 
   // K (+1 for the gap check) rounds over the lanes' heads
   int consumed = 0;
-  float prev = 0.0f;
+  float prev = 0.0f, vK = 0.0f;
+  bool close = false;
   const int n_elig = SIGMOID && a.G > 1 ? a.TG * (a.E / a.G) : a.E;
   const int rounds = SIGMOID ? (a.K < n_elig ? a.K + 1 : a.K) : a.K;
   for (int k = 0; k < rounds; ++k) {
@@ -395,9 +515,35 @@ __device__ __forceinline__ bool select_fp32(const RouteArgs& a, int lane, const 
       sk[VPL - 1] = -INFINITY;
       ++consumed;
     }
-    if (SIGMOID && k > 0 && !(prev - wv > 2.0f * delta)) return false;
+    if (SIGMOID && k > 0 && !(prev - wv > 2.0f * delta)) close = true;
     prev = wv;
+    if (k == a.K - 1) vK = wv;
     if (k < a.K && lane == base + k) my_idx = wl * VPL + wj;
+  }
+  if (!SIGMOID || !close) return true;
+
+  // refine the expert choice: fp64 keys for the eligible experts within
+  // 2 * DELTA of the K-th pick or above
+  const float thr = vK - 2.0f * delta;
+  uint32_t mask = 0;
+  if (eligible_lane) {
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane * VPL + j;
+      if (e < a.E && key_fp32(a, e, logit_at(a, t, e)) >= thr) mask |= 1u << j;
+    }
+  }
+  int2 c;
+  const int n = compact_candidates<VPL>(a, t, mask, lane, list, c);
+  if (n < 0) return false;
+  const bool have = lane < n;
+  const uint64_t ok = order_key64(have ? key_fp64(a, c.x, __int_as_float(c.y)) : 0.0);
+  bool taken = false;
+  for (int k = 0; k < a.K; ++k) {
+    const int w = warp_argmax_u64(have && !taken, ok);
+    if (lane == w) taken = true;
+    const int e = __shfl_sync(kFull, c.x, w & 31);
+    if (lane == base + k) my_idx = e;
   }
   return true;
 }
@@ -405,17 +551,23 @@ __device__ __forceinline__ bool select_fp32(const RouteArgs& a, int lane, const 
 template <int VPL, bool SIGMOID>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
   extern __shared__ double route_smem[];
+  __shared__ int2 cand_lists[kRouteWarps][32];
   double* wkeys = route_smem + (threadIdx.x >> 5) * a.E;
+  int2* list = cand_lists[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
   const int TB = 32 / a.K;  // tokens per fp64 weight pass
-  const int nwarps = gridDim.x * kRouteWarps;
+  // persistent grid: warp w takes tokens w, w + W, w + 2W, ... (W warps in
+  // all), TB at a time, so every warp gets the same number of tokens to
+  // within one
+  const int W = gridDim.x * kRouteWarps;
+  const int wid = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
   const int j_of_lane = lane / a.K, k_of_lane = lane % a.K;
-  for (int t0 = (blockIdx.x * kRouteWarps + (threadIdx.x >> 5)) * TB; t0 < a.T; t0 += nwarps * TB) {
+  for (int i0 = 0; wid + i0 * W < a.T; i0 += TB) {
     int my_idx = 0;
     float my_logit = 0.0f;
     bool my_fast = false;
     for (int j = 0; j < TB; ++j) {
-      const int t = t0 + j;
+      const int t = wid + (i0 + j) * W;
       if (t >= a.T) break;
       float v[VPL];
       const bool bad = load_logits<VPL>(a, t, lane, v);
@@ -424,7 +576,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
       // sigmoid token with a non-finite logit goes to the fp64 path
       const bool use_fast = a.fast && !(SIGMOID && __any_sync(kFull, bad));
       int sel_idx = 0;
-      const bool ok = use_fast && select_fp32<VPL, SIGMOID>(a, lane, v, j * a.K, sel_idx);
+      const bool ok = use_fast && select_fp32<VPL, SIGMOID>(a, t, lane, v, j * a.K, sel_idx, list);
       if (ok) {
         if (j_of_lane == j) {
           my_idx = sel_idx;
@@ -432,13 +584,13 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
           my_fast = true;
         }
       } else if (SIGMOID) {
-        sigmoid_token_fp64<VPL>(a, t, lane, v, wkeys);
+        sigmoid_token_fp64<VPL>(a, t, lane, wkeys);
       } else {
-        softmax_token_full<VPL>(a, t, lane, v);
+        softmax_token_full<VPL>(a, t, lane);
       }
     }
     // fp64 weights of the tokens selected in fp32: lane = (token j, rank k)
-    const int t = t0 + j_of_lane;
+    const int t = wid + (i0 + j_of_lane) * W;
     double val;
     if (SIGMOID) {
       val = 1.0 / (1.0 + exp(-static_cast<double>(my_logit)));
@@ -456,9 +608,18 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
   }
 }
 
+// One wave of resident blocks (or fewer if there are fewer tokens): a second,
+// partial wave would leave most SMs idle for a whole block's duration.
 template <int VPL, bool SIGMOID>
-void launch_one(const RouteArgs& a, int grid, size_t smem, cudaStream_t s) {
-  route_kernel<VPL, SIGMOID><<<grid, kRouteWarps * 32, smem, s>>>(a);
+void launch_one(const RouteArgs& a, int num_sms, size_t smem, cudaStream_t s) {
+  auto k = route_kernel<VPL, SIGMOID>;
+  const int TB = 32 / a.K;
+  const long long warps_needed = (static_cast<long long>(a.T) + TB - 1) / TB;
+  const long long blocks_needed = (warps_needed + kRouteWarps - 1) / kRouteWarps;
+  long long grid = static_cast<long long>(resident_blocks(reinterpret_cast<const void*>(k),
+                                                          kRouteWarps * 32, smem)) * num_sms;
+  if (blocks_needed < grid) grid = blocks_needed;
+  k<<<static_cast<int>(grid < 1 ? 1 : grid), kRouteWarps * 32, smem, s>>>(a);
 }
 
 }  // namespace
@@ -494,18 +655,13 @@ cudaError_t launch_route_topk(const moe_handle* h, const float* logits, const fl
   } else {
     a.fast = a.renorm;  // without renormalisation the weights need all E exponentials
   }
-  const int TB = 32 / a.K;
-  const int warps_needed = (T + TB - 1) / TB;
-  const int blocks_needed = (warps_needed + kRouteWarps - 1) / kRouteWarps;
-  const int cap = h->num_sms * 16;
-  const int grid = blocks_needed < cap ? blocks_needed : cap;
   const size_t smem = sigmoid && a.G > 1 ? static_cast<size_t>(kRouteWarps) * a.E * sizeof(double) : 0;
   switch (vpl) {
-    case 1: sigmoid ? launch_one<1, true>(a, grid, smem, s) : launch_one<1, false>(a, grid, smem, s); break;
-    case 2: sigmoid ? launch_one<2, true>(a, grid, smem, s) : launch_one<2, false>(a, grid, smem, s); break;
-    case 4: sigmoid ? launch_one<4, true>(a, grid, smem, s) : launch_one<4, false>(a, grid, smem, s); break;
-    case 8: sigmoid ? launch_one<8, true>(a, grid, smem, s) : launch_one<8, false>(a, grid, smem, s); break;
-    default: sigmoid ? launch_one<16, true>(a, grid, smem, s) : launch_one<16, false>(a, grid, smem, s); break;
+    case 1: sigmoid ? launch_one<1, true>(a, h->num_sms, smem, s) : launch_one<1, false>(a, h->num_sms, smem, s); break;
+    case 2: sigmoid ? launch_one<2, true>(a, h->num_sms, smem, s) : launch_one<2, false>(a, h->num_sms, smem, s); break;
+    case 4: sigmoid ? launch_one<4, true>(a, h->num_sms, smem, s) : launch_one<4, false>(a, h->num_sms, smem, s); break;
+    case 8: sigmoid ? launch_one<8, true>(a, h->num_sms, smem, s) : launch_one<8, false>(a, h->num_sms, smem, s); break;
+    default: sigmoid ? launch_one<16, true>(a, h->num_sms, smem, s) : launch_one<16, false>(a, h->num_sms, smem, s); break;
   }
   return cudaGetLastError();
 }

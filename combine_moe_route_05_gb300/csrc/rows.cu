@@ -282,8 +282,10 @@ int threads_for(int nvec, int per) {
   return t < 32 ? 32 : (t > 1024 ? 1024 : t);
 }
 
+}  // namespace
+
 // Resident blocks per SM of `kernel`, computed once per (kernel, smem) pair.
-int blocks_per_sm(const void* kernel, int threads, size_t smem) {
+int resident_blocks(const void* kernel, int threads, size_t smem) {
   struct Entry {
     const void* k;
     int threads;
@@ -305,10 +307,12 @@ int blocks_per_sm(const void* kernel, int threads, size_t smem) {
   return per_sm;
 }
 
+namespace {
+
 // Persistent grid: every resident block slot of the GPU, or fewer if there is
 // less work.
 int grid_for(const void* kernel, int threads, size_t smem, int num_sms, long long work_items) {
-  long long g = static_cast<long long>(blocks_per_sm(kernel, threads, smem)) * num_sms;
+  long long g = static_cast<long long>(resident_blocks(kernel, threads, smem)) * num_sms;
   if (work_items < g) g = work_items;
   return static_cast<int>(g < 1 ? 1 : g);
 }
