@@ -32,7 +32,7 @@ EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_handle_create", "moe
            "moe_route_topk", "moe_dispatch_layout", "moe_layout_view", "moe_dispatch",
            "moe_combine", "moe_combine_bwd", "moe_dispatch_bwd", "moe_scale_rows",
            "moe_scale_rows_bwd", "moe_read_device_status", "moe_clear_device_status",
-           "moe_dispatch_layout_static")
+           "moe_dispatch_layout_static", "moe_route_bwd")
 MOE_LAYOUT_STATIC_COUNTERS = 65536
 MOE_LAYOUT_TILE_TOKENS = 512
 
@@ -88,6 +88,7 @@ def lib():
             "moe_read_device_status": ([P, P], st),
             "moe_clear_device_status": ([P, P], st),
             "moe_dispatch_layout_static": ([P, P, i32, P, P, P], st),
+            "moe_route_bwd": ([P, P, P, P, i32, P, P], st),
         }
         for name, (args, res) in sigs.items():
             f = getattr(L, name)
@@ -203,6 +204,16 @@ def moe_route_topk(h, logits, bias, idx, w, stream=None):
     _req(w, torch.float32, (T, h.K), "w")
     _check("moe_route_topk", lib().moe_route_topk(h.ptr, _ptr(logits), _ptr(bias), T, _ptr(idx),
                                                   _ptr(w), _stream(stream)))
+
+
+def moe_route_bwd(h, logits, idx, gw, glogits, stream=None):
+    T = logits.shape[0]
+    _req(logits, torch.float32, (T, h.E), "logits")
+    _req(idx, torch.int32, (T, h.K), "idx")
+    _req(gw, torch.float32, (T, h.K), "gw")
+    _req(glogits, torch.float32, (T, h.E), "glogits")
+    _check("moe_route_bwd", lib().moe_route_bwd(h.ptr, _ptr(logits), _ptr(idx), _ptr(gw), T,
+                                                _ptr(glogits), _stream(stream)))
 
 
 def moe_dispatch_layout(h, idx, stream=None):
@@ -351,6 +362,11 @@ class MoeRouter:
         w = torch.empty(T, self.h.K, dtype=torch.float32, device=logits.device)
         moe_route_topk(self.h, logits, bias, idx, w, stream)
         return idx, w
+
+    def route_bwd(self, logits, idx, gw, stream=None):
+        glogits = torch.empty_like(logits)
+        moe_route_bwd(self.h, logits, idx, gw, glogits, stream)
+        return glogits
 
     def layout(self, idx, stream=None):
         moe_dispatch_layout(self.h, idx, stream)

@@ -188,6 +188,17 @@ moe_status moe_route_topk(moe_handle* h, const float* d_logits, const float* d_b
   return from_cuda(moe::launch_route_topk(h, d_logits, d_bias, T, d_idx, d_w, as_stream(stream)));
 }
 
+moe_status moe_route_bwd(const moe_handle* h, const float* d_logits, const int32_t* d_idx,
+                         const float* d_gw, int32_t T, float* d_glogits, void* stream) {
+  if (!h || T < 0) return MOE_ERR_INVALID;
+  if (T > h->cfg.max_tokens) return MOE_ERR_CAPACITY;
+  if (T > 0 && (!d_logits || !d_idx || !d_gw || !d_glogits)) return MOE_ERR_INVALID;
+  if (!aligned(d_logits, 4) || !aligned(d_idx, 4) || !aligned(d_gw, 4) || !aligned(d_glogits, 4))
+    return MOE_ERR_INVALID;
+  return from_cuda(
+      moe::launch_route_bwd(h, d_logits, d_idx, d_gw, T, d_glogits, as_stream(stream)));
+}
+
 moe_status moe_dispatch_layout(moe_handle* h, const int32_t* d_idx, int32_t T, void* stream) {
   if (!h || T < 0) return MOE_ERR_INVALID;
   if (T > h->cfg.max_tokens) return MOE_ERR_CAPACITY;

@@ -40,6 +40,9 @@ int resident_blocks(const void* kernel, int threads, size_t smem);
 cudaError_t launch_route_topk(const moe_handle* h, const float* logits, const float* bias, int T,
                               int32_t* idx, float* w, cudaStream_t s);
 
+cudaError_t launch_route_bwd(const moe_handle* h, const float* logits, const int32_t* idx,
+                             const float* gw, int T, float* glogits, cudaStream_t s);
+
 cudaError_t launch_layout(const moe_handle* h, const int32_t* idx, int T, cudaStream_t s);
 
 cudaError_t launch_dispatch(const moe_handle* h, const void* x, int64_t row_bytes, const float* w,

@@ -622,6 +622,137 @@ void launch_one(const RouteArgs& a, int num_sms, size_t smem, cudaStream_t s) {
   k<<<static_cast<int>(grid < 1 ? 1 : grid), kRouteWarps * 32, smem, s>>>(a);
 }
 
+// ---------------------------------------------------------------------------
+// Router backward to the logits (DeepSpeed "Avoid collective token preparation
+// for AutoEP DeepEP", "Testing Done": routing-score and router-parameter
+// gradients).  With the selection fixed, the weights are
+//   softmax, renorm:     w_k = c q_k,   q_k = exp(l_k) / sum_{j in sel} exp(l_j)
+//   softmax, no renorm:  w_k = c p_k,   p = softmax(l) over all E
+//   sigmoid, renorm:     w_k = c s_k / S,  S = sum_{j in sel} s_j
+//   sigmoid, no renorm:  w_k = c s_k
+// (the correction bias selects only and gets no gradient), so
+//   softmax renorm:     dL/dl_j = c q_j (gw_j - sum_k q_k gw_k)
+//   softmax no renorm:  dL/dl_e = c p_e (gw_e - sum_k p_k gw_k)   (every e)
+//   sigmoid renorm:     dL/dl_j = s_j (1 - s_j) (c / S) (gw_j - sum_k gw_k s_k / S)
+//   sigmoid no renorm:  dL/dl_j = c gw_j s_j (1 - s_j)
+// computed in fp64 with sums in k order, rounded once to fp32; every other
+// entry of the row is 0.  Lane j*K + k handles entry k of token j, TB = 32/K
+// tokens per warp pass.
+
+struct RouteBwdArgs {
+  const float* logits;
+  const int32_t* idx;
+  const float* gw;
+  float* glogits;
+  int T, E, K;
+  int sigmoid, renorm;
+  double scale;
+};
+
+__global__ void __launch_bounds__(kRouteWarps * 32) route_bwd_kernel(RouteBwdArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int TB = 32 / a.K;
+  const int W = gridDim.x * kRouteWarps;
+  const int wid = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
+  const int j = lane / a.K, k = lane % a.K;
+  const bool vec4 = (a.E & 3) == 0 && ((reinterpret_cast<uintptr_t>(a.glogits) & 15) == 0);
+  for (int i0 = 0; wid + i0 * W < a.T; i0 += TB) {
+    // zero the TB rows
+    for (int jj = 0; jj < TB; ++jj) {
+      const int t = wid + (i0 + jj) * W;
+      if (t >= a.T) break;
+      float* row = a.glogits + static_cast<size_t>(t) * a.E;
+      if (vec4) {
+        for (int e = lane * 4; e < a.E; e += 128)
+          *reinterpret_cast<float4*>(row + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        for (int e = lane; e < a.E; e += 32) row[e] = 0.f;
+      }
+    }
+    const int t = wid + (i0 + j) * W;
+    const bool valid = j < TB && t < a.T;
+    int e = 0;
+    double l = 0.0, g = 0.0;
+    if (valid) {
+      e = __ldg(a.idx + static_cast<size_t>(t) * a.K + k);
+      if (e < 0 || e >= a.E) e = 0;  // invalid indices: routed tokens come from route_topk
+      l = static_cast<double>(__ldg(a.logits + static_cast<size_t>(t) * a.E + e));
+      g = static_cast<double>(__ldg(a.gw + static_cast<size_t>(t) * a.K + k));
+    }
+    const int b = (j * a.K) & 31;  // lane of entry 0 of this token
+    double out;
+    if (!a.sigmoid) {
+      const double lmax = __shfl_sync(kFull, l, b);
+      const double ex = exp(l - lmax);
+      double den = 0.0;
+      for (int kk = 0; kk < a.K; ++kk) den += __shfl_sync(kFull, ex, (b + kk) & 31);
+      const double q = ex / den;
+      double dot = 0.0;
+      for (int kk = 0; kk < a.K; ++kk) dot += __shfl_sync(kFull, q * g, (b + kk) & 31);
+      out = a.scale * q * (g - dot);
+    } else {
+      const double sg = 1.0 / (1.0 + exp(-l));
+      if (a.renorm) {
+        double S = 0.0;
+        for (int kk = 0; kk < a.K; ++kk) S += __shfl_sync(kFull, sg, (b + kk) & 31);
+        double dot = 0.0;
+        for (int kk = 0; kk < a.K; ++kk) dot += __shfl_sync(kFull, g * sg / S, (b + kk) & 31);
+        out = sg * (1.0 - sg) * (a.scale / S) * (g - dot);
+      } else {
+        out = a.scale * g * sg * (1.0 - sg);
+      }
+    }
+    __syncwarp();  // the zero fill above is ordered before these writes
+    if (valid) a.glogits[static_cast<size_t>(t) * a.E + e] = static_cast<float>(out);
+    __syncwarp();
+  }
+}
+
+// softmax without renormalisation: every logit of the row moves (one token per
+// warp, each lane its VPL experts)
+template <int VPL>
+__global__ void __launch_bounds__(kRouteWarps * 32) route_bwd_full_softmax_kernel(RouteBwdArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int W = gridDim.x * kRouteWarps;
+  for (int t = blockIdx.x * kRouteWarps + (threadIdx.x >> 5); t < a.T; t += W) {
+    const float* row = a.logits + static_cast<size_t>(t) * a.E;
+    double m = -INFINITY;
+#pragma unroll
+    for (int jj = 0; jj < VPL; ++jj) {
+      const int e = lane * VPL + jj;
+      if (e < a.E) m = fmax(m, static_cast<double>(__ldg(row + e)));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmax(m, __shfl_xor_sync(kFull, m, off));
+    double part = 0.0;
+#pragma unroll
+    for (int jj = 0; jj < VPL; ++jj) {
+      const int e = lane * VPL + jj;
+      if (e < a.E) part += exp(static_cast<double>(__ldg(row + e)) - m);
+    }
+    double den = 0.0;
+    for (int ll = 0; ll < 32; ++ll) den += __shfl_sync(kFull, part, ll);
+    double dot = 0.0;
+    for (int kk = 0; kk < a.K; ++kk) {
+      int e = __ldg(a.idx + static_cast<size_t>(t) * a.K + kk);
+      if (e < 0 || e >= a.E) e = 0;
+      dot += exp(static_cast<double>(__ldg(row + e)) - m) / den *
+             static_cast<double>(__ldg(a.gw + static_cast<size_t>(t) * a.K + kk));
+    }
+#pragma unroll
+    for (int jj = 0; jj < VPL; ++jj) {
+      const int e = lane * VPL + jj;
+      if (e >= a.E) continue;
+      double ge = 0.0;
+      for (int kk = 0; kk < a.K; ++kk)
+        if (__ldg(a.idx + static_cast<size_t>(t) * a.K + kk) == e)
+          ge = static_cast<double>(__ldg(a.gw + static_cast<size_t>(t) * a.K + kk));
+      const double p = exp(static_cast<double>(__ldg(row + e)) - m) / den;
+      a.glogits[static_cast<size_t>(t) * a.E + e] = static_cast<float>(a.scale * p * (ge - dot));
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_route_topk(const moe_handle* h, const float* logits, const float* bias, int T,
@@ -663,6 +794,45 @@ cudaError_t launch_route_topk(const moe_handle* h, const float* logits, const fl
     case 8: sigmoid ? launch_one<8, true>(a, h->num_sms, smem, s) : launch_one<8, false>(a, h->num_sms, smem, s); break;
     default: sigmoid ? launch_one<16, true>(a, h->num_sms, smem, s) : launch_one<16, false>(a, h->num_sms, smem, s); break;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_bwd(const moe_handle* h, const float* logits, const int32_t* idx,
+                             const float* gw, int T, float* glogits, cudaStream_t s) {
+  const moe_config& c = h->cfg;
+  RouteBwdArgs a;
+  a.logits = logits;
+  a.idx = idx;
+  a.gw = gw;
+  a.glogits = glogits;
+  a.T = T;
+  a.E = c.num_experts;
+  a.K = c.top_k;
+  a.sigmoid = c.score_fn == MOE_SCORE_SIGMOID;
+  a.renorm = c.renorm;
+  a.scale = c.route_scale;
+  if (T == 0) return cudaSuccess;
+  const int threads = kRouteWarps * 32;
+  if (!a.sigmoid && !a.renorm) {
+    const int vpl = a.E <= 32 ? 1 : a.E <= 64 ? 2 : a.E <= 128 ? 4 : a.E <= 256 ? 8 : 16;
+    const long long blocks = (static_cast<long long>(T) + kRouteWarps - 1) / kRouteWarps;
+    const int grid = static_cast<int>(blocks < h->num_sms * 8 ? blocks : h->num_sms * 8);
+    switch (vpl) {
+      case 1: route_bwd_full_softmax_kernel<1><<<grid, threads, 0, s>>>(a); break;
+      case 2: route_bwd_full_softmax_kernel<2><<<grid, threads, 0, s>>>(a); break;
+      case 4: route_bwd_full_softmax_kernel<4><<<grid, threads, 0, s>>>(a); break;
+      case 8: route_bwd_full_softmax_kernel<8><<<grid, threads, 0, s>>>(a); break;
+      default: route_bwd_full_softmax_kernel<16><<<grid, threads, 0, s>>>(a); break;
+    }
+    return cudaGetLastError();
+  }
+  const int TB = 32 / a.K;
+  const long long warps_needed = (static_cast<long long>(T) + TB - 1) / TB;
+  const long long blocks_needed = (warps_needed + kRouteWarps - 1) / kRouteWarps;
+  long long grid = static_cast<long long>(resident_blocks(
+                       reinterpret_cast<const void*>(route_bwd_kernel), threads, 0)) * h->num_sms;
+  if (blocks_needed < grid) grid = blocks_needed;
+  route_bwd_kernel<<<static_cast<int>(grid < 1 ? 1 : grid), threads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -175,6 +175,25 @@ moe_status moe_route_topk(moe_handle* h, const float* d_logits, const float* d_b
                           int32_t* d_idx, float* d_w, void* stream);
 
 /*
+ * Router backward to the logits ([AutoEP-prep] "Testing Done": the parity
+ * list covers routing-score and router-parameter gradients): given the
+ * router-score gradient d_gw [T,K] fp32 (from moe_combine_bwd or
+ * moe_scale_rows_bwd) and the selection d_idx [T,K] of d_logits [T,E],
+ * writes d_glogits [T,E] fp32 = dL/dlogits with the selection held fixed:
+ *   softmax, renorm:     c q_j (gw_j - sum_k q_k gw_k) for the selected j,
+ *                        q = softmax over the selected logits, 0 elsewhere;
+ *   softmax, no renorm:  c p_e (gw_e - sum_k p_k gw_k) for every e, p the
+ *                        full softmax, gw_e = 0 for unselected e;
+ *   sigmoid, renorm:     s_j (1 - s_j) (c / S) (gw_j - sum_k gw_k s_k / S),
+ *                        S = sum of the selected sigmoids;
+ *   sigmoid, no renorm:  c gw_j s_j (1 - s_j).
+ * c = route_scale.  The correction bias only selects and has no gradient.
+ * Computed in fp64 (sums in k order), rounded once to fp32.
+ */
+moe_status moe_route_bwd(const moe_handle* h, const float* d_logits, const int32_t* d_idx,
+                         const float* d_gw, int32_t T, float* d_glogits, void* stream);
+
+/*
  * Dispatch layout ([AutoEP-DeepEP] "Why"; [AutoEP-prep] "Summary"): from
  * d_idx [T,K] computes every array of moe_layout on the device, with no host
  * synchronisation.  Receive rows are grouped by expert, stable by token then

@@ -50,6 +50,8 @@ def lib():
         L.orc_combine_f64.restype = None
         L.orc_dispatch_f64.argtypes = [P, i64, i64, i32, P, P]
         L.orc_dispatch_f64.restype = None
+        L.orc_route_bwd.argtypes = [P, i64, i32, i32, i32, i32, d, P, P, P]
+        L.orc_route_bwd.restype = i32
         L.orc_f32_to_bf16.argtypes = [P, i64, P]
         L.orc_f32_to_bf16.restype = None
         _lib = L
@@ -96,6 +98,22 @@ def route_sigmoid_grouped(logits, bias, K, n_groups, topk_groups, group_score_to
     if rc != 0:
         raise ValueError("orc_route_sigmoid_grouped: invalid sizes")
     return idx, w
+
+
+def route_bwd(logits, idx, gw, score_fn="softmax", renorm=True, route_scale=1.0):
+    """dL/dlogits [T,E] fp64 of the routing weights, selection held fixed."""
+    logits = _c(logits, np.float32)
+    idx = _c(idx, np.int32)
+    gw = _c(gw, np.float64)
+    T, E = logits.shape
+    K = idx.shape[1]
+    out = np.empty((T, E), np.float64)
+    fn = {"softmax": 0, "sigmoid": 1}[score_fn]
+    rc = lib().orc_route_bwd(_p(logits), T, E, K, fn, int(renorm), float(route_scale), _p(idx),
+                             _p(gw), _p(out))
+    if rc != 0:
+        raise ValueError("orc_route_bwd: invalid sizes")
+    return out
 
 
 class Layout:

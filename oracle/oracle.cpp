@@ -39,6 +39,7 @@
 //     earlier for the same token is dropped: it gets pos = -1, is not counted
 //     and contributes nothing.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -448,6 +449,81 @@ void orc_dispatch_f64(const double* x, int64_t H, int64_t T, int K, const int32_
 // reference values the same way the definitions above do.
 void orc_f32_to_bf16(const float* src, int64_t n, uint16_t* dst) {
   for (int64_t i = 0; i < n; ++i) dst[i] = float_to_bf16_bits(src[i]);
+}
+
+// Router backward to the logits (the router-score and router-parameter
+// gradients of [AutoEP-prep] "Testing Done"; dL/dw is the router-score
+// gradient that the combine backward returns).  The selection is fixed; the
+// weights as functions of the logits are
+//   softmax, renorm:     w_k = c * q_k,  q_k = exp(l_k) / sum_{j in sel} exp(l_j)
+//   softmax, no renorm:  w_k = c * p_k,  p = softmax(l) over all E
+//   sigmoid, renorm:     w_k = c * s_k / S,  s = sigmoid(l), S = sum_{j in sel} s_j
+//   sigmoid, no renorm:  w_k = c * s_k
+// (c = route_scale; the correction bias enters only the selection and gets no
+// gradient).  Their derivatives, in fp64:
+//   softmax renorm:     dL/dl_j = c q_j (gw_j - sum_k q_k gw_k),  j selected; 0 else
+//   softmax no renorm:  dL/dl_e = c p_e (gw_e - sum_k p_k gw_k),  gw_e = 0 if e not selected
+//   sigmoid renorm:     dL/dl_j = s_j (1 - s_j) (c / S) (gw_j - sum_k gw_k s_k / S)
+//   sigmoid no renorm:  dL/dl_j = c gw_j s_j (1 - s_j)
+// glogits [T,E] fp64 (every entry written).
+int orc_route_bwd(const float* logits, int64_t T, int E, int K, int score_fn, int renorm,
+                  double route_scale, const int32_t* idx, const double* gw, double* glogits) {
+  if (T < 0 || E <= 0 || K <= 0 || K > E) return -1;
+  for (int64_t t = 0; t < T; ++t) {
+    const float* l = logits + t * E;
+    const int32_t* sel = idx + t * K;
+    const double* g = gw + t * K;
+    double* out = glogits + t * E;
+    for (int e = 0; e < E; ++e) out[e] = 0.0;
+    if (score_fn == 0) {  // softmax
+      const double l_max = static_cast<double>(l[sel[0]]);
+      double den = 0.0;
+      if (renorm) {
+        for (int k = 0; k < K; ++k) den += std::exp(static_cast<double>(l[sel[k]]) - l_max);
+        double dot = 0.0;
+        for (int k = 0; k < K; ++k)
+          dot += std::exp(static_cast<double>(l[sel[k]]) - l_max) / den * g[k];
+        for (int k = 0; k < K; ++k) {
+          double q = std::exp(static_cast<double>(l[sel[k]]) - l_max) / den;
+          out[sel[k]] = route_scale * q * (g[k] - dot);
+        }
+      } else {
+        double m = static_cast<double>(l[0]);
+        for (int e = 1; e < E; ++e) m = std::max(m, static_cast<double>(l[e]));
+        for (int e = 0; e < E; ++e) den += std::exp(static_cast<double>(l[e]) - m);
+        std::vector<double> gfull(static_cast<size_t>(E), 0.0);
+        for (int k = 0; k < K; ++k) gfull[static_cast<size_t>(sel[k])] = g[k];
+        double dot = 0.0;
+        for (int k = 0; k < K; ++k)
+          dot += std::exp(static_cast<double>(l[sel[k]]) - m) / den * g[k];
+        for (int e = 0; e < E; ++e) {
+          double p = std::exp(static_cast<double>(l[e]) - m) / den;
+          out[e] = route_scale * p * (gfull[static_cast<size_t>(e)] - dot);
+        }
+      }
+    } else {  // sigmoid
+      std::vector<double> s(static_cast<size_t>(K));
+      double S = 0.0;
+      for (int k = 0; k < K; ++k) {
+        s[static_cast<size_t>(k)] = 1.0 / (1.0 + std::exp(-static_cast<double>(l[sel[k]])));
+        S += s[static_cast<size_t>(k)];
+      }
+      if (renorm) {
+        double dot = 0.0;
+        for (int k = 0; k < K; ++k) dot += g[k] * s[static_cast<size_t>(k)] / S;
+        for (int k = 0; k < K; ++k) {
+          double sk = s[static_cast<size_t>(k)];
+          out[sel[k]] = sk * (1.0 - sk) * (route_scale / S) * (g[k] - dot);
+        }
+      } else {
+        for (int k = 0; k < K; ++k) {
+          double sk = s[static_cast<size_t>(k)];
+          out[sel[k]] = route_scale * g[k] * sk * (1.0 - sk);
+        }
+      }
+    }
+  }
+  return 0;
 }
 
 }  // extern "C"

@@ -577,3 +577,60 @@ def test_bf16_rounding_of_generator_matches_oracle_rounding():
                                  np.float32)])
     assert (synth.to_bf16_bits(a) == oracle.f32_to_bf16(a)).all()
     assert (oracle.bf16_to_f32(synth.to_bf16_bits(np.float32([1.00390625]))) == np.float32(1.0)).all()
+
+
+# ----------------------------------------------------------------------------
+# router backward to the logits
+
+
+def weights_fp64(logits_row, sel, score_fn, renorm, scale):
+    """Routing weights of a fixed selection as a function of the logits, from
+    library routines (scipy softmax / expit), for numerical differentiation."""
+    l = np.asarray(logits_row, np.float64)
+    if score_fn == "softmax":
+        p = scipy.special.softmax(l[sel]) if renorm else scipy.special.softmax(l)[sel]
+        return scale * p
+    s = scipy.special.expit(l[sel])
+    return scale * (s / s.sum() if renorm else s)
+
+
+@pytest.mark.parametrize("score_fn", ["softmax", "sigmoid"])
+@pytest.mark.parametrize("renorm", [True, False])
+@pytest.mark.parametrize("scale", [1.0, 2.5])
+def test_route_bwd_matches_central_differences(score_fn, renorm, scale):
+    rng = np.random.default_rng(31)
+    T, E, K = 12, 16, 4
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    if score_fn == "softmax":
+        idx, _ = oracle.route_softmax(logits, K, renorm, scale)
+    else:
+        idx, _ = oracle.route_sigmoid_grouped(logits, None, K, 1, 1, 1, renorm, scale)
+    gw = rng.standard_normal((T, K))
+    g = oracle.route_bwd(logits, idx, gw, score_fn, renorm, scale)
+    eps = 1e-6
+    for t in range(T):
+        for e in range(E):
+            lp = logits[t].astype(np.float64).copy()
+            lm = lp.copy()
+            lp[e] += eps
+            lm[e] -= eps
+            fd = (np.dot(gw[t], weights_fp64(lp, idx[t], score_fn, renorm, scale)) -
+                  np.dot(gw[t], weights_fp64(lm, idx[t], score_fn, renorm, scale))) / (2 * eps)
+            assert abs(fd - g[t, e]) <= 1e-7 * (1 + abs(fd)), (t, e, fd, g[t, e])
+
+
+def test_route_bwd_invariants():
+    rng = np.random.default_rng(32)
+    logits = rng.standard_normal((50, 32)).astype(np.float32)
+    idx, w = oracle.route_softmax(logits, 6)
+    gw = rng.standard_normal((50, 6))
+    g = oracle.route_bwd(logits, idx, gw)
+    # softmax is shift invariant: the gradient sums to zero over the logits
+    assert np.abs(g.sum(1)).max() < 1e-12
+    # only the selected logits move a renormalised softmax
+    mask = np.zeros_like(g, bool)
+    np.put_along_axis(mask, idx, True, 1)
+    assert (g[~mask] == 0).all()
+    # a gradient proportional to the weights (uniform rescaling) changes nothing
+    g2 = oracle.route_bwd(logits, idx, np.ones_like(gw))
+    assert np.abs(g2).max() < 1e-15
