@@ -32,7 +32,8 @@ EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_handle_create", "moe
            "moe_route_topk", "moe_dispatch_layout", "moe_layout_view", "moe_dispatch",
            "moe_combine", "moe_combine_bwd", "moe_dispatch_bwd", "moe_scale_rows",
            "moe_scale_rows_bwd", "moe_read_device_status", "moe_clear_device_status",
-           "moe_dispatch_layout_static", "moe_route_bwd")
+           "moe_dispatch_layout_static", "moe_route_bwd", "moe_expand", "moe_combine_partial",
+           "moe_combine_reduce")
 MOE_LAYOUT_STATIC_COUNTERS = 65536
 MOE_LAYOUT_TILE_TOKENS = 512
 
@@ -89,6 +90,9 @@ def lib():
             "moe_clear_device_status": ([P, P], st),
             "moe_dispatch_layout_static": ([P, P, i32, P, P, P], st),
             "moe_route_bwd": ([P, P, P, P, i32, P, P], st),
+            "moe_expand": ([P, P, i32, i32, P, P], st),
+            "moe_combine_partial": ([P, P, i32, i32, P, P, P], st),
+            "moe_combine_reduce": ([P, P, i32, i32, P, P], st),
         }
         for name, (args, res) in sigs.items():
             f = getattr(L, name)
@@ -268,6 +272,32 @@ def moe_dispatch_bwd(h, grecv, gx, stream=None):
                                                       _ptr(gx), _stream(stream)))
 
 
+def moe_expand(h, send, recv, stream=None):
+    H = send.shape[1]
+    _req(send, None, (h.T * min(h.K, h.R), H), "send")
+    _req(recv, send.dtype, (h.T * h.K, H), "recv")
+    _check("moe_expand", lib().moe_expand(h.ptr, _ptr(send), H, _row_dtype(send), _ptr(recv),
+                                          _stream(stream)))
+
+
+def moe_combine_partial(h, y, w, partial, stream=None):
+    H = y.shape[1]
+    _req(y, None, (h.T * h.K, H), "y")
+    _req(w, torch.float32, (h.T, h.K), "w")
+    _req(partial, y.dtype, (h.T * min(h.K, h.R), H), "partial")
+    _check("moe_combine_partial", lib().moe_combine_partial(h.ptr, _ptr(y), H, _row_dtype(y),
+                                                            _ptr(w), _ptr(partial), _stream(stream)))
+
+
+def moe_combine_reduce(h, partial, out, stream=None):
+    H = partial.shape[1]
+    _req(partial, None, (h.T * min(h.K, h.R), H), "partial")
+    _req(out, partial.dtype, (h.T, H), "out")
+    _check("moe_combine_reduce", lib().moe_combine_reduce(h.ptr, _ptr(partial), H,
+                                                          _row_dtype(partial), _ptr(out),
+                                                          _stream(stream)))
+
+
 def moe_scale_rows(h, hrows, recv_w, hs, stream=None):
     I = hrows.shape[1]
     _req(hrows, None, (h.T * h.K, I), "h")
@@ -395,6 +425,24 @@ class MoeRouter:
         gx = torch.empty(max(self.h.T, 0), grecv.shape[1], dtype=grecv.dtype, device=grecv.device)
         moe_dispatch_bwd(self.h, grecv, gx, stream)
         return gx
+
+    def expand(self, send, stream=None):
+        recv = torch.empty(max(self.h.T, 0) * self.h.K, send.shape[1], dtype=send.dtype,
+                           device=send.device)
+        moe_expand(self.h, send, recv, stream)
+        return recv
+
+    def combine_partial(self, y, w=None, stream=None):
+        partial = torch.empty(max(self.h.T, 0) * min(self.h.K, self.h.R), y.shape[1],
+                              dtype=y.dtype, device=y.device)
+        moe_combine_partial(self.h, y, w, partial, stream)
+        return partial
+
+    def combine_reduce(self, partial, stream=None):
+        out = torch.empty(max(self.h.T, 0), partial.shape[1], dtype=partial.dtype,
+                          device=partial.device)
+        moe_combine_reduce(self.h, partial, out, stream)
+        return out
 
     def scale_rows(self, hrows, recv_w, stream=None):
         hs = torch.empty_like(hrows)

@@ -275,6 +275,34 @@ moe_status moe_dispatch_bwd(const moe_handle* h, const void* d_grecv, int32_t H,
   return from_cuda(moe::launch_combine(h, d_grecv, H, dtype, nullptr, d_gx, as_stream(stream)));
 }
 
+moe_status moe_expand(const moe_handle* h, const void* d_send, int32_t H, int32_t dtype,
+                      void* d_recv, void* stream) {
+  if (!h) return MOE_ERR_INVALID;
+  if (h->T < 0) return MOE_ERR_STATE;
+  if (h->T == 0) return empty_rows_ok(H, dtype) ? MOE_OK : MOE_ERR_INVALID;
+  if (!row_ok(d_send, H, dtype) || !row_ok(d_recv, H, dtype)) return MOE_ERR_INVALID;
+  return from_cuda(moe::launch_staged(0, h, d_send, H, dtype, nullptr, d_recv, as_stream(stream)));
+}
+
+moe_status moe_combine_partial(const moe_handle* h, const void* d_y, int32_t H, int32_t dtype,
+                               const float* d_w, void* d_partial, void* stream) {
+  if (!h) return MOE_ERR_INVALID;
+  if (h->T < 0) return MOE_ERR_STATE;
+  if (h->T == 0) return empty_rows_ok(H, dtype) ? MOE_OK : MOE_ERR_INVALID;
+  if (!row_ok(d_y, H, dtype) || !row_ok(d_partial, H, dtype) || !aligned(d_w, 4))
+    return MOE_ERR_INVALID;
+  return from_cuda(moe::launch_staged(1, h, d_y, H, dtype, d_w, d_partial, as_stream(stream)));
+}
+
+moe_status moe_combine_reduce(const moe_handle* h, const void* d_partial, int32_t H,
+                              int32_t dtype, void* d_out, void* stream) {
+  if (!h) return MOE_ERR_INVALID;
+  if (h->T < 0) return MOE_ERR_STATE;
+  if (h->T == 0) return empty_rows_ok(H, dtype) ? MOE_OK : MOE_ERR_INVALID;
+  if (!row_ok(d_partial, H, dtype) || !row_ok(d_out, H, dtype)) return MOE_ERR_INVALID;
+  return from_cuda(moe::launch_staged(2, h, d_partial, H, dtype, nullptr, d_out, as_stream(stream)));
+}
+
 moe_status moe_scale_rows(const moe_handle* h, const void* d_h, int32_t I, int32_t dtype,
                           const float* d_recv_w, void* d_hs, void* stream) {
   if (!h) return MOE_ERR_INVALID;

@@ -54,6 +54,11 @@ cudaError_t launch_combine(const moe_handle* h, const void* y, int H, int dtype,
 cudaError_t launch_combine_bwd(const moe_handle* h, const void* g, const void* y, int H, int dtype,
                                const float* w, void* gy, float* gw, cudaStream_t s);
 
+// op 0: expand send rows to receive rows; 1: combine into per-send-row
+// partials; 2: reduce the partials to token rows
+cudaError_t launch_staged(int op, const moe_handle* h, const void* src, int H, int dtype,
+                          const float* w, void* dst, cudaStream_t s);
+
 cudaError_t launch_scale_rows(const moe_handle* h, const void* hrows, int I, int dtype,
                               const float* recv_w, void* hs, cudaStream_t s);
 

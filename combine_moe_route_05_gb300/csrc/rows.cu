@@ -214,6 +214,138 @@ __global__ void __launch_bounds__(kGatherMaxThreads, 2) combine_bwd_kernel(RowAr
 }
 
 // ---------------------------------------------------------------------------
+// staged (wire-faithful) mode: a token's row goes to each destination rank
+// once (its send row); the receiving side expands it to the rows of its
+// experts there, and the combine returns one partial row per send row, which
+// the token's side then adds up.  One block per token; a send row's entries
+// are the k with equal send_row_of, handled from the first such k.
+
+struct StagedArgs {
+  const uint8_t* src;  // send rows (expand), y (partial), partial rows (reduce)
+  const float* w;
+  const int32_t* pos;
+  const int32_t* send_row_of;
+  uint8_t* dst;        // recv (expand), partial (partial), out (reduce)
+  int64_t row_bytes;
+  int nvec;
+  int T, K;
+};
+
+template <int KMAX>
+__device__ __forceinline__ uint32_t load_send_entries(const StagedArgs& a, int t, int (&p)[KMAX],
+                                                      int (&sr)[KMAX]) {
+  uint32_t first = 0;  // bit k: first entry of its send row
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    p[k] = -1;
+    sr[k] = -1;
+    if (k < a.K) {
+      p[k] = __ldg(a.pos + static_cast<size_t>(t) * a.K + k);
+      sr[k] = __ldg(a.send_row_of + static_cast<size_t>(t) * a.K + k);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    bool f = sr[k] >= 0;
+#pragma unroll
+    for (int j = 0; j < k; ++j)
+      if (sr[j] == sr[k]) f = false;
+    if (f) first |= 1u << k;
+  }
+  return first;
+}
+
+// recv[pos[t,k]] = send[send_row_of[t,k]]: each send row read once
+template <int KMAX>
+__global__ void __launch_bounds__(1024) expand_kernel(StagedArgs a) {
+  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+    int p[KMAX], sr[KMAX];
+    const uint32_t first = load_send_entries<KMAX>(a, t, p, sr);
+    for (int v = threadIdx.x; v < a.nvec; v += blockDim.x) {
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        if (!((first >> k) & 1u)) continue;
+        const Vec16 val = ld_stream(a.src + static_cast<int64_t>(sr[k]) * a.row_bytes + v * 16);
+#pragma unroll
+        for (int j = k; j < KMAX; ++j)
+          if (sr[j] == sr[k] && p[j] >= 0)
+            st_vec(a.dst + static_cast<int64_t>(p[j]) * a.row_bytes + v * 16, val);
+      }
+    }
+  }
+}
+
+// partial[s] = round(sum over the entries of send row s, in k order, of
+// w_k * y[pos[t,k]])
+template <typename Elt, int KMAX, bool WEIGHTED>
+__global__ void __launch_bounds__(kGatherMaxThreads) combine_partial_kernel(StagedArgs a) {
+  using VT = VecTraits<Elt>;
+  constexpr int N = VT::N;
+  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+    int p[KMAX], sr[KMAX];
+    const uint32_t first = load_send_entries<KMAX>(a, t, p, sr);
+    float wk[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      wk[k] = (WEIGHTED && k < a.K) ? __ldg(a.w + static_cast<size_t>(t) * a.K + k) : 1.0f;
+    for (int v = threadIdx.x; v < a.nvec; v += blockDim.x) {
+      Vec16 in[KMAX];
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if (p[k] >= 0) in[k] = ld_stream(a.src + static_cast<int64_t>(p[k]) * a.row_bytes + v * 16);
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        if (!((first >> k) & 1u)) continue;
+        float acc[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) acc[i] = 0.0f;
+#pragma unroll
+        for (int j = k; j < KMAX; ++j) {
+          if (sr[j] != sr[k] || p[j] < 0) continue;
+          float f[N];
+          VT::to_f32(in[j], f);
+#pragma unroll
+          for (int i = 0; i < N; ++i)
+            acc[i] = WEIGHTED ? __fmaf_rn(wk[j], f[i], acc[i]) : __fadd_rn(acc[i], f[i]);
+        }
+        st_vec(a.dst + static_cast<int64_t>(sr[k]) * a.row_bytes + v * 16, VT::from_f32(acc));
+      }
+    }
+  }
+}
+
+// out[t] = round(sum of the token's partial rows, each send row once, in the
+// order of its first entry)
+template <typename Elt, int KMAX>
+__global__ void __launch_bounds__(kGatherMaxThreads) combine_reduce_kernel(StagedArgs a) {
+  using VT = VecTraits<Elt>;
+  constexpr int N = VT::N;
+  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+    int p[KMAX], sr[KMAX];
+    const uint32_t first = load_send_entries<KMAX>(a, t, p, sr);
+    for (int v = threadIdx.x; v < a.nvec; v += blockDim.x) {
+      Vec16 in[KMAX];
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if ((first >> k) & 1u)
+          in[k] = ld_stream(a.src + static_cast<int64_t>(sr[k]) * a.row_bytes + v * 16);
+      float acc[N];
+#pragma unroll
+      for (int i = 0; i < N; ++i) acc[i] = 0.0f;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        if (!((first >> k) & 1u)) continue;
+        float f[N];
+        VT::to_f32(in[k], f);
+#pragma unroll
+        for (int i = 0; i < N; ++i) acc[i] = __fadd_rn(acc[i], f[i]);
+      }
+      st_vec(a.dst + static_cast<int64_t>(t) * a.row_bytes + v * 16, VT::from_f32(acc));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // absorption: hs[r] = round(h[r] * recv_w[r]) over the valid receive rows
 
 template <typename Elt>
@@ -473,6 +605,55 @@ cudaError_t launch_scale_rows_bwd(const moe_handle* h, const void* ghs, const vo
                                    static_cast<const uint8_t*>(hrows), recv_w,
                                    static_cast<uint8_t*>(gh), gw, h->pos, entries, row_bytes, nvec);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_staged(int op, const moe_handle* h, const void* src, int H, int dtype,
+                          const float* w, void* dst, cudaStream_t s) {
+  StagedArgs a{};
+  a.src = static_cast<const uint8_t*>(src);
+  a.w = w;
+  a.pos = h->pos;
+  a.send_row_of = h->send_row_of;
+  a.dst = static_cast<uint8_t*>(dst);
+  a.row_bytes = static_cast<int64_t>(H) * (dtype == MOE_BF16 ? 2 : 4);
+  a.nvec = static_cast<int>(a.row_bytes / 16);
+  a.T = h->T;
+  a.K = h->cfg.top_k;
+  if (a.T == 0) return cudaSuccess;
+  const bool k8 = a.K <= 8;
+  if (op == 0) {  // expand: one block per token, a thread per vector
+    const int block = threads_for(a.nvec, 1);
+    const int grid = a.T < 1048576 ? a.T : 1048576;
+    if (k8) expand_kernel<8><<<grid, block, 0, s>>>(a);
+    else expand_kernel<16><<<grid, block, 0, s>>>(a);
+    return cudaGetLastError();
+  }
+  const int block = gather_threads(a.nvec);
+#define MOE_STAGED_LAUNCH(KERNEL)                                                            \
+  do {                                                                                       \
+    auto kern = KERNEL;                                                                      \
+    kern<<<grid_for(reinterpret_cast<const void*>(kern), block, 0, h->num_sms, a.T), block, 0, \
+           s>>>(a);                                                                          \
+  } while (0)
+  if (op == 1) {
+    if (dtype == MOE_BF16) {
+      if (k8) { if (w) MOE_STAGED_LAUNCH((combine_partial_kernel<__nv_bfloat16, 8, true>)); else MOE_STAGED_LAUNCH((combine_partial_kernel<__nv_bfloat16, 8, false>)); }
+      else { if (w) MOE_STAGED_LAUNCH((combine_partial_kernel<__nv_bfloat16, 16, true>)); else MOE_STAGED_LAUNCH((combine_partial_kernel<__nv_bfloat16, 16, false>)); }
+    } else {
+      if (k8) { if (w) MOE_STAGED_LAUNCH((combine_partial_kernel<float, 8, true>)); else MOE_STAGED_LAUNCH((combine_partial_kernel<float, 8, false>)); }
+      else { if (w) MOE_STAGED_LAUNCH((combine_partial_kernel<float, 16, true>)); else MOE_STAGED_LAUNCH((combine_partial_kernel<float, 16, false>)); }
+    }
+  } else {
+    if (dtype == MOE_BF16) {
+      if (k8) MOE_STAGED_LAUNCH((combine_reduce_kernel<__nv_bfloat16, 8>));
+      else MOE_STAGED_LAUNCH((combine_reduce_kernel<__nv_bfloat16, 16>));
+    } else {
+      if (k8) MOE_STAGED_LAUNCH((combine_reduce_kernel<float, 8>));
+      else MOE_STAGED_LAUNCH((combine_reduce_kernel<float, 16>));
+    }
+  }
+#undef MOE_STAGED_LAUNCH
   return cudaGetLastError();
 }
 

@@ -285,6 +285,29 @@ moe_status moe_dispatch_bwd(const moe_handle* h, const void* d_grecv, int32_t H,
                             void* d_gx, void* stream);
 
 /*
+ * Staged (wire-faithful) mode ([AutoEP-DeepEP] "Why": a token is sent once
+ * per destination rank rather than once per selected expert, the receiving
+ * side groups arrivals by expert, and the combine brings back one reduced row
+ * per (token, rank)).  The send rows d_send [T*min(K,R),H] come from
+ * moe_dispatch; the virtual ranks are expert partitions of this one GPU.
+ *
+ * moe_expand: the receiving side's expansion of arrived rows to expert rows,
+ *   d_recv[pos[t,k]] = d_send[send_row_of[t,k]]  (each send row read once).
+ * moe_combine_partial: stage 1, one partial row per send row s,
+ *   d_partial[s] = round( fp32 sum, in k order, of w[t,k] * d_y[pos[t,k]]
+ *   over the entries with send_row_of[t,k] == s )  (d_w NULL: plain sum);
+ *   d_partial [T*min(K,R),H] in the row dtype (what travels back).
+ * moe_combine_reduce: stage 2, d_out[t] = round( fp32 sum of the token's
+ *   partial rows, each send row once, in the order of its first entry ).
+ */
+moe_status moe_expand(const moe_handle* h, const void* d_send, int32_t H, int32_t dtype,
+                      void* d_recv, void* stream);
+moe_status moe_combine_partial(const moe_handle* h, const void* d_y, int32_t H, int32_t dtype,
+                               const float* d_w, void* d_partial, void* stream);
+moe_status moe_combine_reduce(const moe_handle* h, const void* d_partial, int32_t H,
+                              int32_t dtype, void* d_out, void* stream);
+
+/*
  * Router-score absorption ([Titan-absorb] "Implementation": the W2 input is
  * scaled in float32 and restored to its dtype before the grouped GEMM):
  *   d_hs[r] = round(d_h[r] * d_recv_w[r]) for the T*K receive rows r of the

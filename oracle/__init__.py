@@ -52,6 +52,12 @@ def lib():
         L.orc_dispatch_f64.restype = None
         L.orc_route_bwd.argtypes = [P, i64, i32, i32, i32, i32, d, P, P, P]
         L.orc_route_bwd.restype = i32
+        L.orc_expand.argtypes = [P, i64, i64, i32, P, P, P]
+        L.orc_expand.restype = None
+        L.orc_combine_partial.argtypes = [P, i32, i64, i64, i32, P, P, P, P]
+        L.orc_combine_partial.restype = None
+        L.orc_combine_reduce.argtypes = [P, i32, i64, i64, i32, P, P]
+        L.orc_combine_reduce.restype = None
         L.orc_f32_to_bf16.argtypes = [P, i64, P]
         L.orc_f32_to_bf16.restype = None
         _lib = L
@@ -195,6 +201,36 @@ def dispatch_bwd(grecv, lay):
     gx = np.empty((lay.T, H), grecv.dtype)
     lib().orc_dispatch_bwd(_p(grecv), _dtype_of(grecv), H, lay.T, lay.K, _p(lay.pos), _p(gx))
     return gx
+
+
+def expand(send, lay):
+    """recv[pos[t,k]] = send[send_row_of[t,k]] (rows of dropped entries stay 0)."""
+    send = np.ascontiguousarray(send)
+    H = send.shape[1]
+    recv = np.zeros((lay.T * lay.K, H), send.dtype)
+    lib().orc_expand(_p(send), H * send.itemsize, lay.T, lay.K, _p(lay.pos), _p(lay.send_row_of),
+                     _p(recv))
+    return recv
+
+
+def combine_partial(y, lay, w=None):
+    """Stage-1 partial rows [T*min(K,R), H] (rows past S stay 0)."""
+    y = np.ascontiguousarray(y)
+    H = y.shape[1]
+    partial = np.zeros((lay.T * min(lay.K, lay.R), H), y.dtype)
+    wc = None if w is None else _c(w, np.float32)
+    lib().orc_combine_partial(_p(y), _dtype_of(y), H, lay.T, lay.K, _p(lay.pos),
+                              _p(lay.send_row_of), _p(wc), _p(partial))
+    return partial
+
+
+def combine_reduce(partial, lay):
+    partial = np.ascontiguousarray(partial)
+    H = partial.shape[1]
+    out = np.empty((lay.T, H), partial.dtype)
+    lib().orc_combine_reduce(_p(partial), _dtype_of(partial), H, lay.T, lay.K,
+                             _p(lay.send_row_of), _p(out))
+    return out
 
 
 def scale_rows(h, recv_w, rows=None):

@@ -526,4 +526,71 @@ int orc_route_bwd(const float* logits, int64_t T, int E, int K, int score_fn, in
   return 0;
 }
 
+// Staged (wire-faithful) dispatch and combine ([AutoEP-DeepEP] "Why": a
+// token goes to each destination rank once, not once per selected expert;
+// the receiving side groups the arrivals by expert, and the combine returns
+// one reduced row per (token, rank)).  The send rows come from orc_dispatch
+// with `send`; then:
+//
+// expand: the receiving side copies each arrived row to the rows of its
+// experts on that rank:  recv[pos[t,k]] = send[send_row_of[t,k]].
+void orc_expand(const void* send, int64_t row_bytes, int64_t T, int K, const int32_t* pos,
+                const int32_t* send_row_of, void* recv) {
+  for (int64_t t = 0; t < T; ++t)
+    for (int k = 0; k < K; ++k) {
+      const int64_t p = pos[t * K + k];
+      if (p < 0) continue;
+      std::memcpy(static_cast<char*>(recv) + p * row_bytes,
+                  static_cast<const char*>(send) + static_cast<int64_t>(send_row_of[t * K + k]) * row_bytes,
+                  static_cast<size_t>(row_bytes));
+    }
+}
+
+// combine, stage 1 (on the expert side): one partial row per send row s of
+// token t, the fp32 sum in k order of w[t,k] * y[pos[t,k]] over the entries k
+// with send_row_of[t,k] == s (fma; acc + y when w is NULL), rounded once to
+// the row dtype (what travels back).
+void orc_combine_partial(const void* y, int dtype, int64_t H, int64_t T, int K,
+                         const int32_t* pos, const int32_t* send_row_of, const float* w,
+                         void* partial) {
+  for (int64_t t = 0; t < T; ++t)
+    for (int k = 0; k < K; ++k) {
+      const int32_t s = send_row_of[t * K + k];
+      if (s < 0) continue;
+      bool first = true;
+      for (int j = 0; j < k; ++j)
+        if (send_row_of[t * K + j] == s) first = false;
+      if (!first) continue;
+      for (int64_t h = 0; h < H; ++h) {
+        float acc = 0.0f;
+        for (int j = k; j < K; ++j) {
+          if (send_row_of[t * K + j] != s) continue;
+          const float v = load_elem(y, dtype, static_cast<int64_t>(pos[t * K + j]) * H + h);
+          acc = w ? std::fma(w[t * K + j], v, acc) : acc + v;
+        }
+        store_elem(partial, dtype, static_cast<int64_t>(s) * H + h, acc);
+      }
+    }
+}
+
+// combine, stage 2 (back on the token's side): the fp32 sum of the token's
+// partial rows, each distinct send row once, in the order its first entry
+// appears in k, rounded once.
+void orc_combine_reduce(const void* partial, int dtype, int64_t H, int64_t T, int K,
+                        const int32_t* send_row_of, void* out) {
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t h = 0; h < H; ++h) {
+      float acc = 0.0f;
+      for (int k = 0; k < K; ++k) {
+        const int32_t s = send_row_of[t * K + k];
+        if (s < 0) continue;
+        bool first = true;
+        for (int j = 0; j < k; ++j)
+          if (send_row_of[t * K + j] == s) first = false;
+        if (first) acc = acc + load_elem(partial, dtype, static_cast<int64_t>(s) * H + h);
+      }
+      store_elem(out, dtype, t * H + h, acc);
+    }
+}
+
 }  // extern "C"

@@ -634,3 +634,43 @@ def test_route_bwd_invariants():
     # a gradient proportional to the weights (uniform rescaling) changes nothing
     g2 = oracle.route_bwd(logits, idx, np.ones_like(gw))
     assert np.abs(g2).max() < 1e-15
+
+
+# ----------------------------------------------------------------------------
+# staged (wire-faithful) dispatch and combine
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.uint16])
+def test_dispatch_through_send_rows_equals_direct_dispatch(dtype):
+    idx, L, w, x, y, g = small_case(40, T=64, H=24, E=16, K=4, R=4, dtype=dtype)
+    recv, _, send = oracle.dispatch(x, L, w, with_send=True)
+    assert (oracle.expand(send, L) == recv).all()
+    # each token travels once per destination rank
+    assert L.S == sum(len({int(e) // (L.E // L.R) for e in row}) for row in idx)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.uint16])
+def test_staged_combine_with_one_rank_is_the_combine(dtype):
+    """R = 1: one send row per token holding all K entries, so stage 1 is the
+    combine itself and stage 2 adds it to zero."""
+    idx, L, w, x, y, g = small_case(41, T=50, H=24, E=8, K=4, R=1, dtype=dtype)
+    staged = oracle.combine_reduce(oracle.combine_partial(y, L, w), L)
+    assert (staged == oracle.combine(y, L, w)).all()
+
+
+def test_staged_combine_identity_experts_give_x_times_K_in_bf16():
+    idx, L, w, x, y, g = small_case(42, T=64, H=32, E=16, K=8, R=4, dtype=np.uint16)
+    recv, _, send = oracle.dispatch(x, L, with_send=True)
+    out = oracle.combine_reduce(oracle.combine_partial(oracle.expand(send, L), L), L)
+    ref = synth.to_bf16_bits(oracle.bf16_to_f32(x) * np.float32(8))
+    assert (out == ref).all()
+
+
+def test_staged_combine_within_rounding_of_exact_sum():
+    idx, L, w, x, y, g = small_case(43, T=64, H=40, E=16, K=6, R=4)
+    staged = oracle.combine_reduce(oracle.combine_partial(y, L, w), L)
+    exact = oracle.combine_f64(y, L, w)
+    absmag = oracle.combine_f64(np.abs(y), L, np.abs(w))
+    # stage 1 rounds each partial once and stage 2 adds at most min(K,R) of them
+    bound = (6 + 4 + 4) * 2.0 ** -24 * absmag * 1.01
+    assert (np.abs(staged - exact) <= bound).all()
