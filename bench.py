@@ -381,6 +381,45 @@ def run_gpu(args, wl):
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
     assert moe.moe_read_device_status(h) == 0
 
+    # widened rows, timed apart from the step: router backward to the logits,
+    # and the staged (token once per destination rank) dispatch and combine
+    extras = None
+    if not args.no_extras:
+        def time_op(fn, reps=max(3, args.steps)):
+            for _ in range(2):
+                fn()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            for _ in range(reps):
+                fn()
+            b_.record(stream)
+            torch.cuda.synchronize()
+            return a_.elapsed_time(b_) / reps
+        R = wl.R
+        step()
+        glogits = torch.empty(T, E, dtype=torch.float32, device=device)
+        t_rb = time_op(lambda: moe.moe_route_bwd(h, logits, idx, gw, glogits))
+        send = torch.empty(T * min(K, R), H, dtype=bf, device=device)
+        partial = torch.empty_like(send)
+        t_ds = time_op(lambda: moe.moe_dispatch(h, x, w, recv, recv_w, send))
+        t_ex = time_op(lambda: moe.moe_expand(h, send, recv))
+        t_cp = time_op(lambda: moe.moe_combine_partial(h, y, w, partial))
+        t_cr = time_op(lambda: moe.moe_combine_reduce(h, partial, out))
+        S = int(moe.layout_tensors(h)["S"].item())
+        row = H * 2
+        extras = {
+            "route_bwd": {"ms": t_rb, "gbs": (T * E * 4 + T * K * 12) / (t_rb / 1e3) / 1e9},
+            "staged": {
+                "dedup_factor": T * K / S, "send_rows": S,
+                "dispatch_with_send_ms": t_ds, "expand_ms": t_ex, "combine_partial_ms": t_cp,
+                "combine_reduce_ms": t_cr,
+                "dispatch_with_send_gbs": (T + T * K + S) * row / (t_ds / 1e3) / 1e9,
+                "expand_gbs": (S + T * K) * row / (t_ex / 1e3) / 1e9,
+                "combine_partial_gbs": (T * K + S) * row / (t_cp / 1e3) / 1e9,
+                "combine_reduce_gbs": (S + T) * row / (t_cr / 1e3) / 1e9},
+        }
+        assert moe.moe_read_device_status(h) == 0
+
     if rank != 0:
         return
     peak, peak_src = read_peaks()
@@ -410,6 +449,7 @@ def run_gpu(args, wl):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "kernel_source": kernel_source_hash(),
+        "extras": extras,
     }
     print(json.dumps(line), flush=True)
 
@@ -426,6 +466,7 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extras", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -44,14 +44,14 @@ class MoeConfig(ctypes.Structure):
                 ("num_groups", ctypes.c_int32), ("topk_groups", ctypes.c_int32),
                 ("group_score_topk", ctypes.c_int32), ("renorm", ctypes.c_int32),
                 ("route_scale", ctypes.c_double), ("max_tokens", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("pad_align", ctypes.c_int32)]
 
 
 class MoeLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "cnt_e", "off_e", "cnt_send_r", "off_send_r", "cnt_recv_r", "off_recv_r", "pos",
         "recv_token", "recv_k", "send_token", "send_row_of", "recv_send_row", "S")] + [
-        ("num_tokens", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+        ("num_tokens", ctypes.c_int32), ("pad_align", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -144,11 +144,11 @@ def _req(t, dtype=None, shape=None, name="tensor"):
 
 
 def make_config(num_experts, top_k, num_ranks, max_tokens, score_fn="softmax", num_groups=1,
-                topk_groups=1, group_score_topk=1, renorm=True, route_scale=1.0):
+                topk_groups=1, group_score_topk=1, renorm=True, route_scale=1.0, pad_align=0):
     fn = {"softmax": MOE_SCORE_SOFTMAX, "sigmoid": MOE_SCORE_SIGMOID}[score_fn] \
         if isinstance(score_fn, str) else int(score_fn)
     return MoeConfig(num_experts, top_k, num_ranks, fn, num_groups, topk_groups, group_score_topk,
-                     int(bool(renorm)), float(route_scale), max_tokens, 0)
+                     int(bool(renorm)), float(route_scale), max_tokens, int(pad_align))
 
 
 def moe_workspace_bytes(cfg):
@@ -199,6 +199,15 @@ class Handle:
     def R(self):
         return self.cfg.num_ranks
 
+    @property
+    def pad(self):
+        return max(1, self.cfg.pad_align)
+
+    @property
+    def recv_rows(self):
+        """Rows of a receive-row tensor for the current layout."""
+        return max(self.T, 0) * self.K + self.E * (self.pad - 1)
+
 
 def moe_route_topk(h, logits, bias, idx, w, stream=None):
     T = logits.shape[0]
@@ -236,9 +245,9 @@ def moe_layout_view(h):
 def moe_dispatch(h, x, w, recv, recv_w, send=None, stream=None):
     T, H = x.shape
     _req(x, None, (h.T, H), "x")
-    _req(recv, x.dtype, (h.T * h.K, H), "recv")
+    _req(recv, x.dtype, (h.recv_rows, H), "recv")
     _req(w, torch.float32, (h.T, h.K), "w")
-    _req(recv_w, torch.float32, (h.T * h.K,), "recv_w")
+    _req(recv_w, torch.float32, (h.recv_rows,), "recv_w")
     _req(send, x.dtype, (h.T * min(h.K, h.R), H), "send")
     _check("moe_dispatch", lib().moe_dispatch(h.ptr, _ptr(x), H, _row_dtype(x), _ptr(w), _ptr(recv),
                                               _ptr(recv_w), _ptr(send), _stream(stream)))
@@ -246,7 +255,7 @@ def moe_dispatch(h, x, w, recv, recv_w, send=None, stream=None):
 
 def moe_combine(h, y, w, out, stream=None):
     H = y.shape[1]
-    _req(y, None, (h.T * h.K, H), "y")
+    _req(y, None, (h.recv_rows, H), "y")
     _req(w, torch.float32, (h.T, h.K), "w")
     _req(out, y.dtype, (h.T, H), "out")
     _check("moe_combine", lib().moe_combine(h.ptr, _ptr(y), H, _row_dtype(y), _ptr(w), _ptr(out),
@@ -256,9 +265,9 @@ def moe_combine(h, y, w, out, stream=None):
 def moe_combine_bwd(h, g, y, w, gy, gw, stream=None):
     H = g.shape[1]
     _req(g, None, (h.T, H), "g")
-    _req(y, g.dtype, (h.T * h.K, H), "y")
+    _req(y, g.dtype, (h.recv_rows, H), "y")
     _req(w, torch.float32, (h.T, h.K), "w")
-    _req(gy, g.dtype, (h.T * h.K, H), "gy")
+    _req(gy, g.dtype, (h.recv_rows, H), "gy")
     _req(gw, torch.float32, (h.T, h.K), "gw")
     _check("moe_combine_bwd", lib().moe_combine_bwd(h.ptr, _ptr(g), _ptr(y), H, _row_dtype(g), _ptr(w),
                                                     _ptr(gy), _ptr(gw), _stream(stream)))
@@ -266,7 +275,7 @@ def moe_combine_bwd(h, g, y, w, gy, gw, stream=None):
 
 def moe_dispatch_bwd(h, grecv, gx, stream=None):
     H = grecv.shape[1]
-    _req(grecv, None, (h.T * h.K, H), "grecv")
+    _req(grecv, None, (h.recv_rows, H), "grecv")
     _req(gx, grecv.dtype, (h.T, H), "gx")
     _check("moe_dispatch_bwd", lib().moe_dispatch_bwd(h.ptr, _ptr(grecv), H, _row_dtype(grecv),
                                                       _ptr(gx), _stream(stream)))
@@ -275,14 +284,14 @@ def moe_dispatch_bwd(h, grecv, gx, stream=None):
 def moe_expand(h, send, recv, stream=None):
     H = send.shape[1]
     _req(send, None, (h.T * min(h.K, h.R), H), "send")
-    _req(recv, send.dtype, (h.T * h.K, H), "recv")
+    _req(recv, send.dtype, (h.recv_rows, H), "recv")
     _check("moe_expand", lib().moe_expand(h.ptr, _ptr(send), H, _row_dtype(send), _ptr(recv),
                                           _stream(stream)))
 
 
 def moe_combine_partial(h, y, w, partial, stream=None):
     H = y.shape[1]
-    _req(y, None, (h.T * h.K, H), "y")
+    _req(y, None, (h.recv_rows, H), "y")
     _req(w, torch.float32, (h.T, h.K), "w")
     _req(partial, y.dtype, (h.T * min(h.K, h.R), H), "partial")
     _check("moe_combine_partial", lib().moe_combine_partial(h.ptr, _ptr(y), H, _row_dtype(y),
@@ -300,19 +309,19 @@ def moe_combine_reduce(h, partial, out, stream=None):
 
 def moe_scale_rows(h, hrows, recv_w, hs, stream=None):
     I = hrows.shape[1]
-    _req(hrows, None, (h.T * h.K, I), "h")
-    _req(recv_w, torch.float32, (h.T * h.K,), "recv_w")
-    _req(hs, hrows.dtype, (h.T * h.K, I), "hs")
+    _req(hrows, None, (h.recv_rows, I), "h")
+    _req(recv_w, torch.float32, (h.recv_rows,), "recv_w")
+    _req(hs, hrows.dtype, (h.recv_rows, I), "hs")
     _check("moe_scale_rows", lib().moe_scale_rows(h.ptr, _ptr(hrows), I, _row_dtype(hrows),
                                                   _ptr(recv_w), _ptr(hs), _stream(stream)))
 
 
 def moe_scale_rows_bwd(h, ghs, hrows, recv_w, gh, gw, stream=None):
     I = hrows.shape[1]
-    _req(ghs, None, (h.T * h.K, I), "ghs")
-    _req(hrows, ghs.dtype, (h.T * h.K, I), "h")
-    _req(recv_w, torch.float32, (h.T * h.K,), "recv_w")
-    _req(gh, ghs.dtype, (h.T * h.K, I), "gh")
+    _req(ghs, None, (h.recv_rows, I), "ghs")
+    _req(hrows, ghs.dtype, (h.recv_rows, I), "h")
+    _req(recv_w, torch.float32, (h.recv_rows,), "recv_w")
+    _req(gh, ghs.dtype, (h.recv_rows, I), "gh")
     _req(gw, torch.float32, (h.T, h.K), "gw")
     _check("moe_scale_rows_bwd", lib().moe_scale_rows_bwd(h.ptr, _ptr(ghs), _ptr(hrows), I,
                                                           _row_dtype(ghs), _ptr(recv_w), _ptr(gh),
@@ -333,11 +342,12 @@ LAYOUT_FIELDS = ("cnt_e", "off_e", "cnt_send_r", "off_send_r", "cnt_recv_r", "of
                  "recv_token", "recv_k", "send_token", "send_row_of", "recv_send_row", "S")
 
 
-def layout_sizes(T, K, E, R):
+def layout_sizes(T, K, E, R, pad=1):
     """Element counts (int32) of the layout arrays for T tokens."""
+    RR = T * K + E * (max(1, pad) - 1)
     return {"cnt_e": E, "off_e": E + 1, "cnt_send_r": R, "off_send_r": R + 1, "cnt_recv_r": R,
-            "off_recv_r": R + 1, "pos": T * K, "recv_token": T * K, "recv_k": T * K,
-            "send_token": T * min(K, R), "send_row_of": T * K, "recv_send_row": T * K, "S": 1}
+            "off_recv_r": R + 1, "pos": T * K, "recv_token": RR, "recv_k": RR,
+            "send_token": T * min(K, R), "send_row_of": T * K, "recv_send_row": RR, "S": 1}
 
 
 def moe_dispatch_layout_static(cfg, idx, out, status=None, stream=None):
@@ -346,7 +356,7 @@ def moe_dispatch_layout_static(cfg, idx, out, status=None, stream=None):
     one-element int32 CUDA tensor that collects MOE_DEVERR_* bits."""
     T = idx.shape[0]
     _req(idx, torch.int32, (T, cfg.top_k), "idx")
-    sizes = layout_sizes(T, cfg.top_k, cfg.num_experts, cfg.num_ranks)
+    sizes = layout_sizes(T, cfg.top_k, cfg.num_experts, cfg.num_ranks, cfg.pad_align)
     v = MoeLayout()
     for name in LAYOUT_FIELDS:
         t = out[name]
@@ -365,9 +375,7 @@ def layout_tensors(h):
     """Torch views (int32, on the handle's device) of the current layout arrays."""
     v = moe_layout_view(h)
     T, K, E, R = h.T, h.K, h.E, h.R
-    sizes = {"cnt_e": E, "off_e": E + 1, "cnt_send_r": R, "off_send_r": R + 1, "cnt_recv_r": R,
-             "off_recv_r": R + 1, "pos": T * K, "recv_token": T * K, "recv_k": T * K,
-             "send_token": T * min(K, R), "send_row_of": T * K, "recv_send_row": T * K, "S": 1}
+    sizes = layout_sizes(T, K, E, R, h.pad)
     out = {}
     ws = h.workspace
     base = ws.data_ptr()
@@ -404,8 +412,8 @@ class MoeRouter:
 
     def dispatch(self, x, w=None, with_send=False, stream=None):
         T, H = x.shape
-        recv = torch.empty(T * self.h.K, H, dtype=x.dtype, device=x.device)
-        recv_w = torch.empty(T * self.h.K, dtype=torch.float32, device=x.device) if w is not None else None
+        recv = torch.empty(self.h.recv_rows, H, dtype=x.dtype, device=x.device)
+        recv_w = torch.empty(self.h.recv_rows, dtype=torch.float32, device=x.device) if w is not None else None
         send = torch.empty(T * min(self.h.K, self.h.R), H, dtype=x.dtype, device=x.device) if with_send else None
         moe_dispatch(self.h, x, w, recv, recv_w, send, stream)
         return recv, recv_w, send
@@ -416,7 +424,7 @@ class MoeRouter:
         return out
 
     def combine_bwd(self, g, y=None, w=None, stream=None):
-        gy = torch.empty(max(self.h.T, 0) * self.h.K, g.shape[1], dtype=g.dtype, device=g.device)
+        gy = torch.empty(self.h.recv_rows, g.shape[1], dtype=g.dtype, device=g.device)
         gw = torch.empty(max(self.h.T, 0), self.h.K, dtype=torch.float32, device=g.device) if w is not None else None
         moe_combine_bwd(self.h, g, y, w, gy, gw, stream)
         return gy, gw
@@ -427,8 +435,7 @@ class MoeRouter:
         return gx
 
     def expand(self, send, stream=None):
-        recv = torch.empty(max(self.h.T, 0) * self.h.K, send.shape[1], dtype=send.dtype,
-                           device=send.device)
+        recv = torch.empty(self.h.recv_rows, send.shape[1], dtype=send.dtype, device=send.device)
         moe_expand(self.h, send, recv, stream)
         return recv
 

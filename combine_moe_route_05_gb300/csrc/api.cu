@@ -34,7 +34,10 @@ bool config_valid(const moe_config* c) {
   if (c->renorm != 0 && c->renorm != 1) return false;
   if (!std::isfinite(c->route_scale)) return false;
   if (c->max_tokens < 0) return false;
-  if (static_cast<int64_t>(c->max_tokens) * K > INT32_MAX) return false;
+  if (c->pad_align < 0 || c->pad_align > 4096) return false;
+  const int64_t pad = c->pad_align > 1 ? c->pad_align : 1;
+  if (static_cast<int64_t>(c->max_tokens) * K + static_cast<int64_t>(E) * (pad - 1) > INT32_MAX)
+    return false;
   return true;
 }
 
@@ -65,12 +68,13 @@ Plan plan(const moe_config* c) {
   p.cnt_recv_r = take(R * i4);
   p.off_recv_r = take((R + 1) * i4);
   p.S = take(i4);
+  const size_t RR = T * K + E * static_cast<size_t>(c->pad_align > 1 ? c->pad_align - 1 : 0);
   p.pos = take(T * K * i4);
-  p.recv_token = take(T * K * i4);
-  p.recv_k = take(T * K * i4);
+  p.recv_token = take(RR * i4);
+  p.recv_k = take(RR * i4);
   p.send_token = take(T * (K < R ? K : R) * i4);
   p.send_row_of = take(T * K * i4);
-  p.recv_send_row = take(T * K * i4);
+  p.recv_send_row = take(RR * i4);
   p.tile_hist = take((E + R) * static_cast<size_t>(p.max_tiles) * i4);
   p.total = o;
   return p;
@@ -151,6 +155,7 @@ moe_status moe_handle_create(const moe_config* c, void* d_workspace, size_t work
   h->num_sms = sms;
   h->T = -1;
   h->max_tiles = p.max_tiles;
+  h->pad = c->pad_align > 1 ? c->pad_align : 1;
   h->flags = reinterpret_cast<uint32_t*>(ws + p.flags);
   h->ticket = reinterpret_cast<uint32_t*>(ws + p.ticket);
   h->cnt_e = reinterpret_cast<int32_t*>(ws + p.cnt_e);
@@ -224,7 +229,7 @@ moe_status moe_layout_view(const moe_handle* h, moe_layout* out) {
   out->recv_send_row = h->recv_send_row;
   out->S = h->S;
   out->num_tokens = h->T;
-  out->reserved = 0;
+  out->pad_align = h->pad;
   return MOE_OK;
 }
 

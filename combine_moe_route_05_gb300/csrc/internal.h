@@ -13,6 +13,7 @@ struct moe_handle {
   int num_sms;
   int T;  // tokens of the current layout, -1 before the first
   int max_tiles;
+  int pad;  // receive segments rounded up to a multiple of pad rows (>= 1)
   uint32_t* flags;   // device status word (MOE_DEVERR_* bits)
   uint32_t* ticket;  // arrival counter of the layout's last-block scan
   int32_t* cnt_e;
@@ -58,6 +59,10 @@ cudaError_t launch_combine_bwd(const moe_handle* h, const void* g, const void* y
 // partials; 2: reduce the partials to token rows
 cudaError_t launch_staged(int op, const moe_handle* h, const void* src, int H, int dtype,
                           const float* w, void* dst, cudaStream_t s);
+
+// Writes zeros to the pad rows of a receive-row tensor (rows of row_bytes,
+// a multiple of 4) when the layout is padded; nothing otherwise.
+cudaError_t zero_pad_rows(const moe_handle* h, void* rows, int64_t row_bytes, cudaStream_t s);
 
 cudaError_t launch_scale_rows(const moe_handle* h, const void* hrows, int I, int dtype,
                               const float* recv_w, void* hs, cudaStream_t s);

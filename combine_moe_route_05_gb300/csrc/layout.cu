@@ -39,6 +39,8 @@ static_assert(kTile % 32 == 0 && kTile <= 1024, "tile must be whole warps of one
 struct LayoutArgs {
   const int32_t* idx;
   int T, K, E, R, epr, ntiles;
+  int pad;       // receive segments rounded up to a multiple of pad rows
+  int recv_cap;  // receive rows: T*K + E*(pad-1)
   uint32_t* flags;
   uint32_t* ticket;
   int32_t* cnt_e;
@@ -147,10 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a)
     const int32_t* src = tot + (warp == 0 ? 0 : a.E);
     int32_t* cnt = warp == 0 ? a.cnt_e : a.cnt_send_r;
     int32_t* off = warp == 0 ? a.off_e : a.off_send_r;
+    // expert segments are rounded up to the padding; rank counts are not
+    const int pad = warp == 0 ? a.pad : 1;
     const int per = (n + 31) / 32;
     const int lo = lane * per, hi = min(n, lo + per);
     int local = 0;
-    for (int i = lo; i < hi; ++i) local += src[i];
+    for (int i = lo; i < hi; ++i) local += (src[i] + pad - 1) / pad * pad;
     int incl = local;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a)
     for (int i = lo; i < hi; ++i) {
       cnt[i] = src[i];
       off[i] = run;
-      run += src[i];
+      run += (src[i] + pad - 1) / pad * pad;
     }
     const int total = __shfl_sync(0xffffffffu, incl, 31);
     if (lane == 0) {
@@ -277,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   const int32_t* off_s = off + a.E + 1;
   const int32_t* seg_e = seg;
   const int32_t* seg_r = seg + a.E + 1;
-  const int n_recv_rows = a.T * a.K;
+  const int n_recv_rows = a.recv_cap;
   const int n_send_rows = a.T * KR;
   const uint32_t lt = lanemask_lt();
 
@@ -356,7 +360,19 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
     a.send_token[row] = tile_t0 + tl;
   }
 
-  // tails: receive rows past off_e[E] and send rows past S
+  // pad rows of the expert segments (this block takes experts blockIdx.x,
+  // blockIdx.x + gridDim.x, ...), then the tails: receive rows past off_e[E]
+  // and send rows past S
+  if (a.pad > 1) {
+    for (int e = blockIdx.x; e < a.E; e += gridDim.x) {
+      const int lo = off_e[e] + a.cnt_e[e], hi = off_e[e + 1];
+      for (int p = lo + threadIdx.x; p < hi; p += kThreads) {
+        a.recv_token[p] = -1;
+        a.recv_k[p] = -1;
+        a.recv_send_row[p] = -1;
+      }
+    }
+  }
   const long long gtid = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x;
   const long long gsize = static_cast<long long>(gridDim.x) * kThreads;
   for (long long p = off[a.E] + gtid; p < n_recv_rows; p += gsize) {
@@ -406,6 +422,8 @@ cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T
   a.epr = c.num_experts / c.num_ranks;
   a.ntiles = layout_tiles(T);
   if (a.ntiles > max_tiles) return cudaErrorInvalidValue;
+  a.pad = c.pad_align > 1 ? c.pad_align : 1;
+  a.recv_cap = T * a.K + a.E * (a.pad - 1);
   a.flags = flags;
   a.ticket = ticket;
   a.cnt_e = out.cnt_e;

@@ -214,6 +214,26 @@ __global__ void __launch_bounds__(kGatherMaxThreads, 2) combine_bwd_kernel(RowAr
 }
 
 // ---------------------------------------------------------------------------
+// pad rows of a padded receive layout: zeros (one block per expert)
+
+__global__ void __launch_bounds__(256) zero_pad_rows_kernel(uint8_t* rows, int64_t row_bytes,
+                                                            const int32_t* off_e,
+                                                            const int32_t* cnt_e, int E) {
+  for (int e = blockIdx.x; e < E; e += gridDim.x) {
+    const int64_t lo = static_cast<int64_t>(off_e[e]) + cnt_e[e], hi = off_e[e + 1];
+    uint8_t* base = rows + lo * row_bytes;
+    const int64_t bytes = (hi - lo) * row_bytes;
+    if ((row_bytes & 15) == 0) {
+      const Vec16 z{{0u, 0u, 0u, 0u}};
+      for (int64_t i = threadIdx.x; i < bytes / 16; i += blockDim.x) st_vec(base + i * 16, z);
+    } else {
+      for (int64_t i = threadIdx.x; i < bytes / 4; i += blockDim.x)
+        reinterpret_cast<uint32_t*>(base)[i] = 0u;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // staged (wire-faithful) mode: a token's row goes to each destination rank
 // once (its send row); the receiving side expands it to the rows of its
 // experts there, and the combine returns one partial row per send row, which
@@ -508,7 +528,8 @@ cudaError_t launch_combine_bwd_t(const moe_handle* h, const void* g, const void*
     kp = reinterpret_cast<const void*>(k);
     k<<<grid_for(kp, block, 0, h->num_sms, a.T), block, 0, s>>>(a);
   }
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  return e != cudaSuccess ? e : zero_pad_rows(h, gy, a.row_bytes, s);
 }
 
 }  // namespace
@@ -539,7 +560,11 @@ cudaError_t launch_dispatch(const moe_handle* h, const void* x, int64_t row_byte
     dispatch_kernel<8><<<grid, block, 0, s>>>(a);
   else
     dispatch_kernel<16><<<grid, block, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = zero_pad_rows(h, recv, row_bytes, s);
+  if (e != cudaSuccess) return e;
+  return zero_pad_rows(h, recv_w, sizeof(float), s);
 }
 
 cudaError_t launch_combine(const moe_handle* h, const void* y, int H, int dtype, const float* w,
@@ -605,7 +630,8 @@ cudaError_t launch_scale_rows_bwd(const moe_handle* h, const void* ghs, const vo
                                    static_cast<const uint8_t*>(hrows), recv_w,
                                    static_cast<uint8_t*>(gh), gw, h->pos, entries, row_bytes, nvec);
   }
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  return e != cudaSuccess ? e : zero_pad_rows(h, gh, row_bytes, s);
 }
 
 cudaError_t launch_staged(int op, const moe_handle* h, const void* src, int H, int dtype,
@@ -627,7 +653,8 @@ cudaError_t launch_staged(int op, const moe_handle* h, const void* src, int H, i
     const int grid = a.T < 1048576 ? a.T : 1048576;
     if (k8) expand_kernel<8><<<grid, block, 0, s>>>(a);
     else expand_kernel<16><<<grid, block, 0, s>>>(a);
-    return cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
+    return e != cudaSuccess ? e : zero_pad_rows(h, dst, a.row_bytes, s);
   }
   const int block = gather_threads(a.nvec);
 #define MOE_STAGED_LAUNCH(KERNEL)                                                            \
@@ -654,6 +681,14 @@ cudaError_t launch_staged(int op, const moe_handle* h, const void* src, int H, i
     }
   }
 #undef MOE_STAGED_LAUNCH
+  return cudaGetLastError();
+}
+
+cudaError_t zero_pad_rows(const moe_handle* h, void* rows, int64_t row_bytes, cudaStream_t s) {
+  if (h->pad <= 1 || h->T <= 0 || !rows) return cudaSuccess;
+  const int E = h->cfg.num_experts;
+  zero_pad_rows_kernel<<<E, 256, 0, s>>>(static_cast<uint8_t*>(rows), row_bytes, h->off_e, h->cnt_e,
+                                          E);
   return cudaGetLastError();
 }
 

@@ -93,6 +93,14 @@ typedef enum moe_score_fn { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_s
  *   max_tokens: capacity T_max; a larger batch is rejected with
  *     MOE_ERR_CAPACITY ([AutoEP-DeepEP] review fix: a batch that outgrows the
  *     buffer must not fault).
+ *   pad_align: 0 or 1 = receive segments packed; A > 1 = every expert's
+ *     segment of receive rows is rounded up to a multiple of A rows (a
+ *     grouped-GEMM tile), off_e[e+1] = off_e[e] + ceil(cnt_e[e]/A)*A, as in the
+ *     padded permute of [Titan-absorb] "Implementation".  Pad rows have
+ *     recv_token = recv_k = recv_send_row = -1, and every kernel that writes
+ *     receive rows (dispatch, expand, combine_bwd, scale_rows_bwd) writes
+ *     zeros there (zero rows, zero score).  Receive-row tensors then hold
+ *     T*K + E*(A-1) rows (1..4096).
  */
 typedef struct moe_config {
   int32_t num_experts;
@@ -105,7 +113,7 @@ typedef struct moe_config {
   int32_t renorm;
   double route_scale;
   int32_t max_tokens;
-  int32_t reserved;
+  int32_t pad_align;
 } moe_config;
 
 /*
@@ -115,10 +123,11 @@ typedef struct moe_config {
  *   cnt_send_r[R], off_send_r[R+1]    token-deduplicated rows per rank
  *   cnt_recv_r[R], off_recv_r[R+1]    expert rows per rank
  *   pos[T*K]          receive row of entry (t,k), -1 if dropped
- *   recv_token[T*K]   token of receive row p, recv_k[T*K] its k (tail: -1)
+ *   recv_token[RR]    token of receive row p, recv_k[RR] its k (pad rows and
+ *                     tail: -1); RR = T*K + E*(pad_align-1) receive rows
  *   send_token[T*min(K,R)]  token of send row s (tail beyond S: -1)
  *   send_row_of[T*K]  send row of entry (t,k), -1 if dropped
- *   recv_send_row[T*K] send row that receive row p expands from (tail: -1)
+ *   recv_send_row[RR] send row that receive row p expands from (pad, tail: -1)
  *   S[1]              number of send rows (device scalar)
  */
 typedef struct moe_layout {
@@ -136,7 +145,7 @@ typedef struct moe_layout {
   int32_t* recv_send_row;
   int32_t* S;
   int32_t num_tokens; /* T of the last layout, -1 before the first */
-  int32_t reserved;
+  int32_t pad_align;  /* receive segments padded to multiples of this (1: none) */
 } moe_layout;
 
 typedef struct moe_handle moe_handle;

@@ -32,7 +32,7 @@ def lib():
         L.orc_route_softmax.restype = i32
         L.orc_route_sigmoid_grouped.argtypes = [P, P, i64, i32, i32, i32, i32, i32, i32, d, P, P]
         L.orc_route_sigmoid_grouped.restype = i32
-        L.orc_layout.argtypes = [P, i64, i32, i32, i32] + [P] * 12 + [P]
+        L.orc_layout.argtypes = [P, i64, i32, i32, i32, i32] + [P] * 12 + [P]
         L.orc_layout.restype = i64
         L.orc_dispatch.argtypes = [P, i64, i64, i32, P, P, P, P, P, P]
         L.orc_dispatch.restype = None
@@ -125,8 +125,9 @@ def route_bwd(logits, idx, gw, score_fn="softmax", renorm=True, route_scale=1.0)
 class Layout:
     """Outputs of the dispatch layout, as numpy int32 arrays."""
 
-    def __init__(self, T, K, E, R):
-        self.T, self.K, self.E, self.R = T, K, E, R
+    def __init__(self, T, K, E, R, align=1):
+        self.T, self.K, self.E, self.R, self.align = T, K, E, R, align
+        self.recv_rows = T * K + E * (align - 1)
         self.cnt_e = np.empty(E, np.int32)
         self.off_e = np.empty(E + 1, np.int32)
         self.cnt_send_r = np.empty(R, np.int32)
@@ -134,11 +135,11 @@ class Layout:
         self.cnt_recv_r = np.empty(R, np.int32)
         self.off_recv_r = np.empty(R + 1, np.int32)
         self.pos = np.empty((T, K), np.int32)
-        self.recv_token = np.empty(T * K, np.int32)
-        self.recv_k = np.empty(T * K, np.int32)
+        self.recv_token = np.empty(self.recv_rows, np.int32)
+        self.recv_k = np.empty(self.recv_rows, np.int32)
         self.send_token = np.empty(T * min(K, R), np.int32)
         self.send_row_of = np.empty((T, K), np.int32)
-        self.recv_send_row = np.empty(T * K, np.int32)
+        self.recv_send_row = np.empty(self.recv_rows, np.int32)
         self.S = 0
         self.dropped = 0
 
@@ -146,13 +147,13 @@ class Layout:
               "recv_token", "recv_k", "send_token", "send_row_of", "recv_send_row")
 
 
-def layout(idx, E, R):
+def layout(idx, E, R, align=1):
     idx = _c(idx, np.int32)
     T, K = idx.shape
-    L = Layout(T, K, E, R)
+    L = Layout(T, K, E, R, align)
     S = ctypes.c_int64(0)
-    dropped = lib().orc_layout(_p(idx), T, K, E, R, *[_p(getattr(L, f)) for f in Layout.FIELDS],
-                               ctypes.addressof(S))
+    dropped = lib().orc_layout(_p(idx), T, K, E, R, align,
+                               *[_p(getattr(L, f)) for f in Layout.FIELDS], ctypes.addressof(S))
     if dropped < 0:
         raise ValueError("orc_layout: invalid sizes")
     L.S = int(S.value)
@@ -164,8 +165,8 @@ def dispatch(x, lay, w=None, with_send=False):
     x = np.ascontiguousarray(x)
     T, H = x.shape
     K = lay.K
-    recv = np.zeros((T * K, H), x.dtype)
-    recv_w = np.zeros(T * K, np.float32) if w is not None else None
+    recv = np.zeros((lay.recv_rows, H), x.dtype)
+    recv_w = np.zeros(lay.recv_rows, np.float32) if w is not None else None
     send = np.zeros((T * min(K, lay.R), H), x.dtype) if with_send else None
     wc = None if w is None else _c(w, np.float32)
     lib().orc_dispatch(_p(x), H * x.itemsize, T, K, _p(lay.pos), _p(wc), _p(lay.send_row_of),
@@ -187,7 +188,7 @@ def combine_bwd(g, y, lay, w=None):
     y = np.ascontiguousarray(y)
     assert g.dtype == y.dtype
     H = g.shape[1]
-    gy = np.zeros((lay.T * lay.K, H), g.dtype)
+    gy = np.zeros((getattr(lay, "recv_rows", lay.T * lay.K), H), g.dtype)
     wc = None if w is None else _c(w, np.float32)
     gw = np.zeros((lay.T, lay.K), np.float64) if w is not None else None
     lib().orc_combine_bwd(_p(g), _p(y), _dtype_of(g), H, lay.T, lay.K, _p(lay.pos), _p(wc), _p(gy),
@@ -207,7 +208,7 @@ def expand(send, lay):
     """recv[pos[t,k]] = send[send_row_of[t,k]] (rows of dropped entries stay 0)."""
     send = np.ascontiguousarray(send)
     H = send.shape[1]
-    recv = np.zeros((lay.T * lay.K, H), send.dtype)
+    recv = np.zeros((getattr(lay, "recv_rows", lay.T * lay.K), H), send.dtype)
     lib().orc_expand(_p(send), H * send.itemsize, lay.T, lay.K, _p(lay.pos), _p(lay.send_row_of),
                      _p(recv))
     return recv
@@ -268,7 +269,7 @@ def combine_f64(y, lay, w=None):
 def dispatch_f64(x, lay):
     x = _c(x, np.float64)
     H = x.shape[1]
-    recv = np.zeros((lay.T * lay.K, H), np.float64)
+    recv = np.zeros((getattr(lay, "recv_rows", lay.T * lay.K), H), np.float64)
     lib().orc_dispatch_f64(_p(x), H, lay.T, lay.K, _p(lay.pos), _p(recv))
     return recv
 

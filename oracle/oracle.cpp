@@ -209,14 +209,21 @@ int orc_route_sigmoid_grouped(const float* logits, const float* bias, int64_t T,
 //   recv_send_row[pos[t,k]] = send_row_of[t,k]               (tail -1)
 //   cnt_recv_r[r] = sum of cnt_e over r's experts, off_recv_r[r] = off_e[r*E/R]
 // Returns the number of dropped entries, or -1 for invalid sizes.
-int64_t orc_layout(const int32_t* idx, int64_t T, int K, int E, int R, int32_t* cnt_e,
+//
+// Padded layout (align > 1; the TorchAO padded permute of [Titan-absorb]
+// "Implementation", zero-sentinel scores): every expert segment is rounded up
+// to a multiple of `align` rows, off_e[e+1] = off_e[e] + ceil(cnt_e/align)*align;
+// the pad rows carry recv_token = recv_k = recv_send_row = -1, and the
+// receive arrays hold T*K + E*(align-1) rows.  align = 1: no padding.
+int64_t orc_layout(const int32_t* idx, int64_t T, int K, int E, int R, int align, int32_t* cnt_e,
                    int32_t* off_e, int32_t* cnt_send_r, int32_t* off_send_r, int32_t* cnt_recv_r,
                    int32_t* off_recv_r, int32_t* pos, int32_t* recv_token, int32_t* recv_k,
                    int32_t* send_token, int32_t* send_row_of, int32_t* recv_send_row,
                    int64_t* S_out) {
-  if (T < 0 || K <= 0 || E <= 0 || R <= 0 || E % R) return -1;
+  if (T < 0 || K <= 0 || E <= 0 || R <= 0 || E % R || align < 1) return -1;
   const int epr = E / R;
   const int64_t send_cap = T * (K < R ? K : R);
+  const int64_t recv_cap = T * K + static_cast<int64_t>(E) * (align - 1);
   int64_t dropped = 0;
 
   std::vector<char> valid(static_cast<size_t>(T * K), 0);
@@ -234,7 +241,7 @@ int64_t orc_layout(const int32_t* idx, int64_t T, int K, int E, int R, int32_t* 
   for (int64_t i = 0; i < T * K; ++i)
     if (valid[static_cast<size_t>(i)]) ++cnt_e[idx[i]];
   off_e[0] = 0;
-  for (int e = 0; e < E; ++e) off_e[e + 1] = off_e[e] + cnt_e[e];
+  for (int e = 0; e < E; ++e) off_e[e + 1] = off_e[e] + (cnt_e[e] + align - 1) / align * align;
 
   std::vector<int64_t> seen_e(static_cast<size_t>(E), 0);
   for (int64_t t = 0; t < T; ++t)
@@ -250,7 +257,10 @@ int64_t orc_layout(const int32_t* idx, int64_t T, int K, int E, int R, int32_t* 
       recv_token[p] = static_cast<int32_t>(t);
       recv_k[p] = k;
     }
-  for (int64_t p = off_e[E]; p < T * K; ++p) recv_token[p] = recv_k[p] = recv_send_row[p] = -1;
+  for (int e = 0; e < E; ++e)  // pad rows of each segment
+    for (int64_t p = off_e[e] + cnt_e[e]; p < off_e[e + 1]; ++p)
+      recv_token[p] = recv_k[p] = recv_send_row[p] = -1;
+  for (int64_t p = off_e[E]; p < recv_cap; ++p) recv_token[p] = recv_k[p] = recv_send_row[p] = -1;
 
   // ranks(t): the set of destination ranks of token t's valid entries
   std::vector<char> in_ranks(static_cast<size_t>(R));

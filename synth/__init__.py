@@ -53,6 +53,7 @@ class Workload:
     absorb: bool = False
     I: int = 0                   # W2 input width when scores are absorbed
     identity_experts: bool = False
+    pad_align: int = 0           # receive segments rounded up to this many rows (0: packed)
     seed: int = 0
     extra: dict = field(default_factory=dict)
 

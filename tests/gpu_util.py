@@ -34,7 +34,7 @@ def router(wl, max_tokens=None):
     return moe.MoeRouter(wl.E, wl.K, wl.R, wl.T if max_tokens is None else max_tokens,
                          score_fn=wl.score_fn, num_groups=wl.n_groups, topk_groups=wl.topk_groups,
                          group_score_topk=wl.group_score_topk, renorm=wl.renorm,
-                         route_scale=wl.route_scale)
+                         route_scale=wl.route_scale, pad_align=wl.pad_align)
 
 
 def oracle_route(wl, logits, bias):

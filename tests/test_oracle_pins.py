@@ -674,3 +674,45 @@ def test_staged_combine_within_rounding_of_exact_sum():
     # stage 1 rounds each partial once and stage 2 adds at most min(K,R) of them
     bound = (6 + 4 + 4) * 2.0 ** -24 * absmag * 1.01
     assert (np.abs(staged - exact) <= bound).all()
+
+
+# ----------------------------------------------------------------------------
+# padded (capacity-aligned) receive layout
+
+
+@pytest.mark.parametrize("align", [1, 4, 7, 128])
+def test_padded_layout_shifts_segments_to_aligned_starts(align):
+    rng = np.random.default_rng(50 + align)
+    T, E, K, R = 90, 16, 4, 4
+    idx = random_idx(rng, T, E, K)
+    L0 = oracle.layout(idx, E, R)
+    L = oracle.layout(idx, E, R, align)
+    assert (L.cnt_e == L0.cnt_e).all()
+    assert (L.off_e % align == 0).all()
+    assert (np.diff(L.off_e) == -(-L0.cnt_e // align) * align).all()
+    # same rank inside each segment, only the segment start moves
+    e_of = idx
+    assert ((L.pos - L.off_e[e_of]) == (L0.pos - L0.off_e[e_of])).all()
+    for e in range(E):
+        seg = slice(L.off_e[e], L.off_e[e + 1])
+        n = L.cnt_e[e]
+        assert (L.recv_token[seg][:n] == L0.recv_token[L0.off_e[e]:L0.off_e[e + 1]]).all()
+        assert (L.recv_token[seg][n:] == -1).all() and (L.recv_k[seg][n:] == -1).all()
+    assert L.recv_rows == T * K + E * (align - 1)
+    assert (L.send_token == L0.send_token).all() and (L.send_row_of == L0.send_row_of).all()
+
+
+def test_padded_layout_leaves_row_results_unchanged():
+    idx, L0, w, x, y0, g = small_case(51, T=60, H=24, E=8, K=3, R=2, dtype=np.uint16)
+    L = oracle.layout(idx, 8, 2, 16)
+    recv0, rw0, _ = oracle.dispatch(x, L0, w)
+    recv, rw, _ = oracle.dispatch(x, L, w)
+    # the same rows, moved to the padded positions; pad rows stay zero
+    assert (recv[L.pos.reshape(-1)] == recv0[L0.pos.reshape(-1)]).all()
+    pad = np.ones(L.recv_rows, bool)
+    pad[L.pos.reshape(-1)] = False
+    assert (recv[pad] == 0).all() and (rw[pad] == 0).all()
+    y = np.zeros((L.recv_rows, y0.shape[1]), np.uint16)
+    y[L.pos.reshape(-1)] = y0[L0.pos.reshape(-1)]
+    assert (oracle.combine(y, L, w) == oracle.combine(y0, L0, w)).all()
+    assert (oracle.dispatch_bwd(y, L) == oracle.dispatch_bwd(y0, L0)).all()
