@@ -205,8 +205,11 @@ class Handle:
 
     @property
     def recv_rows(self):
-        """Rows of a receive-row tensor for the current layout."""
-        return max(self.T, 0) * self.K + self.E * (self.pad - 1)
+        """Rows of a receive-row tensor for the current layout (-1 before the
+        first layout, so that the library itself reports MOE_ERR_STATE)."""
+        if self.T < 0:
+            return -1
+        return self.T * self.K + self.E * (self.pad - 1)
 
 
 def moe_route_topk(h, logits, bias, idx, w, stream=None):
@@ -412,8 +415,9 @@ class MoeRouter:
 
     def dispatch(self, x, w=None, with_send=False, stream=None):
         T, H = x.shape
-        recv = torch.empty(self.h.recv_rows, H, dtype=x.dtype, device=x.device)
-        recv_w = torch.empty(self.h.recv_rows, dtype=torch.float32, device=x.device) if w is not None else None
+        rr = max(self.h.recv_rows, 0)
+        recv = torch.empty(rr, H, dtype=x.dtype, device=x.device)
+        recv_w = torch.empty(rr, dtype=torch.float32, device=x.device) if w is not None else None
         send = torch.empty(T * min(self.h.K, self.h.R), H, dtype=x.dtype, device=x.device) if with_send else None
         moe_dispatch(self.h, x, w, recv, recv_w, send, stream)
         return recv, recv_w, send
@@ -424,7 +428,7 @@ class MoeRouter:
         return out
 
     def combine_bwd(self, g, y=None, w=None, stream=None):
-        gy = torch.empty(self.h.recv_rows, g.shape[1], dtype=g.dtype, device=g.device)
+        gy = torch.empty(max(self.h.recv_rows, 0), g.shape[1], dtype=g.dtype, device=g.device)
         gw = torch.empty(max(self.h.T, 0), self.h.K, dtype=torch.float32, device=g.device) if w is not None else None
         moe_combine_bwd(self.h, g, y, w, gy, gw, stream)
         return gy, gw
@@ -435,7 +439,8 @@ class MoeRouter:
         return gx
 
     def expand(self, send, stream=None):
-        recv = torch.empty(self.h.recv_rows, send.shape[1], dtype=send.dtype, device=send.device)
+        recv = torch.empty(max(self.h.recv_rows, 0), send.shape[1], dtype=send.dtype,
+                           device=send.device)
         moe_expand(self.h, send, recv, stream)
         return recv
 
