@@ -175,9 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a)
   }
   __syncthreads();
   for (int r = threadIdx.x; r < a.R; r += kThreads) {
-    const int lo = a.off_e[r * a.epr], hi = a.off_e[(r + 1) * a.epr];
-    a.off_recv_r[r] = lo;
-    a.cnt_recv_r[r] = hi - lo;
+    // rows that arrive at rank r (pads excluded); its region starts at the
+    // padded offset of its first expert
+    int n = 0;
+    for (int e = r * a.epr; e < (r + 1) * a.epr; ++e) n += tot[e];
+    a.off_recv_r[r] = a.off_e[r * a.epr];
+    a.cnt_recv_r[r] = n;
   }
   if (threadIdx.x == 0) {
     a.off_recv_r[a.R] = a.off_e[a.E];

@@ -121,7 +121,9 @@ typedef struct moe_config {
  * for the last layout's T tokens (all int32):
  *   cnt_e[E], off_e[E+1]              per-expert counts, exclusive offsets
  *   cnt_send_r[R], off_send_r[R+1]    token-deduplicated rows per rank
- *   cnt_recv_r[R], off_recv_r[R+1]    expert rows per rank
+ *   cnt_recv_r[R], off_recv_r[R+1]    rows arriving at each rank (pads not
+ *                                     counted) and where its region of receive
+ *                                     rows starts (padded when pad_align > 1)
  *   pos[T*K]          receive row of entry (t,k), -1 if dropped
  *   recv_token[RR]    token of receive row p, recv_k[RR] its k (pad rows and
  *                     tail: -1); RR = T*K + E*(pad_align-1) receive rows
