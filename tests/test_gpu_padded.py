@@ -33,15 +33,17 @@ def test_padded_chain(i, align):
     y_entries = synth.rows(wl, wl.seed, "y", wl.T * wl.K, wl.H)
     y[L.pos.reshape(-1)] = y_entries
     y_d = to_dev(y)
+    # rows past off_e[E] belong to no segment and are not written
+    n = int(L.off_e[-1])
     recv, recv_w, send = r.dispatch(to_dev(inp["x"]), to_dev(w), with_send=True)
     orecv, orw, _ = oracle.dispatch(inp["x"], L, w)
-    assert np.array_equal(to_host(recv), orecv)          # includes the zero pad rows
-    assert np.array_equal(to_host(recv_w), orw)
-    assert np.array_equal(to_host(r.expand(send)), orecv)
+    assert np.array_equal(to_host(recv)[:n], orecv[:n])  # includes the zero pad rows
+    assert np.array_equal(to_host(recv_w)[:n], orw[:n])
+    assert np.array_equal(to_host(r.expand(send))[:n], orecv[:n])
     assert_ulp(to_host(r.combine(y_d, to_dev(w))), oracle.combine(y, L, w), 0, "combine")
     gy, gw = r.combine_bwd(to_dev(inp["g"]), y_d, to_dev(w))
     ogy, ogw = oracle.combine_bwd(inp["g"], y, L, w)
-    assert np.array_equal(to_host(gy), ogy)               # zero pad rows
+    assert np.array_equal(to_host(gy)[:n], ogy[:n])       # zero pad rows
     assert np.allclose(to_host(gw), ogw, rtol=1e-3, atol=1e-3)
     assert_ulp(to_host(r.dispatch_bwd(y_d)), oracle.dispatch_bwd(y, L), 0, "dispatch_bwd")
     # the token-side results equal those of the packed layout
@@ -69,5 +71,5 @@ def test_padded_absorption_rows():
     assert np.array_equal(hs[:n], oracle.scale_rows(h, recv_w, rows=n)[:n])
     gh, gw = r.scale_rows_bwd(to_dev(ghs), to_dev(h), to_dev(recv_w))
     ogh, ogw = oracle.scale_rows_bwd(ghs, h, recv_w, L, rows=n)
-    assert np.array_equal(to_host(gh), ogh)
+    assert np.array_equal(to_host(gh)[:n], ogh[:n])
     assert np.allclose(to_host(gw), ogw, rtol=1e-3, atol=1e-3)
