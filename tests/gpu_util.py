@@ -54,6 +54,7 @@ class SubLayout:
         self.T = len(tokens)
         self.K = L.K
         self.R = L.R
+        self.recv_rows = self.T * self.K
         self.rows = L.pos[tokens].reshape(-1)
         local = np.arange(self.T * self.K, dtype=np.int32)
         self.pos = np.where(self.rows >= 0, local, -1).astype(np.int32).reshape(self.T, self.K)
