@@ -35,6 +35,7 @@ import synth  # noqa: E402
 METRIC = "dispatch+combine fwd+bwd tokens/s and achieved HBM GB/s (% of GB300 peak)"
 UNIT = "tokens/s"
 DOMINANT = "combine_bwd"
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e data-sheet bandwidth, for context beside the measured peak
 KERNEL_SOURCES = ("combine_moe_route_05_gb300/csrc/rows.cu", "combine_moe_route_05_gb300/csrc/common.cuh")
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "combine_bwd_deepseek_v3.md")
 
@@ -204,6 +205,7 @@ def time_oracle(wl, tokens, reps=1):
 
 
 def cpu_baseline(wl, tokens):
+    tokens = min(tokens, wl.T) if tokens > 0 else wl.T
     t = time_oracle(wl, tokens)[0]
     return {"value": tokens / t, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": "first %d of %d tokens of the same workload, whole path (route, layout, "
@@ -341,6 +343,7 @@ def run_gpu(args, wl):
     el_ms = start.elapsed_time(end)
     ms_step = reduce_max(el_ms / args.steps, world, device)
     stage_ms = {n: float(np.mean([e[j].elapsed_time(e[j + 1]) for e in evs])) for j, n in enumerate(names)}
+    step_median_ms = float(np.median([e[0].elapsed_time(e[-1]) for e in evs]))
 
     # end to end through the same public calls, inputs from pinned host memory
     # and outputs read back every step
@@ -438,6 +441,8 @@ def run_gpu(args, wl):
         "data": "synthetic", "config": workload_config(wl),
         "hbm_gbs": total_bytes / (ms_step / 1e3) / 1e9,
         "hbm_frac_of_peak": total_bytes / (ms_step / 1e3) / 1e9 / peak,
+        "hbm_frac_of_nominal": total_bytes / (ms_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+        "ms_per_step_median": step_median_ms,
         "bytes_per_step": total_bytes,
         "stage_ms": stage_ms,
         "stage_gbs": {n: sb[n] / (stage_ms[n] / 1e3) / 1e9 for n in names},
@@ -457,12 +462,13 @@ def run_gpu(args, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", type=int, default=3)
     ap.add_argument("--tokens", type=int, default=0, help="override T (small profiling cases)")
-    ap.add_argument("--cpu-tokens", type=int, default=1024)
+    ap.add_argument("--cpu-tokens", type=int, default=0,
+                    help="oracle baseline sample in tokens (0 = the whole batch)")
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

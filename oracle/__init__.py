@@ -60,6 +60,10 @@ def lib():
         L.orc_combine_reduce.restype = None
         L.orc_f32_to_bf16.argtypes = [P, i64, P]
         L.orc_f32_to_bf16.restype = None
+        L.orc_w2_absorbed.argtypes = [P, i64, P, P, i64, i32, P, P, P, i64, P, P]
+        L.orc_w2_absorbed.restype = None
+        L.orc_f64_to_bf16.argtypes = [P, i64, P]
+        L.orc_f64_to_bf16.restype = None
         _lib = L
     return _lib
 
@@ -242,6 +246,35 @@ def scale_rows(h, recv_w, rows=None):
     rw = _c(recv_w, np.float32)
     lib().orc_scale_rows(_p(h), _dtype_of(h), I, rows, _p(rw), _p(hs))
     return hs
+
+
+def w2_absorbed(h, recv_w, w2, off_e, cnt_e, rows=None):
+    """Absorbed W2 projection of the listed receive rows (all rows if None):
+    returns (y as bf16 bits [n, H], its fp64 value before rounding [n, H]).
+    h is bf16 bits [rows, I]; w2 is bf16 bits [E, H, I]."""
+    h = _c(h, np.uint16)
+    w2 = _c(w2, np.uint16)
+    E, H, I = w2.shape
+    assert h.shape[1] == I
+    off_e = _c(off_e, np.int32)
+    cnt_e = _c(cnt_e, np.int32)
+    assert off_e.shape == (E + 1,) and cnt_e.shape == (E,)
+    rows = np.arange(h.shape[0], dtype=np.int64) if rows is None else _c(rows, np.int64)
+    assert rows.size == 0 or (rows.min() >= 0 and rows.max() < h.shape[0])
+    rw = _c(recv_w, np.float32)
+    y = np.zeros((rows.size, H), np.uint16)
+    y64 = np.zeros((rows.size, H), np.float64)
+    lib().orc_w2_absorbed(_p(h), I, _p(rw), _p(w2), H, E, _p(off_e), _p(cnt_e), _p(rows),
+                          rows.size, _p(y), _p(y64))
+    return y, y64
+
+
+def f64_to_bf16(a):
+    """Round-to-nearest-even of fp64 values to bf16 bits, rounding once."""
+    a = _c(a, np.float64)
+    out = np.zeros(a.shape, np.uint16)
+    lib().orc_f64_to_bf16(_p(a), a.size, _p(out))
+    return out
 
 
 def scale_rows_bwd(ghs, h, recv_w, lay, rows=None):

@@ -69,6 +69,24 @@ uint16_t float_to_bf16_bits(float f) {
   return static_cast<uint16_t>(upper);
 }
 
+// Round-to-nearest-even of an fp64 value to bfloat16, rounding once: the fp32
+// conversion can land exactly on a bfloat16 midpoint that the fp64 value is
+// not on; the value is then moved one fp32 step toward the fp64 value, so the
+// bfloat16 rounding sees which side of the midpoint it lies.
+uint16_t double_to_bf16_bits(double x) {
+  float f = static_cast<float>(x);
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0xffffu) == 0x8000u && static_cast<double>(f) != x && std::isfinite(f)) {
+    if (std::fabs(x) > std::fabs(static_cast<double>(f)))
+      u += 1;
+    else
+      u -= 1;
+    std::memcpy(&f, &u, 4);
+  }
+  return float_to_bf16_bits(f);
+}
+
 float load_elem(const void* base, int dtype, int64_t i) {
   if (dtype == DT_BF16) return bf16_bits_to_float(static_cast<const uint16_t*>(base)[i]);
   return static_cast<const float*>(base)[i];
@@ -601,6 +619,49 @@ void orc_combine_reduce(const void* partial, int dtype, int64_t H, int64_t T, in
       }
       store_elem(out, dtype, t * H + h, acc);
     }
+}
+
+// Router-score absorption fused with the W2 projection ([Titan-absorb]
+// "Implementation": GroupedLinear scales the W2 input by the routed score in
+// float32 and restores the input dtype before the grouped GEMM, so the W2 GEMM
+// of expert e consumes the scaled rows of e's receive segment):
+//   e(r)    = the expert whose receive segment [off_e[e], off_e[e+1]) holds r
+//   hs[r,i] = round_bf16(h[r,i] * recv_w[r])                     (fp32 product)
+//   y[r,n]  = round_bf16(sum_i hs[r,i] * W2[e(r)][n,i])   (fp64 sum, one rounding)
+// for the real rows of a segment (r - off_e[e] < cnt_e[e]); a pad row of a
+// padded layout, or a row outside every segment, is 0.  W2 is stored
+// [E][H][I]: output column n of expert e is the I-vector W2[e][n].  Only the
+// listed rows are computed: y and y64 are [nrows, H].
+void orc_w2_absorbed(const uint16_t* h, int64_t I, const float* recv_w, const uint16_t* w2,
+                     int64_t H, int E, const int32_t* off_e, const int32_t* cnt_e,
+                     const int64_t* rows, int64_t nrows, uint16_t* y, double* y64) {
+  std::vector<double> hs(static_cast<size_t>(I));
+  for (int64_t j = 0; j < nrows; ++j) {
+    const int64_t r = rows[j];
+    int e = -1;
+    for (int c = 0; c < E; ++c)
+      if (r >= off_e[c] && r < off_e[c + 1]) e = c;
+    const bool real = e >= 0 && r - off_e[e] < cnt_e[e];
+    if (real)
+      for (int64_t i = 0; i < I; ++i) {
+        const float scaled = bf16_bits_to_float(h[r * I + i]) * recv_w[r];
+        hs[i] = bf16_bits_to_float(float_to_bf16_bits(scaled));
+      }
+    for (int64_t n = 0; n < H; ++n) {
+      double acc = 0.0;
+      if (real) {
+        const uint16_t* wrow = w2 + (static_cast<int64_t>(e) * H + n) * I;
+        for (int64_t i = 0; i < I; ++i) acc += hs[i] * static_cast<double>(bf16_bits_to_float(wrow[i]));
+      }
+      y64[j * H + n] = acc;
+      y[j * H + n] = double_to_bf16_bits(acc);
+    }
+  }
+}
+
+// fp64 -> bfloat16 round-to-nearest-even of n values (for the tests' pins).
+void orc_f64_to_bf16(const double* src, int64_t n, uint16_t* dst) {
+  for (int64_t i = 0; i < n; ++i) dst[i] = double_to_bf16_bits(src[i]);
 }
 
 }  // extern "C"
