@@ -33,7 +33,7 @@ EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_handle_create", "moe
            "moe_combine", "moe_combine_bwd", "moe_dispatch_bwd", "moe_scale_rows",
            "moe_scale_rows_bwd", "moe_read_device_status", "moe_clear_device_status",
            "moe_dispatch_layout_static", "moe_route_bwd", "moe_expand", "moe_combine_partial",
-           "moe_combine_reduce")
+           "moe_combine_reduce", "moe_w2_absorbed")
 MOE_LAYOUT_STATIC_COUNTERS = 65536
 MOE_LAYOUT_TILE_TOKENS = 512
 
@@ -93,6 +93,7 @@ def lib():
             "moe_expand": ([P, P, i32, i32, P, P], st),
             "moe_combine_partial": ([P, P, i32, i32, P, P, P], st),
             "moe_combine_reduce": ([P, P, i32, i32, P, P], st),
+            "moe_w2_absorbed": ([P, P, i32, P, P, i32, P, P], st),
         }
         for name, (args, res) in sigs.items():
             f = getattr(L, name)
@@ -331,6 +332,18 @@ def moe_scale_rows_bwd(h, ghs, hrows, recv_w, gh, gw, stream=None):
                                                           _ptr(gw), _stream(stream)))
 
 
+def moe_w2_absorbed(h, hrows, recv_w, w2, y, stream=None):
+    """y = bf16(bf16(h * recv_w) @ W2[e].T) per expert segment (W2 [E, H, I])."""
+    I = hrows.shape[1]
+    H = w2.shape[1]
+    _req(hrows, torch.bfloat16, (h.recv_rows, I), "h")
+    _req(recv_w, torch.float32, (h.recv_rows,), "recv_w")
+    _req(w2, torch.bfloat16, (h.E, H, I), "w2")
+    _req(y, torch.bfloat16, (h.recv_rows, H), "y")
+    _check("moe_w2_absorbed", lib().moe_w2_absorbed(h.ptr, _ptr(hrows), I, _ptr(recv_w), _ptr(w2),
+                                                    H, _ptr(y), _stream(stream)))
+
+
 def moe_read_device_status(h):
     flags = ctypes.c_uint32(0)
     _check("moe_read_device_status", lib().moe_read_device_status(h.ptr, ctypes.byref(flags)))
@@ -460,6 +473,11 @@ class MoeRouter:
         hs = torch.empty_like(hrows)
         moe_scale_rows(self.h, hrows, recv_w, hs, stream)
         return hs
+
+    def w2_absorbed(self, hrows, recv_w, w2, stream=None):
+        y = torch.empty(hrows.shape[0], w2.shape[1], dtype=torch.bfloat16, device=hrows.device)
+        moe_w2_absorbed(self.h, hrows, recv_w, w2, y, stream)
+        return y
 
     def scale_rows_bwd(self, ghs, hrows, recv_w, stream=None):
         gh = torch.empty_like(hrows)

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoeroute.so")
-SOURCES = ["route.cu", "layout.cu", "rows.cu", "api.cu", "layout_static.cu"]
+SOURCES = ["route.cu", "layout.cu", "rows.cu", "api.cu", "layout_static.cu", "w2_gemm.cu"]
 
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

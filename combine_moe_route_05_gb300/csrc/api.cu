@@ -10,7 +10,6 @@
 namespace moe {
 size_t layout_smem_bytes(int E, int R);
 cudaError_t prepare_layout_kernels();
-cudaError_t prepare_dispatch_kernel();
 }  // namespace moe
 
 namespace {
@@ -142,7 +141,7 @@ moe_status moe_handle_create(const moe_config* c, void* d_workspace, size_t work
     return MOE_ERR_CUDA;
   // fails with "no kernel image" on a device the library was not built for
   if (moe::prepare_layout_kernels() != cudaSuccess) return MOE_ERR_CUDA;
-  if (moe::prepare_dispatch_kernel() != cudaSuccess) return MOE_ERR_CUDA;
+  if (moe::prepare_w2_kernel() != cudaSuccess) return MOE_ERR_CUDA;
 
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
   if (cudaMemset(ws, 0, p.S + sizeof(int32_t)) != cudaSuccess) return MOE_ERR_CUDA;
@@ -329,6 +328,20 @@ moe_status moe_scale_rows_bwd(const moe_handle* h, const void* d_ghs, const void
   if (!d_recv_w || !aligned(d_recv_w, 4) || !d_gw || !aligned(d_gw, 4)) return MOE_ERR_INVALID;
   return from_cuda(moe::launch_scale_rows_bwd(h, d_ghs, d_h, I, dtype, d_recv_w, d_gh, d_gw,
                                               as_stream(stream)));
+}
+
+moe_status moe_w2_absorbed(const moe_handle* h, const void* d_h, int32_t I, const float* d_recv_w,
+                           const void* d_w2, int32_t H, void* d_y, void* stream) {
+  if (!h) return MOE_ERR_INVALID;
+  if (!moe::w2_shape_ok(I, H)) return MOE_ERR_INVALID;
+  if (static_cast<int64_t>(h->cfg.num_experts) * H > INT32_MAX) return MOE_ERR_INVALID;
+  if (h->T < 0) return MOE_ERR_STATE;
+  if (static_cast<int64_t>(h->T) * h->cfg.top_k + static_cast<int64_t>(h->cfg.num_experts) * (h->pad - 1) == 0)
+    return MOE_OK;
+  if (!d_h || !d_w2 || !d_y) return MOE_ERR_INVALID;
+  if (!aligned(d_h, 16) || !aligned(d_w2, 16) || !aligned(d_y, 16)) return MOE_ERR_INVALID;
+  if (!d_recv_w || !aligned(d_recv_w, 4)) return MOE_ERR_INVALID;
+  return from_cuda(moe::launch_w2_absorbed(h, d_h, I, d_recv_w, d_w2, H, d_y, as_stream(stream)));
 }
 
 moe_status moe_read_device_status(const moe_handle* h, uint32_t* host_flags) {

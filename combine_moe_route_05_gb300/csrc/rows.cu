@@ -534,7 +534,6 @@ cudaError_t launch_combine_bwd_t(const moe_handle* h, const void* g, const void*
 
 }  // namespace
 
-cudaError_t prepare_dispatch_kernel() { return cudaSuccess; }
 
 cudaError_t launch_dispatch(const moe_handle* h, const void* x, int64_t row_bytes, const float* w,
                             void* recv, float* recv_w, void* send, cudaStream_t s) {

@@ -1,0 +1,434 @@
+// Router-score absorption fused into the W2 grouped GEMM, on the fifth-
+// generation tensor cores (tcgen05 MMA, accumulators in tensor memory, TMA
+// operand loads).
+//
+// What it computes ([Titan-absorb] "Implementation": the W2 input is scaled by
+// the routed score in float32 and restored to its dtype before the grouped
+// GEMM; the pages' "FusedMOE" section names an SM100+ fused MoE backend as the
+// direction): for every receive row r of expert e's segment,
+//   hs[r,i] = round_bf16(h[r,i] * recv_w[r])
+//   y[r,n]  = round_bf16(sum_i hs[r,i] * W2[e][n,i])      (fp32 accumulation)
+// with W2 stored [E][H][I].  The scaling is the GEMM's prologue: the scaled
+// rows never reach HBM.  A pad row of a padded layout gets y = 0.
+//
+// One CTA computes one 128 x 256 output tile of one expert (a tile never
+// straddles two experts: the expert's segment is cut into 128-row tiles, the
+// last one ragged).  Warp roles:
+//   warp 0     TMA producer: h slice [128 x 64] and W2 slice [256 x 64] per
+//              stage, 128-byte swizzled, into a 4-stage ring;
+//   warps 2-5  prologue: scale their row of the h slice in shared memory by
+//              the row's score (fp32 product, bf16 round-to-nearest-even);
+//              then the epilogue: tensor memory -> registers -> bf16 -> HBM;
+//   warp 1     tensor memory allocation, and one thread issuing the MMAs
+//              (four K=16 steps per stage) and the commits that free a stage.
+// Every wait is bounded; a wait that gives up raises MOE_DEVERR_TIMEOUT and
+// the CTA winds down (copies in flight are waited for, tensor memory freed).
+#include <cuda.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;     // rows per tile: the MMA's M, one tensor-memory lane per row
+constexpr int kBN = 256;     // output columns per tile: the MMA's N
+constexpr int kBK = 64;      // contraction per stage: one 128-byte swizzle row of bf16
+constexpr int kUmmaK = 16;   // contraction per MMA instruction (16-bit operands)
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kABytes = kBM * kBK * 2;
+constexpr uint32_t kBBytes = kBN * kBK * 2;
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr uint32_t kTmemCols = kBN;  // fp32 accumulator, one column per output column
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes + 256;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A
+// and B bf16 (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
+// in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (static_cast<uint32_t>(kBN >> 3) << 17) |
+                            (static_cast<uint32_t>(kBM >> 4) << 24);
+
+struct W2Args {
+  const float* recv_w;
+  const int32_t* off_e;
+  const int32_t* cnt_e;
+  __nv_bfloat16* y;
+  uint32_t* flags;
+  int E, I, H;
+  int n_tiles;  // H / kBN
+};
+
+// Shared-memory matrix descriptor of a K-major operand tile in the 128-byte
+// swizzle layout (rows of 128 bytes, 8-row groups 1024 bytes apart): start
+// address >> 4 in bits 0-13, leading offset 16 B (unused by this layout) in
+// bits 16-29, stride offset 1024 B >> 4 in bits 32-45, descriptor version 1 in
+// bits 46-47, base offset 0 (tiles are 1024-byte aligned), swizzle mode 2
+// (128-byte) in bits 61-63.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3ffffu) >> 4);
+  d |= static_cast<uint64_t>(16 >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `bar` with the given parity; false after ~1 s.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one M=128 x N=256 x K=16 step.
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+// 32 consecutive fp32 columns of this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+struct TileInfo {
+  int expert;   // -1: no tile for this CTA
+  int row0;     // first receive row of the tile
+  int seg_end;  // end of the expert's segment (pads included)
+  int real_end; // end of the expert's real rows
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    w2_absorbed_kernel(const __grid_constant__ CUtensorMap tm_h,
+                       const __grid_constant__ CUtensorMap tm_w2, W2Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  // operand tiles start on 1024-byte shared-memory boundaries (the swizzle
+  // pattern repeats every 8 rows of 128 bytes)
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sA = smem;                        // [kStages][kBM x kBK] bf16, swizzled
+  uint8_t* sB = smem + kStages * kABytes;    // [kStages][kBN x kBK] bf16, swizzled
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* full = bars;                     // TMA landed
+  uint64_t* ready = bars + kStages;          // h slice scaled
+  uint64_t* empty = bars + 2 * kStages;      // MMAs done with the stage
+  uint64_t* acc_full = bars + 3 * kStages;   // accumulator complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 1);
+  TileInfo* tile = reinterpret_cast<TileInfo*>(tmem_slot + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = blockIdx.x / a.n_tiles, nt = blockIdx.x % a.n_tiles;
+  const int nkb = (a.I + kBK - 1) / kBK;
+
+  if (warp == 0) {
+    // which expert's segment holds m-tile mt: a running scan of per-expert
+    // tile counts, 32 experts per step
+    int running = 0;
+    TileInfo ti{-1, 0, 0, 0};
+    for (int base = 0; base < a.E; base += 32) {
+      const int e = base + lane;
+      int lo = 0, seg = 0;
+      if (e < a.E) {
+        lo = a.off_e[e];
+        seg = a.off_e[e + 1] - lo;
+      }
+      const int tiles = (seg + kBM - 1) / kBM;
+      int incl = tiles;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += o;
+      }
+      const int first = running + incl - tiles;
+      const bool hit = tiles > 0 && mt >= first && mt < first + tiles;
+      const uint32_t b = __ballot_sync(0xffffffffu, hit);
+      if (b) {
+        const int src = __ffs(b) - 1;
+        if (lane == src) {
+          ti.expert = e;
+          ti.row0 = lo + (mt - first) * kBM;
+          ti.seg_end = lo + seg;
+          ti.real_end = lo + a.cnt_e[e];
+        }
+        ti.expert = __shfl_sync(0xffffffffu, ti.expert, src);
+        ti.row0 = __shfl_sync(0xffffffffu, ti.row0, src);
+        ti.seg_end = __shfl_sync(0xffffffffu, ti.seg_end, src);
+        ti.real_end = __shfl_sync(0xffffffffu, ti.real_end, src);
+        break;
+      }
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      *tile = ti;
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(&full[s], 1);
+        mbar_init(&ready[s], 4);
+        mbar_init(&empty[s], 1);
+      }
+      mbar_init(acc_full, 1);
+      fence_mbar_init();
+    }
+  }
+  __syncthreads();
+  const TileInfo ti = *tile;
+  if (ti.expert < 0) return;  // uniform: more CTAs are launched than there are tiles
+
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  bool ok = true;
+  if (warp == 0) {
+    if (lane == 0) {
+      int issued = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % kStages;
+        const uint32_t ph = (kb / kStages) & 1u;
+        if (kb >= kStages && !wait_phase(&empty[s], ph ^ 1u)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], kStageBytes);
+        tma_load_2d(sA + s * kABytes, &tm_h, kb * kBK, ti.row0, &full[s]);
+        tma_load_2d(sB + s * kBBytes, &tm_w2, kb * kBK, ti.expert * a.H + nt * kBN, &full[s]);
+        ++issued;
+      }
+      // the last stages' copies must have landed before the CTA may exit
+      for (int kb = issued - kStages < 0 ? 0 : issued - kStages; kb < issued; ++kb)
+        if (!wait_phase(&full[kb % kStages], (kb / kStages) & 1u)) ok = false;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % kStages;
+        const uint32_t ph = (kb / kStages) & 1u;
+        if (!wait_phase(&ready[s], ph)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_addr(sA + s * kABytes), b0 = smem_addr(sB + s * kBBytes);
+#pragma unroll
+        for (int k = 0; k < kBK / kUmmaK; ++k)
+          umma_bf16(tmem, sw128_desc(a0 + k * kUmmaK * 2), sw128_desc(b0 + k * kUmmaK * 2),
+                    (kb | k) != 0);
+        umma_commit(&empty[s]);
+      }
+      umma_commit(acc_full);
+    }
+  } else {
+    // prologue: thread t scales row t of each h slice
+    const int t = threadIdx.x - 64;
+    const int row = ti.row0 + t;
+    const float score = row < ti.real_end ? __ldg(a.recv_w + row) : 0.0f;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb % kStages;
+      const uint32_t ph = (kb / kStages) & 1u;
+      // each lane waits itself (acquiring the copy); the warp leaves together
+      const bool got = wait_phase(&full[s], ph);
+      if (!__all_sync(0xffffffffu, got)) {
+        ok = false;
+        break;
+      }
+      uint8_t* line = sA + s * kABytes + t * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        // a rotated chunk order keeps the eight threads of a shared-memory
+        // phase on distinct banks (the row's chunks are permuted by the
+        // swizzle, but all eight stay within the row's 128 bytes)
+        uint4* p = reinterpret_cast<uint4*>(line + ((c + t) & 7) * 16);
+        uint4 v = *p;
+        uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float lo = __fmul_rn(__uint_as_float(u[j] << 16), score);
+          const float hi = __fmul_rn(__uint_as_float(u[j] & 0xffff0000u), score);
+          u[j] = pack_bf16x2(lo, hi);
+        }
+        *p = v;
+      }
+      fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ready[s]);
+    }
+    // epilogue: lanes of tensor-memory quarter (warp % 4) are tile rows
+    // 32 * (warp % 4) + lane
+    if (ok) ok = __all_sync(0xffffffffu, wait_phase(acc_full, 0));
+    tc_fence_after();
+    const int q = warp & 3;
+    const int erow = ti.row0 + q * 32 + lane;
+    const bool real = erow < ti.real_end;
+    const bool pad = !real && erow < ti.seg_end;
+    __nv_bfloat16* dst = a.y + static_cast<size_t>(erow) * a.H + nt * kBN;
+    if (ok) {
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v);
+        if (real || pad) {
+          Vec16 o[4];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            o[j >> 2].u[j & 3] =
+                real ? pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])) : 0u;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) st_vec(dst + c * 32 + j * 8, o[j]);
+        }
+      }
+    }
+  }
+  if (!ok) raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    // the accumulator must be complete before its columns are released; on
+    // the normal path this returns at once
+    if (lane == 0 && !wait_phase(acc_full, 0)) raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
+    __syncwarp();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiled>(p);
+  }();
+  return fn;
+}
+
+// 2-D bf16 tensor map of a row-major [rows, cols] matrix, box [box_rows, kBK]
+// with the 128-byte swizzle; out-of-range elements read as zero.
+bool encode_rows(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t prepare_w2_kernel() {
+  return cudaFuncSetAttribute(w2_absorbed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kSmemBytes));
+}
+
+bool w2_shape_ok(int I, int H) { return I >= 8 && I % 8 == 0 && H >= kBN && H % kBN == 0; }
+
+cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, const float* recv_w,
+                               const void* w2, int H, void* y, cudaStream_t s) {
+  const moe_config& c = h->cfg;
+  const int E = c.num_experts;
+  const long long rows_cap = static_cast<long long>(h->T) * c.top_k +
+                             static_cast<long long>(E) * (h->pad - 1);
+  if (rows_cap <= 0) return cudaSuccess;
+  CUtensorMap tm_h, tm_w2;
+  if (!encode_rows(&tm_h, hrows, static_cast<uint64_t>(rows_cap), I, kBM) ||
+      !encode_rows(&tm_w2, w2, static_cast<uint64_t>(E) * H, I, kBN))
+    return cudaErrorInvalidValue;
+  W2Args a;
+  a.recv_w = recv_w;
+  a.off_e = h->off_e;
+  a.cnt_e = h->cnt_e;
+  a.y = static_cast<__nv_bfloat16*>(y);
+  a.flags = h->flags;
+  a.E = E;
+  a.I = I;
+  a.H = H;
+  a.n_tiles = H / kBN;
+  // sum over experts of ceil(segment / kBM) <= (rows + E * (kBM - 1)) / kBM
+  const long long m_tiles = (rows_cap + static_cast<long long>(E) * (kBM - 1)) / kBM;
+  const long long grid = m_tiles * a.n_tiles;
+  if (static_cast<long long>(E) * H > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  w2_absorbed_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(tm_h, tm_w2, a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -338,6 +338,27 @@ moe_status moe_scale_rows_bwd(const moe_handle* h, const void* d_ghs, const void
                               void* stream);
 
 /*
+ * Router-score absorption fused into the W2 grouped GEMM ([Titan-absorb]
+ * "Implementation": GroupedLinear scales the W2 input by the routed score in
+ * float32 and restores the input dtype before the grouped GEMM; the same
+ * page's "FusedMOE" section points at an SM100+ fused MoE backend).  For each
+ * receive row r of expert e's segment in the current layout:
+ *   hs[r,i] = round_bf16(d_h[r,i] * d_recv_w[r])          (fp32 product)
+ *   d_y[r,n] = round_bf16(sum_i hs[r,i] * d_w2[e][n,i])    (fp32 accumulation)
+ * The scaled rows hs exist only on chip (the GEMM's prologue); the products
+ * run on the tensor cores.  A pad row of a padded layout gets d_y = 0.
+ *   d_h     bf16 [T*K + E*(pad_align-1), I] receive rows (expert-grouped)
+ *   d_recv_w fp32 per receive row (as written by moe_dispatch)
+ *   d_w2    bf16 [E, H, I]: row n of expert e holds the I weights of output n
+ *   d_y     bf16 [T*K + E*(pad_align-1), H]; rows outside the segments untouched
+ * All device pointers caller-owned and 16-byte aligned.  Requires I % 8 == 0,
+ * H % 256 == 0 and E*H < 2^31, else MOE_ERR_INVALID; MOE_ERR_STATE before the
+ * first layout.  bf16 only.
+ */
+moe_status moe_w2_absorbed(const moe_handle* h, const void* d_h, int32_t I, const float* d_recv_w,
+                           const void* d_w2, int32_t H, void* d_y, void* stream);
+
+/*
  * Copies the device status word to *host_flags (MOE_DEVERR_* bits).  This
  * SYNCHRONISES the handle's device; keep it off the hot path.
  */

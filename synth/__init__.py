@@ -184,11 +184,16 @@ def make_inputs(wl, seed=None, want=("logits", "bias", "x", "y", "g")):
         elif k == "ghs":
             out[k] = normal_bf16(seed, "ghs", (wl.T * wl.K, wl.I))
         elif k == "w2":
-            w2 = normal_f32(seed, "w2", (wl.E, wl.I, wl.H)) * np.float32(1.0 / np.sqrt(wl.I))
-            out[k] = to_bf16_bits(w2)
+            out[k] = w2_weights(seed, wl.E, wl.H, wl.I)
         else:
             raise KeyError(k)
     return out
+
+
+def w2_weights(seed, E, H, I):
+    """Random W2 weights, bf16 bits [E, H, I] ~ N(0, 1/I): row n of expert e
+    holds the I input weights of output n."""
+    return to_bf16_bits(normal_f32(seed, "w2", (E, H, I)) * np.float32(1.0 / np.sqrt(I)))
 
 
 def shard_seed(seed, rank):
