@@ -11,16 +11,18 @@
 // with W2 stored [E][H][I].  The scaling is the GEMM's prologue: the scaled
 // rows never reach HBM.  A pad row of a padded layout gets y = 0.
 //
-// One CTA computes one 128 x 256 output tile of one expert (a tile never
-// straddles two experts: the expert's segment is cut into 128-row tiles, the
-// last one ragged).  Warp roles:
+// A persistent CTA per SM walks 128 x 256 output tiles of the experts (a tile
+// never straddles two experts: each expert's segment is cut into 128-row
+// tiles, the last one ragged).  Warp roles:
 //   warp 0     TMA producer: h slice [128 x 64] and W2 slice [256 x 64] per
 //              stage, 128-byte swizzled, into a 4-stage ring;
-//   warps 2-5  prologue: scale their row of the h slice in shared memory by
+//   warps 2-5  prologue: scale their row of each h slice in shared memory by
 //              the row's score (fp32 product, bf16 round-to-nearest-even);
-//              then the epilogue: tensor memory -> registers -> bf16 -> HBM;
-//   warp 1     tensor memory allocation, and one thread issuing the MMAs
-//              (four K=16 steps per stage) and the commits that free a stage.
+//   warp 1     tensor memory allocation (two 256-column accumulators), and one
+//              thread issuing the MMAs (four K=16 steps per stage) and the
+//              commits that free a stage or hand over an accumulator;
+//   warps 6-9  epilogue: tensor memory -> registers -> bf16 rows in HBM,
+//              overlapping the next tile's MMAs in the other accumulator.
 // Every wait is bounded; a wait that gives up raises MOE_DEVERR_TIMEOUT and
 // the CTA winds down (copies in flight are waited for, tensor memory freed).
 #include <cuda.h>
@@ -36,12 +38,14 @@ constexpr int kBN = 256;     // output columns per tile: the MMA's N
 constexpr int kBK = 64;      // contraction per stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;   // contraction per MMA instruction (16-bit operands)
 constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // warps: 0 TMA, 1 MMA, 2-5 prologue, 6-9 epilogue
 constexpr uint32_t kABytes = kBM * kBK * 2;
 constexpr uint32_t kBBytes = kBN * kBK * 2;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kTmemCols = kBN;  // fp32 accumulator, one column per output column
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes + 256;
+constexpr uint32_t kTmemCols = kBN;  // one fp32 accumulator: a column per output column
+// operand ring, barriers and the tables of at most MOE_MAX_EXPERTS experts
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes + 256 +
+                              sizeof(int32_t) * (3 * MOE_MAX_EXPERTS + 2);
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A
@@ -152,13 +156,46 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
-struct TileInfo {
-  int expert;   // -1: no tile for this CTA
-  int row0;     // first receive row of the tile
-  int seg_end;  // end of the expert's segment (pads included)
-  int real_end; // end of the expert's real rows
+// Shared-memory tables of one CTA: the layout's expert segments and, per
+// expert, the index of its first 128-row m-tile (tile_first[E] = all m-tiles).
+struct Tables {
+  int32_t* tile_first;  // [E + 1]
+  int32_t* off;         // [E + 1]
+  int32_t* cnt;         // [E]
 };
 
+struct Tile {
+  int expert, row0, nt;
+  int seg_end;   // end of the expert's segment (pads included)
+  int real_end;  // end of the expert's real rows
+};
+
+// Tile `tile` (n-tile fastest) -> expert and rows: the last expert whose first
+// m-tile is <= the tile's m-tile (an empty expert shares its first m-tile with
+// the next expert and is never the last such one).
+__device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles, int tile) {
+  const int mt = tile / n_tiles;
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tb.tile_first[mid] <= mt)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  Tile t;
+  t.expert = lo;
+  t.nt = tile - mt * n_tiles;
+  t.row0 = tb.off[lo] + (mt - tb.tile_first[lo]) * kBM;
+  t.seg_end = tb.off[lo + 1];
+  t.real_end = tb.off[lo] + tb.cnt[lo];
+  return t;
+}
+
+// Persistent: CTA b takes tiles b, b + gridDim.x, ... in every role, so the
+// four roles walk the same tile sequence.  The stage ring runs on across
+// tiles; the two accumulators alternate, so the epilogue of one tile overlaps
+// the MMAs of the next.
 __global__ void __launch_bounds__(kThreads, 1)
     w2_absorbed_kernel(const __grid_constant__ CUtensorMap tm_h,
                        const __grid_constant__ CUtensorMap tm_w2, W2Args a) {
@@ -166,77 +203,60 @@ __global__ void __launch_bounds__(kThreads, 1)
   // operand tiles start on 1024-byte shared-memory boundaries (the swizzle
   // pattern repeats every 8 rows of 128 bytes)
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sA = smem;                        // [kStages][kBM x kBK] bf16, swizzled
-  uint8_t* sB = smem + kStages * kABytes;    // [kStages][kBN x kBK] bf16, swizzled
+  uint8_t* sA = smem;                      // [kStages][kBM x kBK] bf16, swizzled
+  uint8_t* sB = smem + kStages * kABytes;  // [kStages][kBN x kBK] bf16, swizzled
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint64_t* full = bars;                     // TMA landed
-  uint64_t* ready = bars + kStages;          // h slice scaled
-  uint64_t* empty = bars + 2 * kStages;      // MMAs done with the stage
-  uint64_t* acc_full = bars + 3 * kStages;   // accumulator complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kStages + 1);
-  TileInfo* tile = reinterpret_cast<TileInfo*>(tmem_slot + 4);
+  uint64_t* full = bars;                   // TMA landed
+  uint64_t* ready = bars + kStages;        // h slice scaled
+  uint64_t* empty = bars + 2 * kStages;    // MMAs done with the stage
+  uint64_t* acc_full = bars + 3 * kStages; // [2] accumulator complete
+  uint64_t* acc_empty = acc_full + 2;      // [2] accumulator drained
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  Tables tb;
+  tb.tile_first = reinterpret_cast<int32_t*>(tmem_slot + 4);
+  tb.off = tb.tile_first + (a.E + 1);
+  tb.cnt = tb.off + (a.E + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = blockIdx.x / a.n_tiles, nt = blockIdx.x % a.n_tiles;
   const int nkb = (a.I + kBK - 1) / kBK;
 
+  for (int e = threadIdx.x; e <= a.E; e += kThreads) {
+    tb.off[e] = a.off_e[e];
+    if (e < a.E) tb.cnt[e] = a.cnt_e[e];
+  }
+  __syncthreads();
   if (warp == 0) {
-    // which expert's segment holds m-tile mt: a running scan of per-expert
-    // tile counts, 32 experts per step
+    // exclusive scan of the per-expert m-tile counts
     int running = 0;
-    TileInfo ti{-1, 0, 0, 0};
     for (int base = 0; base < a.E; base += 32) {
       const int e = base + lane;
-      int lo = 0, seg = 0;
-      if (e < a.E) {
-        lo = a.off_e[e];
-        seg = a.off_e[e + 1] - lo;
-      }
-      const int tiles = (seg + kBM - 1) / kBM;
+      const int tiles = e < a.E ? (tb.off[e + 1] - tb.off[e] + kBM - 1) / kBM : 0;
       int incl = tiles;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
         const int o = __shfl_up_sync(0xffffffffu, incl, d);
         if (lane >= d) incl += o;
       }
-      const int first = running + incl - tiles;
-      const bool hit = tiles > 0 && mt >= first && mt < first + tiles;
-      const uint32_t b = __ballot_sync(0xffffffffu, hit);
-      if (b) {
-        const int src = __ffs(b) - 1;
-        if (lane == src) {
-          ti.expert = e;
-          ti.row0 = lo + (mt - first) * kBM;
-          ti.seg_end = lo + seg;
-          ti.real_end = lo + a.cnt_e[e];
-        }
-        ti.expert = __shfl_sync(0xffffffffu, ti.expert, src);
-        ti.row0 = __shfl_sync(0xffffffffu, ti.row0, src);
-        ti.seg_end = __shfl_sync(0xffffffffu, ti.seg_end, src);
-        ti.real_end = __shfl_sync(0xffffffffu, ti.real_end, src);
-        break;
-      }
+      if (e < a.E) tb.tile_first[e] = running + incl - tiles;
       running += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) {
-      *tile = ti;
+      tb.tile_first[a.E] = running;
       for (int s = 0; s < kStages; ++s) {
         mbar_init(&full[s], 1);
         mbar_init(&ready[s], 4);
         mbar_init(&empty[s], 1);
       }
-      mbar_init(acc_full, 1);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&acc_full[i], 1);
+        mbar_init(&acc_empty[i], 4);
+      }
       fence_mbar_init();
     }
-  }
-  __syncthreads();
-  const TileInfo ti = *tile;
-  if (ti.expert < 0) return;  // uniform: more CTAs are launched than there are tiles
-
-  if (warp == 1) {
+  } else if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
-                 "r"(kTmemCols)
+                 "r"(2 * kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -244,95 +264,122 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int total = tb.tile_first[a.E] * a.n_tiles;
 
   bool ok = true;
   if (warp == 0) {
     if (lane == 0) {
-      int issued = 0;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t ph = (kb / kStages) & 1u;
-        if (kb >= kStages && !wait_phase(&empty[s], ph ^ 1u)) {
-          ok = false;
-          break;
+      int it = 0;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode_tile(tb, a.E, a.n_tiles, tile);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          if (it >= kStages && !wait_phase(&empty[s], ph ^ 1u)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], kStageBytes);
+          tma_load_2d(sA + s * kABytes, &tm_h, kb * kBK, t.row0, &full[s]);
+          tma_load_2d(sB + s * kBBytes, &tm_w2, kb * kBK, t.expert * a.H + t.nt * kBN, &full[s]);
         }
-        mbar_arrive_expect_tx(&full[s], kStageBytes);
-        tma_load_2d(sA + s * kABytes, &tm_h, kb * kBK, ti.row0, &full[s]);
-        tma_load_2d(sB + s * kBBytes, &tm_w2, kb * kBK, ti.expert * a.H + nt * kBN, &full[s]);
-        ++issued;
       }
       // the last stages' copies must have landed before the CTA may exit
-      for (int kb = issued - kStages < 0 ? 0 : issued - kStages; kb < issued; ++kb)
-        if (!wait_phase(&full[kb % kStages], (kb / kStages) & 1u)) ok = false;
+      for (int j = it - kStages < 0 ? 0 : it - kStages; j < it; ++j)
+        if (!wait_phase(&full[j % kStages], (j / kStages) & 1u)) ok = false;
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int s = kb % kStages;
-        const uint32_t ph = (kb / kStages) & 1u;
-        if (!wait_phase(&ready[s], ph)) {
+      int it = 0, n = 0;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+        const int acc = n & 1;
+        const uint32_t aph = (n >> 1) & 1u;
+        if (n >= 2 && !wait_phase(&acc_empty[acc], aph ^ 1u)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = smem_addr(sA + s * kABytes), b0 = smem_addr(sB + s * kBBytes);
+        const uint32_t d = tmem + acc * kTmemCols;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!wait_phase(&ready[s], ph)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(sA + s * kABytes), b0 = smem_addr(sB + s * kBBytes);
 #pragma unroll
-        for (int k = 0; k < kBK / kUmmaK; ++k)
-          umma_bf16(tmem, sw128_desc(a0 + k * kUmmaK * 2), sw128_desc(b0 + k * kUmmaK * 2),
-                    (kb | k) != 0);
-        umma_commit(&empty[s]);
+          for (int k = 0; k < kBK / kUmmaK; ++k)
+            umma_bf16(d, sw128_desc(a0 + k * kUmmaK * 2), sw128_desc(b0 + k * kUmmaK * 2),
+                      (kb | k) != 0);
+          umma_commit(&empty[s]);
+        }
+        umma_commit(&acc_full[acc]);
       }
-      umma_commit(acc_full);
+    }
+  } else if (warp < 6) {
+    // prologue: thread t scales row t of each h slice of its tiles
+    const int t = threadIdx.x - 64;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile);
+      const int row = ti.row0 + t;
+      const float score = row < ti.real_end ? __ldg(a.recv_w + row) : 0.0f;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        // each lane waits itself (acquiring the copy); the warp leaves together
+        const bool got = wait_phase(&full[s], ph);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        uint8_t* line = sA + s * kABytes + t * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          // a rotated chunk order keeps the eight threads of a shared-memory
+          // phase on distinct banks (the swizzle permutes a row's chunks, but
+          // all eight stay within the row's 128 bytes)
+          uint4* p = reinterpret_cast<uint4*>(line + ((c + t) & 7) * 16);
+          uint4 v = *p;
+          uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float lo = __fmul_rn(__uint_as_float(u[j] << 16), score);
+            const float hi = __fmul_rn(__uint_as_float(u[j] & 0xffff0000u), score);
+            u[j] = pack_bf16x2(lo, hi);
+          }
+          *p = v;
+        }
+        fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ready[s]);
+      }
     }
   } else {
-    // prologue: thread t scales row t of each h slice
-    const int t = threadIdx.x - 64;
-    const int row = ti.row0 + t;
-    const float score = row < ti.real_end ? __ldg(a.recv_w + row) : 0.0f;
-    for (int kb = 0; kb < nkb; ++kb) {
-      const int s = kb % kStages;
-      const uint32_t ph = (kb / kStages) & 1u;
-      // each lane waits itself (acquiring the copy); the warp leaves together
-      const bool got = wait_phase(&full[s], ph);
-      if (!__all_sync(0xffffffffu, got)) {
+    // epilogue: the lanes of tensor-memory quarter (warp % 4) are tile rows
+    // 32 * (warp % 4) + lane
+    const int q = warp & 3;
+    int n = 0;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+      const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile);
+      const int acc = n & 1;
+      const uint32_t aph = (n >> 1) & 1u;
+      if (!__all_sync(0xffffffffu, wait_phase(&acc_full[acc], aph))) {
         ok = false;
         break;
       }
-      uint8_t* line = sA + s * kABytes + t * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        // a rotated chunk order keeps the eight threads of a shared-memory
-        // phase on distinct banks (the row's chunks are permuted by the
-        // swizzle, but all eight stay within the row's 128 bytes)
-        uint4* p = reinterpret_cast<uint4*>(line + ((c + t) & 7) * 16);
-        uint4 v = *p;
-        uint32_t* u = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float lo = __fmul_rn(__uint_as_float(u[j] << 16), score);
-          const float hi = __fmul_rn(__uint_as_float(u[j] & 0xffff0000u), score);
-          u[j] = pack_bf16x2(lo, hi);
-        }
-        *p = v;
-      }
-      fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ready[s]);
-    }
-    // epilogue: lanes of tensor-memory quarter (warp % 4) are tile rows
-    // 32 * (warp % 4) + lane
-    if (ok) ok = __all_sync(0xffffffffu, wait_phase(acc_full, 0));
-    tc_fence_after();
-    const int q = warp & 3;
-    const int erow = ti.row0 + q * 32 + lane;
-    const bool real = erow < ti.real_end;
-    const bool pad = !real && erow < ti.seg_end;
-    __nv_bfloat16* dst = a.y + static_cast<size_t>(erow) * a.H + nt * kBN;
-    if (ok) {
+      tc_fence_after();
+      const int row = ti.row0 + q * 32 + lane;
+      const bool real = row < ti.real_end;
+      const bool pad = !real && row < ti.seg_end;
+      __nv_bfloat16* dst = a.y + static_cast<size_t>(row) * a.H + ti.nt * kBN;
+      const uint32_t taddr = tmem + acc * kTmemCols + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
       for (int c = 0; c < kBN / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 32, v);
+        tmem_ld32(taddr + c * 32, v);
         if (real || pad) {
           Vec16 o[4];
 #pragma unroll
@@ -343,6 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j) st_vec(dst + c * 32 + j * 8, o[j]);
         }
       }
+      tc_fence_before();  // the loads above precede the MMAs that reuse the columns
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
     }
   }
   if (!ok) raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
@@ -350,12 +400,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    // the accumulator must be complete before its columns are released; on
-    // the normal path this returns at once
-    if (lane == 0 && !wait_phase(acc_full, 0)) raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
+    // every MMA must be complete before the columns are released: wait for
+    // the last commit of each accumulator (on the normal path the epilogue
+    // already has, and these return at once)
+    if (lane == 0) {
+      int n = 0;
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) ++n;
+      for (int j = n - 2 < 0 ? 0 : n - 2; j < n; ++j)
+        if (!wait_phase(&acc_full[j & 1], (j >> 1) & 1u)) raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
+    }
     __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
+                 "r"(2 * kTmemCols)
                  : "memory");
   }
 }
@@ -424,10 +480,13 @@ cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, co
   a.n_tiles = H / kBN;
   // sum over experts of ceil(segment / kBM) <= (rows + E * (kBM - 1)) / kBM
   const long long m_tiles = (rows_cap + static_cast<long long>(E) * (kBM - 1)) / kBM;
-  const long long grid = m_tiles * a.n_tiles;
+  const long long tiles = m_tiles * a.n_tiles;
   if (static_cast<long long>(E) * H > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  w2_absorbed_kernel<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, s>>>(tm_h, tm_w2, a);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // one CTA per SM (the operand ring fills its shared memory), never more
+  // CTAs than tiles could exist
+  const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
+  w2_absorbed_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w2, a);
   return cudaGetLastError();
 }
 
