@@ -16,12 +16,14 @@
 // tiles, the last one ragged).  Warp roles:
 //   warp 0     TMA producer: h slice [128 x 64] and W2 slice [256 x 64] per
 //              stage, 128-byte swizzled, into a 4-stage ring;
-//   warps 2-5  prologue: scale their row of each h slice in shared memory by
-//              the row's score (fp32 product, bf16 round-to-nearest-even);
+//   warps 2-9  prologue: scale each h slice in shared memory, two threads per
+//              row, by the row's score (fp32 product, bf16 round-to-nearest-
+//              even), as soon as the slice lands (h and W2 complete on
+//              separate barriers);
 //   warp 1     tensor memory allocation (two 256-column accumulators), and one
 //              thread issuing the MMAs (four K=16 steps per stage) and the
 //              commits that free a stage or hand over an accumulator;
-//   warps 6-9  epilogue: tensor memory -> registers -> bf16 rows in HBM,
+//   warps 10-13 epilogue: tensor memory -> registers -> bf16 rows in HBM,
 //              overlapping the next tile's MMAs in the other accumulator.
 // Every wait is bounded; a wait that gives up raises MOE_DEVERR_TIMEOUT and
 // the CTA winds down (copies in flight are waited for, tensor memory freed).
@@ -38,7 +40,10 @@ constexpr int kBN = 256;     // output columns per tile: the MMA's N
 constexpr int kBK = 64;      // contraction per stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;   // contraction per MMA instruction (16-bit operands)
 constexpr int kStages = 4;
-constexpr int kThreads = 320;  // warps: 0 TMA, 1 MMA, 2-5 prologue, 6-9 epilogue
+constexpr int kPrologueWarps = 8;  // two threads per tile row
+constexpr int kEpilogueWarps = 4;  // one thread per tile row (tensor-memory lane)
+// warps: 0 TMA, 1 MMA, 2-9 prologue, 10-13 epilogue
+constexpr int kThreads = 32 * (2 + kPrologueWarps + kEpilogueWarps);
 constexpr uint32_t kABytes = kBM * kBK * 2;
 constexpr uint32_t kBBytes = kBN * kBK * 2;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
@@ -206,10 +211,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sA = smem;                      // [kStages][kBM x kBK] bf16, swizzled
   uint8_t* sB = smem + kStages * kABytes;  // [kStages][kBN x kBK] bf16, swizzled
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint64_t* full = bars;                   // TMA landed
-  uint64_t* ready = bars + kStages;        // h slice scaled
-  uint64_t* empty = bars + 2 * kStages;    // MMAs done with the stage
-  uint64_t* acc_full = bars + 3 * kStages; // [2] accumulator complete
+  uint64_t* full_a = bars;                  // h slice landed
+  uint64_t* full_b = bars + kStages;        // W2 slice landed
+  uint64_t* ready = bars + 2 * kStages;     // h slice scaled
+  uint64_t* empty = bars + 3 * kStages;     // MMAs done with the stage
+  uint64_t* acc_full = bars + 4 * kStages;  // [2] accumulator complete
   uint64_t* acc_empty = acc_full + 2;      // [2] accumulator drained
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
   Tables tb;
@@ -243,13 +249,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tb.tile_first[a.E] = running;
       for (int s = 0; s < kStages; ++s) {
-        mbar_init(&full[s], 1);
-        mbar_init(&ready[s], 4);
+        mbar_init(&full_a[s], 1);
+        mbar_init(&full_b[s], 1);
+        mbar_init(&ready[s], kPrologueWarps);
         mbar_init(&empty[s], 1);
       }
       for (int i = 0; i < 2; ++i) {
         mbar_init(&acc_full[i], 1);
-        mbar_init(&acc_empty[i], 4);
+        mbar_init(&acc_empty[i], kEpilogueWarps);
       }
       fence_mbar_init();
     }
@@ -279,14 +286,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], kStageBytes);
-          tma_load_2d(sA + s * kABytes, &tm_h, kb * kBK, t.row0, &full[s]);
-          tma_load_2d(sB + s * kBBytes, &tm_w2, kb * kBK, t.expert * a.H + t.nt * kBN, &full[s]);
+          // h and W2 complete on separate barriers: the prologue needs only h
+          mbar_arrive_expect_tx(&full_a[s], kABytes);
+          tma_load_2d(sA + s * kABytes, &tm_h, kb * kBK, t.row0, &full_a[s]);
+          mbar_arrive_expect_tx(&full_b[s], kBBytes);
+          tma_load_2d(sB + s * kBBytes, &tm_w2, kb * kBK, t.expert * a.H + t.nt * kBN, &full_b[s]);
         }
       }
       // the last stages' copies must have landed before the CTA may exit
-      for (int j = it - kStages < 0 ? 0 : it - kStages; j < it; ++j)
-        if (!wait_phase(&full[j % kStages], (j / kStages) & 1u)) ok = false;
+      for (int j = it - kStages < 0 ? 0 : it - kStages; j < it; ++j) {
+        if (!wait_phase(&full_a[j % kStages], (j / kStages) & 1u)) ok = false;
+        if (!wait_phase(&full_b[j % kStages], (j / kStages) & 1u)) ok = false;
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -303,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
-          if (!wait_phase(&ready[s], ph)) {
+          if (!wait_phase(&full_b[s], ph) || !wait_phase(&ready[s], ph)) {
             ok = false;
             break;
           }
@@ -318,31 +329,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&acc_full[acc]);
       }
     }
-  } else if (warp < 6) {
-    // prologue: thread t scales row t of each h slice of its tiles
-    const int t = threadIdx.x - 64;
+  } else if (warp < 2 + kPrologueWarps) {
+    // prologue: two threads per row of each h slice, four of the row's eight
+    // 16-byte chunks each; the row's score is fetched one tile ahead
+    const int p = threadIdx.x - 64;
+    const int prow = p >> 1, half = p & 1;
+    auto score_of = [&](int tile) {
+      if (tile >= total) return 0.0f;
+      const Tile t = decode_tile(tb, a.E, a.n_tiles, tile);
+      const int row = t.row0 + prow;
+      return row < t.real_end ? __ldg(a.recv_w + row) : 0.0f;
+    };
+    float next_score = score_of(blockIdx.x);
     int it = 0;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile);
-      const int row = ti.row0 + t;
-      const float score = row < ti.real_end ? __ldg(a.recv_w + row) : 0.0f;
+      const float score = next_score;
+      next_score = score_of(tile + gridDim.x);
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
         // each lane waits itself (acquiring the copy); the warp leaves together
-        const bool got = wait_phase(&full[s], ph);
+        const bool got = wait_phase(&full_a[s], ph);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
-        uint8_t* line = sA + s * kABytes + t * 128;
+        uint8_t* line = sA + s * kABytes + prow * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          // a rotated chunk order keeps the eight threads of a shared-memory
-          // phase on distinct banks (the swizzle permutes a row's chunks, but
-          // all eight stay within the row's 128 bytes)
-          uint4* p = reinterpret_cast<uint4*>(line + ((c + t) & 7) * 16);
-          uint4 v = *p;
+        for (int c = 0; c < 4; ++c) {
+          // the swizzle permutes a row's chunks within its 128 bytes, and the
+          // score is per row, so the thread takes physical chunks; rotating
+          // them by row keeps the eight threads of a shared-memory phase (four
+          // rows, two halves) on distinct banks
+          uint4* q = reinterpret_cast<uint4*>(line + (half * 4 + ((c + prow) & 3)) * 16);
+          uint4 v = *q;
           uint32_t* u = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -350,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float hi = __fmul_rn(__uint_as_float(u[j] & 0xffff0000u), score);
             u[j] = pack_bf16x2(lo, hi);
           }
-          *p = v;
+          *q = v;
         }
         fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
         __syncwarp();
