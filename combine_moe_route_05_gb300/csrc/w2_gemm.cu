@@ -13,18 +13,21 @@
 //
 // A persistent CTA per SM walks 128 x 256 output tiles of the experts (a tile
 // never straddles two experts: each expert's segment is cut into 128-row
-// tiles, the last one ragged).  Warp roles:
-//   warp 0     TMA producer: h slice [128 x 64] and W2 slice [256 x 64] per
-//              stage, 128-byte swizzled, into a 4-stage ring;
-//   warps 2-9  prologue: scale each h slice in shared memory, two threads per
-//              row, by the row's score (fp32 product, bf16 round-to-nearest-
-//              even), as soon as the slice lands (h and W2 complete on
-//              separate barriers);
-//   warp 1     tensor memory allocation (two 256-column accumulators), and one
-//              thread issuing the MMAs (four K=16 steps per stage) and the
-//              commits that free a stage or hand over an accumulator;
-//   warps 10-13 epilogue: tensor memory -> registers -> bf16 rows in HBM,
-//              overlapping the next tile's MMAs in the other accumulator.
+// tiles, the last one ragged).  The scaled h slice is the MMA's A operand in
+// TENSOR memory, so shared memory carries only the TMA landings, the
+// prologue's read of h and the tensor cores' read of W2.  Warp roles:
+//   warp 2      TMA: h slices [128 x 64] into a 3-stage ring (128-byte
+//               swizzle), freed as soon as the prologue has read them;
+//   warp 0      TMA: W2 slices [256 x 64] into a 5-stage ring;
+//   warps 3-10  prologue: read an h slice (one row per thread, half of its K
+//               range per warp), scale it by the row's score (fp32 product,
+//               bf16 round-to-nearest-even) and store it into one of eight
+//               32-column A stages in tensor memory;
+//   warp 1      tensor memory (one 256-column accumulator + the A stages) and
+//               one thread issuing the MMAs (four K=16 steps per slice) and the
+//               commits that free the stages and hand over the accumulator;
+//   warps 11-18 epilogue: accumulator -> registers -> bf16 rows in HBM (two
+//               warps per lane quarter, half the columns each).
 // Every wait is bounded; a wait that gives up raises MOE_DEVERR_TIMEOUT and
 // the CTA winds down (copies in flight are waited for, tensor memory freed).
 #include <cuda.h>
@@ -39,18 +42,25 @@ constexpr int kBM = 128;     // rows per tile: the MMA's M, one tensor-memory la
 constexpr int kBN = 256;     // output columns per tile: the MMA's N
 constexpr int kBK = 64;      // contraction per stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;   // contraction per MMA instruction (16-bit operands)
-constexpr int kStages = 4;
-constexpr int kPrologueWarps = 8;  // two threads per tile row
-constexpr int kEpilogueWarps = 4;  // one thread per tile row (tensor-memory lane)
-// warps: 0 TMA, 1 MMA, 2-9 prologue, 10-13 epilogue
-constexpr int kThreads = 32 * (2 + kPrologueWarps + kEpilogueWarps);
+constexpr int kStagesA = 3;       // h slices in shared memory
+constexpr int kStagesB = 5;       // W2 slices in shared memory
+constexpr int kStagesT = 8;       // scaled h slices in tensor memory
+constexpr int kPrologueWarps = 8; // two per lane quarter, half the K range each
+constexpr int kEpilogueWarps = 8; // two per lane quarter, half the columns each
+constexpr int kFirstPrologueWarp = 3;
+constexpr int kFirstEpilogueWarp = kFirstPrologueWarp + kPrologueWarps;
+constexpr int kThreads = 32 * (kFirstEpilogueWarp + kEpilogueWarps);
 constexpr uint32_t kABytes = kBM * kBK * 2;
 constexpr uint32_t kBBytes = kBN * kBK * 2;
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kTmemCols = kBN;  // one fp32 accumulator: a column per output column
-// operand ring, barriers and the tables of at most MOE_MAX_EXPERTS experts
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStages * kStageBytes + 256 +
-                              sizeof(int32_t) * (3 * MOE_MAX_EXPERTS + 2);
+constexpr uint32_t kAccCols = kBN;         // fp32 accumulator: a column per output column
+constexpr uint32_t kACols = kBK / 2;       // a scaled h slice: two bf16 per 32-bit column
+constexpr uint32_t kTmemCols = 512;        // accumulator + kStagesT A stages
+static_assert(kAccCols + kStagesT * kACols <= kTmemCols, "tensor memory budget");
+static_assert(8 * (2 * kStagesA + 2 * kStagesB + 2 * kStagesT + 2) + 16 <= 512, "barrier area");
+// operand rings, barriers and the tables of at most MOE_MAX_EXPERTS experts
+constexpr size_t kBarrierBytes = 512;  // 34 mbarriers and the tensor-memory address
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStagesA * kABytes + kStagesB * kBBytes +
+                              kBarrierBytes + sizeof(int32_t) * (3 * MOE_MAX_EXPERTS + 2);
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A
@@ -122,15 +132,28 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, one M=128 x N=256 x K=16 step.
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc,
-                                          uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]^T: A from tensor memory (lane = row, 32-bit
+// column j = bf16 elements 2j, 2j+1 of the row's K range).
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc,
+                                                 uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+      "setp.ne.b32 p, %3, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b_desc), "r"(accumulate), "r"(kIdesc)
       : "memory");
+}
+
+// 16 consecutive 32-bit columns of this warp's 32 tensor-memory lanes.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Arrive on `bar` once every MMA this thread issued so far has completed.
@@ -198,9 +221,8 @@ __device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles
 }
 
 // Persistent: CTA b takes tiles b, b + gridDim.x, ... in every role, so the
-// four roles walk the same tile sequence.  The stage ring runs on across
-// tiles; the two accumulators alternate, so the epilogue of one tile overlaps
-// the MMAs of the next.
+// roles walk the same sequence of (tile, K slice) jobs; each ring runs on
+// across tiles.
 __global__ void __launch_bounds__(kThreads, 1)
     w2_absorbed_kernel(const __grid_constant__ CUtensorMap tm_h,
                        const __grid_constant__ CUtensorMap tm_w2, W2Args a) {
@@ -208,18 +230,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // operand tiles start on 1024-byte shared-memory boundaries (the swizzle
   // pattern repeats every 8 rows of 128 bytes)
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sA = smem;                      // [kStages][kBM x kBK] bf16, swizzled
-  uint8_t* sB = smem + kStages * kABytes;  // [kStages][kBN x kBK] bf16, swizzled
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  uint64_t* full_a = bars;                  // h slice landed
-  uint64_t* full_b = bars + kStages;        // W2 slice landed
-  uint64_t* ready = bars + 2 * kStages;     // h slice scaled
-  uint64_t* empty = bars + 3 * kStages;     // MMAs done with the stage
-  uint64_t* acc_full = bars + 4 * kStages;  // [2] accumulator complete
-  uint64_t* acc_empty = acc_full + 2;      // [2] accumulator drained
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint8_t* sA = smem;                       // [kStagesA][kBM x kBK] bf16, swizzled
+  uint8_t* sB = smem + kStagesA * kABytes;  // [kStagesB][kBN x kBK] bf16, swizzled
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStagesB * kBBytes);
+  uint64_t* full_a = bars;                   // [kStagesA] h slice landed
+  uint64_t* free_a = full_a + kStagesA;      // [kStagesA] h slice read by the prologue
+  uint64_t* full_b = free_a + kStagesA;      // [kStagesB] W2 slice landed
+  uint64_t* empty_b = full_b + kStagesB;     // [kStagesB] MMAs done with the W2 slice
+  uint64_t* ready_t = empty_b + kStagesB;    // [kStagesT] scaled slice in tensor memory
+  uint64_t* empty_t = ready_t + kStagesT;    // [kStagesT] MMAs done with it
+  uint64_t* acc_full = empty_t + kStagesT;   // accumulator complete
+  uint64_t* acc_empty = acc_full + 1;        // accumulator drained
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
   Tables tb;
-  tb.tile_first = reinterpret_cast<int32_t*>(tmem_slot + 4);
+  tb.tile_first = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(bars) + kBarrierBytes);
   tb.off = tb.tile_first + (a.E + 1);
   tb.cnt = tb.off + (a.E + 1);
 
@@ -248,92 +272,103 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) {
       tb.tile_first[a.E] = running;
-      for (int s = 0; s < kStages; ++s) {
+      for (int s = 0; s < kStagesA; ++s) {
         mbar_init(&full_a[s], 1);
+        mbar_init(&free_a[s], kPrologueWarps);
+      }
+      for (int s = 0; s < kStagesB; ++s) {
         mbar_init(&full_b[s], 1);
-        mbar_init(&ready[s], kPrologueWarps);
-        mbar_init(&empty[s], 1);
+        mbar_init(&empty_b[s], 1);
       }
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(&acc_full[i], 1);
-        mbar_init(&acc_empty[i], kEpilogueWarps);
+      for (int s = 0; s < kStagesT; ++s) {
+        mbar_init(&ready_t[s], kPrologueWarps);
+        mbar_init(&empty_t[s], 1);
       }
+      mbar_init(acc_full, 1);
+      mbar_init(acc_empty, kEpilogueWarps);
       fence_mbar_init();
     }
   } else if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
-                 "r"(2 * kTmemCols)
+                 "r"(kTmemCols)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = *tmem_slot;     // accumulator: columns [0, 256)
+  const uint32_t tmem_a = tmem + kAccCols;  // A stages: 32 columns each
   const int total = tb.tile_first[a.E] * a.n_tiles;
+  const int my_tiles =
+      blockIdx.x < total ? (total - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x : 0;
 
   bool ok = true;
-  if (warp == 0) {
+  if (warp == 0 || warp == 2) {
+    // TMA producers: warp 0 the W2 slices, warp 2 the h slices
     if (lane == 0) {
+      const bool is_b = warp == 0;
+      const int stages = is_b ? kStagesB : kStagesA;
+      uint64_t* full = is_b ? full_b : full_a;
+      uint64_t* freed = is_b ? empty_b : free_a;
       int it = 0;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const Tile t = decode_tile(tb, a.E, a.n_tiles, tile);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1u;
-          if (it >= kStages && !wait_phase(&empty[s], ph ^ 1u)) {
+          const int s = it % stages;
+          const uint32_t ph = (it / stages) & 1u;
+          if (it >= stages && !wait_phase(&freed[s], ph ^ 1u)) {
             ok = false;
             break;
           }
-          // h and W2 complete on separate barriers: the prologue needs only h
-          mbar_arrive_expect_tx(&full_a[s], kABytes);
-          tma_load_2d(sA + s * kABytes, &tm_h, kb * kBK, t.row0, &full_a[s]);
-          mbar_arrive_expect_tx(&full_b[s], kBBytes);
-          tma_load_2d(sB + s * kBBytes, &tm_w2, kb * kBK, t.expert * a.H + t.nt * kBN, &full_b[s]);
+          if (is_b) {
+            mbar_arrive_expect_tx(&full[s], kBBytes);
+            tma_load_2d(sB + s * kBBytes, &tm_w2, kb * kBK, t.expert * a.H + t.nt * kBN, &full[s]);
+          } else {
+            mbar_arrive_expect_tx(&full[s], kABytes);
+            tma_load_2d(sA + s * kABytes, &tm_h, kb * kBK, t.row0, &full[s]);
+          }
         }
       }
-      // the last stages' copies must have landed before the CTA may exit
-      for (int j = it - kStages < 0 ? 0 : it - kStages; j < it; ++j) {
-        if (!wait_phase(&full_a[j % kStages], (j / kStages) & 1u)) ok = false;
-        if (!wait_phase(&full_b[j % kStages], (j / kStages) & 1u)) ok = false;
-      }
+      // the last copies must have landed before the CTA may exit
+      for (int j = it - stages < 0 ? 0 : it - stages; j < it; ++j)
+        if (!wait_phase(&full[j % stages], (j / stages) & 1u)) ok = false;
     }
   } else if (warp == 1) {
     if (lane == 0) {
       int it = 0, n = 0;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
-        const int acc = n & 1;
-        const uint32_t aph = (n >> 1) & 1u;
-        if (n >= 2 && !wait_phase(&acc_empty[acc], aph ^ 1u)) {
+        if (n >= 1 && !wait_phase(acc_empty, (n - 1) & 1u)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem + acc * kTmemCols;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1u;
-          if (!wait_phase(&full_b[s], ph) || !wait_phase(&ready[s], ph)) {
+          const int sb = it % kStagesB, st = it % kStagesT;
+          if (!wait_phase(&ready_t[st], (it / kStagesT) & 1u) ||
+              !wait_phase(&full_b[sb], (it / kStagesB) & 1u)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_addr(sA + s * kABytes), b0 = smem_addr(sB + s * kBBytes);
+          const uint32_t b0 = smem_addr(sB + sb * kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k)
-            umma_bf16(d, sw128_desc(a0 + k * kUmmaK * 2), sw128_desc(b0 + k * kUmmaK * 2),
-                      (kb | k) != 0);
-          umma_commit(&empty[s]);
+            umma_bf16_tmem_a(tmem, tmem_a + st * kACols + k * (kUmmaK / 2),
+                             sw128_desc(b0 + k * kUmmaK * 2), (kb | k) != 0);
+          umma_commit(&empty_b[sb]);
+          umma_commit(&empty_t[st]);
         }
-        umma_commit(&acc_full[acc]);
+        umma_commit(acc_full);
       }
     }
-  } else if (warp < 2 + kPrologueWarps) {
-    // prologue: two threads per row of each h slice, four of the row's eight
-    // 16-byte chunks each; the row's score is fetched one tile ahead
-    const int p = threadIdx.x - 64;
-    const int prow = p >> 1, half = p & 1;
+  } else if (warp < kFirstEpilogueWarp) {
+    // prologue: lane quarter q = warp % 4 (tensor memory is reachable by the
+    // warps of that quarter only), K half kh; thread = row 32 q + lane
+    const int q = warp & 3;
+    const int kh = (warp - kFirstPrologueWarp) >> 2;
+    const int prow = q * 32 + lane;
+    const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
     auto score_of = [&](int tile) {
       if (tile >= total) return 0.0f;
       const Tile t = decode_tile(tb, a.E, a.n_tiles, tile);
@@ -346,47 +381,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float score = next_score;
       next_score = score_of(tile + gridDim.x);
       for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1u;
+        const int sa = it % kStagesA, st = it % kStagesT;
         // each lane waits itself (acquiring the copy); the warp leaves together
-        const bool got = wait_phase(&full_a[s], ph);
+        bool got = wait_phase(&full_a[sa], (it / kStagesA) & 1u);
+        if (got && it >= kStagesT) got = wait_phase(&empty_t[st], ((it / kStagesT) & 1u) ^ 1u);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
-        uint8_t* line = sA + s * kABytes + prow * 128;
+        tc_fence_after();
+        // 16-byte chunk c of row r sits at r * 128 + ((c ^ (r % 8)) * 16); this
+        // warp's K half is chunks 4 kh .. 4 kh + 3 (eight rows of a phase hit
+        // eight distinct banks)
+        const uint8_t* line = sA + sa * kABytes + prow * 128;
+        uint32_t packed[16];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          // the swizzle permutes a row's chunks within its 128 bytes, and the
-          // score is per row, so the thread takes physical chunks; rotating
-          // them by row keeps the eight threads of a shared-memory phase (four
-          // rows, two halves) on distinct banks
-          uint4* q = reinterpret_cast<uint4*>(line + (half * 4 + ((c + prow) & 3)) * 16);
-          uint4 v = *q;
-          uint32_t* u = reinterpret_cast<uint32_t*>(&v);
+          const int chunk = kh * 4 + c;
+          const uint4 v = *reinterpret_cast<const uint4*>(line + ((chunk ^ (prow & 7)) << 4));
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const float lo = __fmul_rn(__uint_as_float(u[j] << 16), score);
             const float hi = __fmul_rn(__uint_as_float(u[j] & 0xffff0000u), score);
-            u[j] = pack_bf16x2(lo, hi);
+            packed[c * 4 + j] = pack_bf16x2(lo, hi);
           }
-          *q = v;
         }
-        fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ready[s]);
+        if (lane == 0) mbar_arrive(&free_a[sa]);  // the h slice may be refilled
+        tmem_st16(tmem_a + lane_bits + st * kACols + kh * 16, packed);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ready_t[st]);
       }
     }
   } else {
-    // epilogue: the lanes of tensor-memory quarter (warp % 4) are tile rows
-    // 32 * (warp % 4) + lane
+    // epilogue: lane quarter q = warp % 4 (tile rows 32 q + lane), column half
+    // ch of the accumulator
     const int q = warp & 3;
+    const int ch = (warp - kFirstEpilogueWarp) >> 2;
     int n = 0;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
       const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile);
-      const int acc = n & 1;
-      const uint32_t aph = (n >> 1) & 1u;
-      if (!__all_sync(0xffffffffu, wait_phase(&acc_full[acc], aph))) {
+      if (!__all_sync(0xffffffffu, wait_phase(acc_full, n & 1u))) {
         ok = false;
         break;
       }
@@ -394,10 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = ti.row0 + q * 32 + lane;
       const bool real = row < ti.real_end;
       const bool pad = !real && row < ti.seg_end;
-      __nv_bfloat16* dst = a.y + static_cast<size_t>(row) * a.H + ti.nt * kBN;
-      const uint32_t taddr = tmem + acc * kTmemCols + (static_cast<uint32_t>(q * 32) << 16);
+      __nv_bfloat16* dst = a.y + static_cast<size_t>(row) * a.H + ti.nt * kBN + ch * (kBN / 2);
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ch * (kBN / 2);
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = 0; c < kBN / 2 / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(taddr + c * 32, v);
         if (real || pad) {
@@ -412,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();  // the loads above precede the MMAs that reuse the columns
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (lane == 0) mbar_arrive(acc_empty);
     }
   }
   if (!ok) raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
@@ -421,17 +458,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     // every MMA must be complete before the columns are released: wait for
-    // the last commit of each accumulator (on the normal path the epilogue
-    // already has, and these return at once)
-    if (lane == 0) {
-      int n = 0;
-      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) ++n;
-      for (int j = n - 2 < 0 ? 0 : n - 2; j < n; ++j)
-        if (!wait_phase(&acc_full[j & 1], (j >> 1) & 1u)) raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
-    }
+    // the last tile's accumulator commit (on the normal path the epilogue
+    // already has, and this returns at once)
+    if (lane == 0 && my_tiles > 0 && !wait_phase(acc_full, (my_tiles - 1) & 1u))
+      raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
     __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(2 * kTmemCols)
+                 "r"(kTmemCols)
                  : "memory");
   }
 }
