@@ -26,8 +26,9 @@
 //   warp 1      tensor memory (one 256-column accumulator + the A stages) and
 //               one thread issuing the MMAs (four K=16 steps per slice) and the
 //               commits that free the stages and hand over the accumulator;
-//   warps 11-18 epilogue: accumulator -> registers -> bf16 rows in HBM (two
-//               warps per lane quarter, half the columns each).
+//   warps 11-18 epilogue: accumulator -> registers (two warps per lane
+//               quarter, half the columns each), accumulator handed back, then
+//               bf16 rows to HBM while the next tile's MMAs run.
 // Every wait is bounded; a wait that gives up raises MOE_DEVERR_TIMEOUT and
 // the CTA winds down (copies in flight are waited for, tensor memory freed).
 #include <cuda.h>
@@ -144,16 +145,18 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_
       : "memory");
 }
 
-// 16 consecutive 32-bit columns of this warp's 32 tensor-memory lanes.
+// 16 consecutive 32-bit columns of this warp's 32 tensor-memory lanes.  The
+// store reads its source registers asynchronously, so the store and its wait
+// are one asm statement: the registers stay reserved until the wait returns.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
       "r"(v[15])
       : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Arrive on `bar` once every MMA this thread issued so far has completed.
@@ -164,19 +167,23 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// 32 consecutive fp32 columns of this warp's 32 tensor-memory lanes.
+// 32 consecutive fp32 columns of this warp's 32 tensor-memory lanes.  The
+// load and its wait are one asm statement: the load is asynchronous, and the
+// registers are defined only once the wait has returned, so no use of them
+// may be scheduled in between.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
         "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
         "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
         "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
         "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      : "r"(taddr)
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -407,12 +414,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             packed[c * 4 + j] = pack_bf16x2(lo, hi);
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&free_a[sa]);  // the h slice may be refilled
         tmem_st16(tmem_a + lane_bits + st * kACols + kh * 16, packed);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ready_t[st]);
+        if (lane == 0) {
+          mbar_arrive(&free_a[sa]);  // the h slice may be refilled
+          mbar_arrive(&ready_t[st]);
+        }
       }
     }
   } else {
@@ -433,23 +441,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool pad = !real && row < ti.seg_end;
       __nv_bfloat16* dst = a.y + static_cast<size_t>(row) * a.H + ti.nt * kBN + ch * (kBN / 2);
       const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ch * (kBN / 2);
-#pragma unroll 1
+      // the row's 128 columns as bf16 pairs in registers, so the accumulator
+      // is handed back to the MMAs before the (slower) stores to HBM
+      uint32_t packed[kBN / 4];
+#pragma unroll
       for (int c = 0; c < kBN / 2 / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(taddr + c * 32, v);
-        if (real || pad) {
-          Vec16 o[4];
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            o[j >> 2].u[j & 3] =
-                real ? pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])) : 0u;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) st_vec(dst + c * 32 + j * 8, o[j]);
-        }
+        for (int j = 0; j < 16; ++j)
+          packed[c * 16 + j] =
+              real ? pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])) : 0u;
       }
       tc_fence_before();  // the loads above precede the MMAs that reuse the columns
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
+      if (real || pad) {
+#pragma unroll
+        for (int j = 0; j < kBN / 2 / 8; ++j) {
+          Vec16 o;
+          o.u[0] = packed[4 * j];
+          o.u[1] = packed[4 * j + 1];
+          o.u[2] = packed[4 * j + 2];
+          o.u[3] = packed[4 * j + 3];
+          st_vec(dst + j * 8, o);
+        }
+      }
     }
   }
   if (!ok) raise_flag(a.flags, MOE_DEVERR_TIMEOUT);

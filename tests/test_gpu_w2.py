@@ -113,6 +113,21 @@ def test_w2_absorbed_all_rows(case):
     assert alt_frac > 5 * max(frac, 0.002), (alt_frac, frac)
 
 
+def test_w2_absorbed_repeated_runs_identical():
+    """The pipeline hands shared-memory stages, tensor-memory stages and the
+    accumulator between warps; a hand-over race shows up as run-to-run
+    differences in whole rows.  Eight runs must be bitwise identical and each
+    within the bound."""
+    wl, r, L, recv_w, h, w2 = problem(synth.WORKLOADS[4].with_tokens(700), I=256, H=512)
+    n = int(L.off_e[-1])
+    first = run_gpu(r, h, recv_w, w2)
+    for _ in range(7):
+        assert np.array_equal(run_gpu(r, h, recv_w, w2)[:n], first[:n])
+    yb, y64 = oracle.w2_absorbed(h, recv_w, w2, L.off_e, L.cnt_e, rows=np.arange(n))
+    seg_of = np.repeat(np.arange(wl.E), np.diff(L.off_e))
+    check_rows(first[:n], y64, yb, abs_terms(h[:n], recv_w[:n], w2, seg_of), h.shape[1], "repeat")
+
+
 def test_w2_absorbed_full_size_sampled_rows():
     """The whole Qwen3-235B-shaped problem (T=32768, K=8, E=128, I=1536,
     H=4096), checked on sampled rows: the first, a middle and the last row of
