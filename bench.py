@@ -68,6 +68,77 @@ def read_peaks():
     return 6800.0, "fallback"
 
 
+def read_bf16_peak():
+    """Dense bf16 tensor peak in TFLOP/s: the burst figure (the W2 GEMM is
+    timed on its own, not inside a long step)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured (burst)"
+    return 1900.0, "fallback"
+
+
+def w2_absorbed_extra(device, stream, reps, tokens=None):
+    """Router scores absorbed into the W2 input, fused into the W2 grouped GEMM
+    (tensor cores), on the Qwen3-235B-shaped layer (T=32768, K=8, E=128,
+    I=1536, H=4096), against the unfused path: scale_rows, then cuBLAS per
+    expert.  Inputs: N(0,1) logits and h, W2 ~ N(0, 1/I), seeded on device."""
+    import torch
+    import combine_moe_route_05_gb300 as moe
+    wl = synth.WORKLOADS[4]
+    T = tokens or wl.T
+    E, K, R, I, H = wl.E, wl.K, wl.R, wl.I, 4096
+    g = torch.Generator(device=device).manual_seed(wl.seed)
+    r = moe.MoeRouter(E, K, R, T)
+    idx, w = r.route(torch.randn(T, E, device=device, generator=g))
+    r.layout(idx)
+    rows = r.h.recv_rows
+    hrows = torch.randn(rows, I, device=device, generator=g).to(torch.bfloat16)
+    w2 = (torch.randn(E, H, I, device=device, generator=g) * (1.0 / I ** 0.5)).to(torch.bfloat16)
+    _, recv_w, _ = r.dispatch(torch.zeros(T, 8, dtype=torch.bfloat16, device=device), w)
+    y = torch.empty(rows, H, dtype=torch.bfloat16, device=device)
+    hs = torch.empty_like(hrows)
+    y_ref = torch.empty_like(y)
+    cnt = moe.layout_tensors(r.h)["cnt_e"].tolist()
+
+    def unfused():
+        moe.moe_scale_rows(r.h, hrows, recv_w, hs)
+        o = 0
+        for e in range(E):
+            if cnt[e]:
+                torch.matmul(hs[o:o + cnt[e]], w2[e].t(), out=y_ref[o:o + cnt[e]])
+            o += cnt[e]
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        for _ in range(reps):
+            fn()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        return a_.elapsed_time(b_) / reps
+
+    t_fused = timed(lambda: moe.moe_w2_absorbed(r.h, hrows, recv_w, w2, y))
+    t_unfused = timed(unfused)
+    assert moe.moe_read_device_status(r.h) == 0
+    same = bool(torch.equal(y, y_ref))
+    flop = 2.0 * T * K * H * I
+    peak, src = read_bf16_peak()
+    achieved = flop / (t_fused / 1e3) / 1e12
+    return {
+        "workload": "qwen3_235b_absorbed T=%d K=%d E=%d I=%d H=%d (W2 [E,H,I] bf16)" % (T, K, E, I, H),
+        "fused_ms": t_fused, "unfused_ms": t_unfused, "scale_rows_plus_cublas_per_expert_ms": t_unfused,
+        "bitwise_equal_to_unfused": same,
+        "roofline": {"kernel": "w2_absorbed", "bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "algorithmic_flops": flop, "peak_source": src},
+    }
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -422,6 +493,8 @@ def run_gpu(args, wl):
                 "combine_reduce_gbs": (S + T) * row / (t_cr / 1e3) / 1e9},
         }
         assert moe.moe_read_device_status(h) == 0
+        extras["w2_absorbed"] = w2_absorbed_extra(device, stream, max(5, args.steps // 5),
+                                                  tokens=args.tokens or None)
 
     if rank != 0:
         return
