@@ -11,14 +11,17 @@
 // with W2 stored [E][H][I].  The scaling is the GEMM's prologue: the scaled
 // rows never reach HBM.  A pad row of a padded layout gets y = 0.
 //
-// A persistent CTA per SM walks 128 x 256 output tiles of the experts (a tile
-// never straddles two experts: each expert's segment is cut into 128-row
-// tiles, the last one ragged).  The scaled h slice is the MMA's A operand in
-// TENSOR memory, so shared memory carries only the TMA landings, the
-// prologue's read of h and the tensor cores' read of W2.  Warp roles:
+// Persistent clusters of two CTAs walk pairs of 128 x 256 output tiles (a
+// tile never straddles two experts: each expert's segment is cut into 128-row
+// tiles, the last one ragged; the two CTAs of a cluster take adjacent m-tiles
+// of one expert and the same W2 columns).  The scaled h slice is the MMA's A
+// operand in TENSOR memory, so shared memory carries only the TMA landings,
+// the prologue's read of h and the tensor cores' read of W2.  Warp roles:
 //   warp 2      TMA: h slices [128 x 64] into a 3-stage ring (128-byte
-//               swizzle), freed as soon as the prologue has read them;
-//   warp 0      TMA: W2 slices [256 x 64] into a 5-stage ring;
+//               swizzle), freed once the prologue has consumed them;
+//   warp 0      TMA: this CTA's half [128 x 64] of each W2 slice, multicast
+//               into both CTAs of the cluster, 5-stage ring (a stage is free
+//               when the MMAs of both CTAs are done with it);
 //   warps 3-10  prologue: read an h slice (one row per thread, half of its K
 //               range per warp), scale it by the row's score (fp32 product,
 //               bf16 round-to-nearest-even) and store it into one of eight
@@ -133,6 +136,28 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// The same tile into the same shared-memory offset of every CTA in `mask`,
+// completing on the barrier at the same offset in each of them.
+__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, int x, int y,
+                                                      uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of both CTAs of the pair.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]^T: A from tensor memory (lane = row, 32-bit
 // column j = bf16 elements 2j, 2j+1 of the row's K range).
 __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc,
@@ -167,6 +192,15 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
+// The same, on the barrier at the same offset in every CTA of `mask`.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(smem_addr(bar)),
+      "h"(mask)
+      : "memory");
+}
+
 // 32 consecutive fp32 columns of this warp's 32 tensor-memory lanes.  The
 // load and its wait are one asm statement: the load is asynchronous, and the
 // registers are defined only once the wait has returned, so no use of them
@@ -192,7 +226,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Shared-memory tables of one CTA: the layout's expert segments and, per
-// expert, the index of its first 128-row m-tile (tile_first[E] = all m-tiles).
+// expert, the index of its first pair of 128-row m-tiles (tile_first[E] = all
+// pairs).
 struct Tables {
   int32_t* tile_first;  // [E + 1]
   int32_t* off;         // [E + 1]
@@ -205,10 +240,13 @@ struct Tile {
   int real_end;  // end of the expert's real rows
 };
 
-// Tile `tile` (n-tile fastest) -> expert and rows: the last expert whose first
-// m-tile is <= the tile's m-tile (an empty expert shares its first m-tile with
-// the next expert and is never the last such one).
-__device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles, int tile) {
+// Pair tile `tile` (n-tile fastest) -> expert and this CTA's rows: the last
+// expert whose first pair is <= the tile's pair (an empty expert shares its
+// first pair with the next expert and is never the last such one).  CTA `rank`
+// of the pair takes m-tile 2 * pair + rank of the expert; past the expert's
+// last m-tile it has no rows (row0 >= seg_end) but still shares W2.
+__device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles, int tile,
+                                            int rank) {
   const int mt = tile / n_tiles;
   int lo = 0, hi = E - 1;
   while (lo < hi) {
@@ -221,15 +259,18 @@ __device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles
   Tile t;
   t.expert = lo;
   t.nt = tile - mt * n_tiles;
-  t.row0 = tb.off[lo] + (mt - tb.tile_first[lo]) * kBM;
+  t.row0 = tb.off[lo] + (2 * (mt - tb.tile_first[lo]) + rank) * kBM;
   t.seg_end = tb.off[lo + 1];
   t.real_end = tb.off[lo] + tb.cnt[lo];
   return t;
 }
 
-// Persistent: CTA b takes tiles b, b + gridDim.x, ... in every role, so the
-// roles walk the same sequence of (tile, K slice) jobs; each ring runs on
-// across tiles.
+// Persistent clusters of two CTAs: pair p takes pair tiles p, p + npairs, ...
+// in every role of both CTAs, so all roles walk the same sequence of (tile,
+// K slice) jobs; each ring runs on across tiles.  The two CTAs compute
+// adjacent 128-row m-tiles of one expert against the same W2 slices: each
+// loads half of every W2 slice and multicasts it to both, so W2 crosses the L2
+// once per pair.
 __global__ void __launch_bounds__(kThreads, 1)
     w2_absorbed_kernel(const __grid_constant__ CUtensorMap tm_h,
                        const __grid_constant__ CUtensorMap tm_w2, W2Args a) {
@@ -256,6 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (a.I + kBK - 1) / kBK;
+  const int rank = static_cast<int>(cluster_rank());
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   for (int e = threadIdx.x; e <= a.E; e += kThreads) {
     tb.off[e] = a.off_e[e];
@@ -267,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int running = 0;
     for (int base = 0; base < a.E; base += 32) {
       const int e = base + lane;
-      const int tiles = e < a.E ? (tb.off[e + 1] - tb.off[e] + kBM - 1) / kBM : 0;
+      const int tiles = e < a.E ? ((tb.off[e + 1] - tb.off[e] + kBM - 1) / kBM + 1) / 2 : 0;
       int incl = tiles;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -285,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int s = 0; s < kStagesB; ++s) {
         mbar_init(&full_b[s], 1);
-        mbar_init(&empty_b[s], 1);
+        mbar_init(&empty_b[s], 2);  // both CTAs' MMAs are done with the W2 slice
       }
       for (int s = 0; s < kStagesT; ++s) {
         mbar_init(&ready_t[s], kPrologueWarps);
@@ -302,13 +345,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                  : "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  // the peer's barriers must be initialised before its multicast copies and
+  // commits can reach them
+  cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;     // accumulator: columns [0, 256)
   const uint32_t tmem_a = tmem + kAccCols;  // A stages: 32 columns each
   const int total = tb.tile_first[a.E] * a.n_tiles;
-  const int my_tiles =
-      blockIdx.x < total ? (total - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x : 0;
+  const int my_tiles = pair < total ? (total - pair + npairs - 1) / npairs : 0;
 
   bool ok = true;
   if (warp == 0 || warp == 2) {
@@ -319,8 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t* full = is_b ? full_b : full_a;
       uint64_t* freed = is_b ? empty_b : free_a;
       int it = 0;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode_tile(tb, a.E, a.n_tiles, tile);
+      for (int tile = pair; tile < total && ok; tile += npairs) {
+        const Tile t = decode_tile(tb, a.E, a.n_tiles, tile, rank);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % stages;
           const uint32_t ph = (it / stages) & 1u;
@@ -329,22 +373,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (is_b) {
+            // this CTA's half of the W2 slice, into both CTAs; the slice is
+            // complete when both halves have landed
             mbar_arrive_expect_tx(&full[s], kBBytes);
-            tma_load_2d(sB + s * kBBytes, &tm_w2, kb * kBK, t.expert * a.H + t.nt * kBN, &full[s]);
+            tma_load_2d_multicast(sB + s * kBBytes + rank * (kBBytes / 2), &tm_w2, kb * kBK,
+                                  t.expert * a.H + t.nt * kBN + rank * (kBN / 2), &full[s], 0x3);
           } else {
             mbar_arrive_expect_tx(&full[s], kABytes);
             tma_load_2d(sA + s * kABytes, &tm_h, kb * kBK, t.row0, &full[s]);
           }
         }
       }
-      // the last copies must have landed before the CTA may exit
-      for (int j = it - stages < 0 ? 0 : it - stages; j < it; ++j)
+      // the last copies must have landed before the CTA may exit, and the
+      // peer's last commits on this CTA's W2 barriers must have arrived
+      for (int j = it - stages < 0 ? 0 : it - stages; j < it; ++j) {
         if (!wait_phase(&full[j % stages], (j / stages) & 1u)) ok = false;
+        if (is_b && !wait_phase(&freed[j % stages], (j / stages) & 1u)) ok = false;
+      }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       int it = 0, n = 0;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+      for (int tile = pair; tile < total && ok; tile += npairs, ++n) {
         if (n >= 1 && !wait_phase(acc_empty, (n - 1) & 1u)) {
           ok = false;
           break;
@@ -363,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kBK / kUmmaK; ++k)
             umma_bf16_tmem_a(tmem, tmem_a + st * kACols + k * (kUmmaK / 2),
                              sw128_desc(b0 + k * kUmmaK * 2), (kb | k) != 0);
-          umma_commit(&empty_b[sb]);
+          umma_commit_multicast(&empty_b[sb], 0x3);  // frees the slice in both CTAs
           umma_commit(&empty_t[st]);
         }
         umma_commit(acc_full);
@@ -378,15 +428,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
     auto score_of = [&](int tile) {
       if (tile >= total) return 0.0f;
-      const Tile t = decode_tile(tb, a.E, a.n_tiles, tile);
+      const Tile t = decode_tile(tb, a.E, a.n_tiles, tile, rank);
       const int row = t.row0 + prow;
       return row < t.real_end ? __ldg(a.recv_w + row) : 0.0f;
     };
-    float next_score = score_of(blockIdx.x);
+    float next_score = score_of(pair);
     int it = 0;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    for (int tile = pair; tile < total && ok; tile += npairs) {
       const float score = next_score;
-      next_score = score_of(tile + gridDim.x);
+      next_score = score_of(tile + npairs);
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int sa = it % kStagesA, st = it % kStagesT;
         // each lane waits itself (acquiring the copy); the warp leaves together
@@ -429,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int ch = (warp - kFirstEpilogueWarp) >> 2;
     int n = 0;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
-      const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile);
+    for (int tile = pair; tile < total && ok; tile += npairs, ++n) {
+      const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile, rank);
       if (!__all_sync(0xffffffffu, wait_phase(acc_full, n & 1u))) {
         ok = false;
         break;
@@ -471,7 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (!ok) raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
   tc_fence_before();
-  __syncthreads();
+  // neither CTA leaves while the other may still reach its shared memory
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     // every MMA must be complete before the columns are released: wait for
@@ -536,7 +587,7 @@ cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, co
   if (rows_cap <= 0) return cudaSuccess;
   CUtensorMap tm_h, tm_w2;
   if (!encode_rows(&tm_h, hrows, static_cast<uint64_t>(rows_cap), I, kBM) ||
-      !encode_rows(&tm_w2, w2, static_cast<uint64_t>(E) * H, I, kBN))
+      !encode_rows(&tm_w2, w2, static_cast<uint64_t>(E) * H, I, kBN / 2))
     return cudaErrorInvalidValue;
   W2Args a;
   a.recv_w = recv_w;
@@ -548,16 +599,31 @@ cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, co
   a.I = I;
   a.H = H;
   a.n_tiles = H / kBN;
-  // sum over experts of ceil(segment / kBM) <= (rows + E * (kBM - 1)) / kBM
-  const long long m_tiles = (rows_cap + static_cast<long long>(E) * (kBM - 1)) / kBM;
-  const long long tiles = m_tiles * a.n_tiles;
   if (static_cast<long long>(E) * H > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-  // one CTA per SM (the operand ring fills its shared memory), never more
-  // CTAs than tiles could exist
-  const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
-  w2_absorbed_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w2, a);
-  return cudaGetLastError();
+  // pairs of CTAs in clusters of two, as many as can be resident at once
+  static int max_pairs[64] = {0};
+  const int dev = h->device >= 0 && h->device < 64 ? h->device : 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_pairs[dev] == 0) {
+    cfg.gridDim = dim3(2 * (h->num_sms / 2), 1, 1);
+    int n = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, w2_absorbed_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_pairs[dev] = n;
+  }
+  cfg.gridDim = dim3(2 * max_pairs[dev], 1, 1);
+  return cudaLaunchKernelEx(&cfg, w2_absorbed_kernel, tm_h, tm_w2, a);
 }
 
 }  // namespace moe
