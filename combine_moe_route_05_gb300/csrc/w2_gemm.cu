@@ -11,24 +11,22 @@
 // with W2 stored [E][H][I].  The scaling is the GEMM's prologue: the scaled
 // rows never reach HBM.  A pad row of a padded layout gets y = 0.
 //
-// Persistent clusters of two CTAs walk pairs of 128 x 256 output tiles (a
-// tile never straddles two experts: each expert's segment is cut into 128-row
-// tiles, the last one ragged; the two CTAs of a cluster take adjacent m-tiles
-// of one expert and the same W2 columns).  The scaled h slice is the MMA's A
-// operand in TENSOR memory, so shared memory carries only the TMA landings,
-// the prologue's read of h and the tensor cores' read of W2.  Warp roles:
+// A persistent CTA per SM walks 128 x 256 output tiles of the experts (a tile
+// never straddles two experts: each expert's segment is cut into 128-row
+// tiles, the last one ragged).  The scaled h slice is the MMA's A operand in
+// TENSOR memory, so shared memory carries only the TMA landings, the
+// prologue's read of h and the tensor cores' read of W2.  Warp roles:
 //   warp 2      TMA: h slices [128 x 64] into a 3-stage ring (128-byte
-//               swizzle), freed once the prologue has consumed them;
-//   warp 0      TMA: this CTA's half [128 x 64] of each W2 slice, multicast
-//               into both CTAs of the cluster, 5-stage ring (a stage is free
-//               when the MMAs of both CTAs are done with it);
+//               swizzle), freed as soon as the prologue has read them;
+//   warp 0      TMA: W2 slices [256 x 64] into a 5-stage ring;
 //   warps 3-10  prologue: read an h slice (one row per thread, half of its K
 //               range per warp), scale it by the row's score (fp32 product,
-//               bf16 round-to-nearest-even) and store it into one of eight
-//               32-column A stages in tensor memory;
-//   warp 1      tensor memory (one 256-column accumulator + the A stages) and
-//               one thread issuing the MMAs (four K=16 steps per slice) and the
-//               commits that free the stages and hand over the accumulator;
+//               bf16 round-to-nearest-even) and store it into the 32-column A
+//               stage in tensor memory that pairs with the W2 stage of the
+//               same index (one barrier: both operands in place);
+//   warp 1      tensor memory (one 256-column accumulator + five A stages)
+//               and one thread issuing the MMAs (four K=16 steps per slice)
+//               and one commit per slice, freeing both operand stages;
 //   warps 11-18 epilogue: accumulator -> registers (two warps per lane
 //               quarter, half the columns each), accumulator handed back, then
 //               bf16 rows to HBM while the next tile's MMAs run.
@@ -47,8 +45,10 @@ constexpr int kBN = 256;     // output columns per tile: the MMA's N
 constexpr int kBK = 64;      // contraction per stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;   // contraction per MMA instruction (16-bit operands)
 constexpr int kStagesA = 3;       // h slices in shared memory
-constexpr int kStagesB = 5;       // W2 slices in shared memory
-constexpr int kStagesT = 8;       // scaled h slices in tensor memory
+// W2 slices in shared memory and scaled h slices in tensor memory share one
+// ring index, so one barrier says "both operands of slice j are in place" and
+// one commit frees both
+constexpr int kStages = 5;
 constexpr int kPrologueWarps = 8; // two per lane quarter, half the K range each
 constexpr int kEpilogueWarps = 8; // two per lane quarter, half the columns each
 constexpr int kFirstPrologueWarp = 3;
@@ -58,12 +58,12 @@ constexpr uint32_t kABytes = kBM * kBK * 2;
 constexpr uint32_t kBBytes = kBN * kBK * 2;
 constexpr uint32_t kAccCols = kBN;         // fp32 accumulator: a column per output column
 constexpr uint32_t kACols = kBK / 2;       // a scaled h slice: two bf16 per 32-bit column
-constexpr uint32_t kTmemCols = 512;        // accumulator + kStagesT A stages
-static_assert(kAccCols + kStagesT * kACols <= kTmemCols, "tensor memory budget");
-static_assert(8 * (2 * kStagesA + 2 * kStagesB + 2 * kStagesT + 2) + 16 <= 512, "barrier area");
+constexpr uint32_t kTmemCols = 512;        // accumulator + kStages A stages (power of 2)
+static_assert(kAccCols + kStages * kACols <= kTmemCols, "tensor memory budget");
+static_assert(8 * (2 * kStagesA + 2 * kStages + 2) + 16 <= 512, "barrier area");
 // operand rings, barriers and the tables of at most MOE_MAX_EXPERTS experts
 constexpr size_t kBarrierBytes = 512;  // 34 mbarriers and the tensor-memory address
-constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStagesA * kABytes + kStagesB * kBBytes +
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStagesA * kABytes + kStages * kBBytes +
                               kBarrierBytes + sizeof(int32_t) * (3 * MOE_MAX_EXPERTS + 2);
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 
@@ -136,28 +136,6 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// The same tile into the same shared-memory offset of every CTA in `mask`,
-// completing on the barrier at the same offset in each of them.
-__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, int x, int y,
-                                                      uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// All threads of both CTAs of the pair.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
 // D[tmem] (+)= A[tmem] * B[smem]^T: A from tensor memory (lane = row, 32-bit
 // column j = bf16 elements 2j, 2j+1 of the row's K range).
 __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc,
@@ -192,30 +170,18 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
-// The same, on the barrier at the same offset in every CTA of `mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(smem_addr(bar)),
-      "h"(mask)
-      : "memory");
-}
-
-// 32 consecutive fp32 columns of this warp's 32 tensor-memory lanes.  The
+// 16 consecutive fp32 columns of this warp's 32 tensor-memory lanes.  The
 // load and its wait are one asm statement: the load is asynchronous, and the
 // registers are defined only once the wait has returned, so no use of them
 // may be scheduled in between.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
       "tcgen05.wait::ld.sync.aligned;"
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
         "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
-        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
-        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        "=r"(v[14]), "=r"(v[15])
       : "r"(taddr)
       : "memory");
 }
@@ -226,8 +192,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Shared-memory tables of one CTA: the layout's expert segments and, per
-// expert, the index of its first pair of 128-row m-tiles (tile_first[E] = all
-// pairs).
+// expert, the index of its first 128-row m-tile (tile_first[E] = all m-tiles).
 struct Tables {
   int32_t* tile_first;  // [E + 1]
   int32_t* off;         // [E + 1]
@@ -240,13 +205,10 @@ struct Tile {
   int real_end;  // end of the expert's real rows
 };
 
-// Pair tile `tile` (n-tile fastest) -> expert and this CTA's rows: the last
-// expert whose first pair is <= the tile's pair (an empty expert shares its
-// first pair with the next expert and is never the last such one).  CTA `rank`
-// of the pair takes m-tile 2 * pair + rank of the expert; past the expert's
-// last m-tile it has no rows (row0 >= seg_end) but still shares W2.
-__device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles, int tile,
-                                            int rank) {
+// Tile `tile` (n-tile fastest) -> expert and rows: the last expert whose first
+// m-tile is <= the tile's m-tile (an empty expert shares its first m-tile with
+// the next expert and is never the last such one).
+__device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles, int tile) {
   const int mt = tile / n_tiles;
   int lo = 0, hi = E - 1;
   while (lo < hi) {
@@ -259,18 +221,15 @@ __device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles
   Tile t;
   t.expert = lo;
   t.nt = tile - mt * n_tiles;
-  t.row0 = tb.off[lo] + (2 * (mt - tb.tile_first[lo]) + rank) * kBM;
+  t.row0 = tb.off[lo] + (mt - tb.tile_first[lo]) * kBM;
   t.seg_end = tb.off[lo + 1];
   t.real_end = tb.off[lo] + tb.cnt[lo];
   return t;
 }
 
-// Persistent clusters of two CTAs: pair p takes pair tiles p, p + npairs, ...
-// in every role of both CTAs, so all roles walk the same sequence of (tile,
-// K slice) jobs; each ring runs on across tiles.  The two CTAs compute
-// adjacent 128-row m-tiles of one expert against the same W2 slices: each
-// loads half of every W2 slice and multicasts it to both, so W2 crosses the L2
-// once per pair.
+// Persistent: CTA b takes tiles b, b + gridDim.x, ... in every role, so the
+// roles walk the same sequence of (tile, K slice) jobs; each ring runs on
+// across tiles.
 __global__ void __launch_bounds__(kThreads, 1)
     w2_absorbed_kernel(const __grid_constant__ CUtensorMap tm_h,
                        const __grid_constant__ CUtensorMap tm_w2, W2Args a) {
@@ -279,15 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // pattern repeats every 8 rows of 128 bytes)
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;                       // [kStagesA][kBM x kBK] bf16, swizzled
-  uint8_t* sB = smem + kStagesA * kABytes;  // [kStagesB][kBN x kBK] bf16, swizzled
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStagesB * kBBytes);
+  uint8_t* sB = smem + kStagesA * kABytes;  // [kStages][kBN x kBK] bf16, swizzled
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
   uint64_t* full_a = bars;                   // [kStagesA] h slice landed
   uint64_t* free_a = full_a + kStagesA;      // [kStagesA] h slice read by the prologue
-  uint64_t* full_b = free_a + kStagesA;      // [kStagesB] W2 slice landed
-  uint64_t* empty_b = full_b + kStagesB;     // [kStagesB] MMAs done with the W2 slice
-  uint64_t* ready_t = empty_b + kStagesB;    // [kStagesT] scaled slice in tensor memory
-  uint64_t* empty_t = ready_t + kStagesT;    // [kStagesT] MMAs done with it
-  uint64_t* acc_full = empty_t + kStagesT;   // accumulator complete
+  uint64_t* full = free_a + kStagesA;       // [kStages] W2 slice landed, scaled h slice stored
+  uint64_t* empty = full + kStages;         // [kStages] MMAs done with both
+  uint64_t* acc_full = empty + kStages;     // accumulator complete
   uint64_t* acc_empty = acc_full + 1;        // accumulator drained
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
   Tables tb;
@@ -297,8 +254,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (a.I + kBK - 1) / kBK;
-  const int rank = static_cast<int>(cluster_rank());
-  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   for (int e = threadIdx.x; e <= a.E; e += kThreads) {
     tb.off[e] = a.off_e[e];
@@ -310,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int running = 0;
     for (int base = 0; base < a.E; base += 32) {
       const int e = base + lane;
-      const int tiles = e < a.E ? ((tb.off[e + 1] - tb.off[e] + kBM - 1) / kBM + 1) / 2 : 0;
+      const int tiles = e < a.E ? (tb.off[e + 1] - tb.off[e] + kBM - 1) / kBM : 0;
       int incl = tiles;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -326,13 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&full_a[s], 1);
         mbar_init(&free_a[s], kPrologueWarps);
       }
-      for (int s = 0; s < kStagesB; ++s) {
-        mbar_init(&full_b[s], 1);
-        mbar_init(&empty_b[s], 2);  // both CTAs' MMAs are done with the W2 slice
-      }
-      for (int s = 0; s < kStagesT; ++s) {
-        mbar_init(&ready_t[s], kPrologueWarps);
-        mbar_init(&empty_t[s], 1);
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(&full[s], 1 + kPrologueWarps);  // W2 producer + prologue warps
+        mbar_init(&empty[s], 1);
       }
       mbar_init(acc_full, 1);
       mbar_init(acc_empty, kEpilogueWarps);
@@ -345,26 +296,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                  : "memory");
   }
   tc_fence_before();
-  // the peer's barriers must be initialised before its multicast copies and
-  // commits can reach them
-  cluster_sync();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;     // accumulator: columns [0, 256)
   const uint32_t tmem_a = tmem + kAccCols;  // A stages: 32 columns each
   const int total = tb.tile_first[a.E] * a.n_tiles;
-  const int my_tiles = pair < total ? (total - pair + npairs - 1) / npairs : 0;
+  const int my_tiles =
+      blockIdx.x < total ? (total - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x : 0;
 
   bool ok = true;
   if (warp == 0 || warp == 2) {
     // TMA producers: warp 0 the W2 slices, warp 2 the h slices
     if (lane == 0) {
       const bool is_b = warp == 0;
-      const int stages = is_b ? kStagesB : kStagesA;
-      uint64_t* full = is_b ? full_b : full_a;
-      uint64_t* freed = is_b ? empty_b : free_a;
+      const int stages = is_b ? kStages : kStagesA;
+      uint64_t* landed = is_b ? full : full_a;
+      uint64_t* freed = is_b ? empty : free_a;
       int it = 0;
-      for (int tile = pair; tile < total && ok; tile += npairs) {
-        const Tile t = decode_tile(tb, a.E, a.n_tiles, tile, rank);
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode_tile(tb, a.E, a.n_tiles, tile);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % stages;
           const uint32_t ph = (it / stages) & 1u;
@@ -373,48 +323,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (is_b) {
-            // this CTA's half of the W2 slice, into both CTAs; the slice is
-            // complete when both halves have landed
-            mbar_arrive_expect_tx(&full[s], kBBytes);
-            tma_load_2d_multicast(sB + s * kBBytes + rank * (kBBytes / 2), &tm_w2, kb * kBK,
-                                  t.expert * a.H + t.nt * kBN + rank * (kBN / 2), &full[s], 0x3);
+            mbar_arrive_expect_tx(&landed[s], kBBytes);
+            tma_load_2d(sB + s * kBBytes, &tm_w2, kb * kBK, t.expert * a.H + t.nt * kBN, &landed[s]);
           } else {
-            mbar_arrive_expect_tx(&full[s], kABytes);
-            tma_load_2d(sA + s * kABytes, &tm_h, kb * kBK, t.row0, &full[s]);
+            mbar_arrive_expect_tx(&landed[s], kABytes);
+            tma_load_2d(sA + s * kABytes, &tm_h, kb * kBK, t.row0, &landed[s]);
           }
         }
       }
-      // the last copies must have landed before the CTA may exit, and the
-      // peer's last commits on this CTA's W2 barriers must have arrived
-      for (int j = it - stages < 0 ? 0 : it - stages; j < it; ++j) {
-        if (!wait_phase(&full[j % stages], (j / stages) & 1u)) ok = false;
-        if (is_b && !wait_phase(&freed[j % stages], (j / stages) & 1u)) ok = false;
-      }
+      // the last copies must have landed before the CTA may exit
+      // (the W2 barrier also needs the prologue's arrivals; its phases for the
+      // last slices complete once the prologue has stored them)
+      for (int j = it - stages < 0 ? 0 : it - stages; j < it; ++j)
+        if (!wait_phase(&landed[j % stages], (j / stages) & 1u)) ok = false;
     }
   } else if (warp == 1) {
     if (lane == 0) {
       int it = 0, n = 0;
-      for (int tile = pair; tile < total && ok; tile += npairs, ++n) {
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
         if (n >= 1 && !wait_phase(acc_empty, (n - 1) & 1u)) {
           ok = false;
           break;
         }
         tc_fence_after();
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int sb = it % kStagesB, st = it % kStagesT;
-          if (!wait_phase(&ready_t[st], (it / kStagesT) & 1u) ||
-              !wait_phase(&full_b[sb], (it / kStagesB) & 1u)) {
+          const int s = it % kStages;
+          if (!wait_phase(&full[s], (it / kStages) & 1u)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t b0 = smem_addr(sB + sb * kBBytes);
+          const uint32_t b0 = smem_addr(sB + s * kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k)
-            umma_bf16_tmem_a(tmem, tmem_a + st * kACols + k * (kUmmaK / 2),
+            umma_bf16_tmem_a(tmem, tmem_a + s * kACols + k * (kUmmaK / 2),
                              sw128_desc(b0 + k * kUmmaK * 2), (kb | k) != 0);
-          umma_commit_multicast(&empty_b[sb], 0x3);  // frees the slice in both CTAs
-          umma_commit(&empty_t[st]);
+          umma_commit(&empty[s]);
         }
         umma_commit(acc_full);
       }
@@ -428,20 +372,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
     auto score_of = [&](int tile) {
       if (tile >= total) return 0.0f;
-      const Tile t = decode_tile(tb, a.E, a.n_tiles, tile, rank);
+      const Tile t = decode_tile(tb, a.E, a.n_tiles, tile);
       const int row = t.row0 + prow;
       return row < t.real_end ? __ldg(a.recv_w + row) : 0.0f;
     };
-    float next_score = score_of(pair);
+    float next_score = score_of(blockIdx.x);
     int it = 0;
-    for (int tile = pair; tile < total && ok; tile += npairs) {
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const float score = next_score;
-      next_score = score_of(tile + npairs);
+      next_score = score_of(tile + gridDim.x);
       for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int sa = it % kStagesA, st = it % kStagesT;
+        const int sa = it % kStagesA, st = it % kStages;
         // each lane waits itself (acquiring the copy); the warp leaves together
         bool got = wait_phase(&full_a[sa], (it / kStagesA) & 1u);
-        if (got && it >= kStagesT) got = wait_phase(&empty_t[st], ((it / kStagesT) & 1u) ^ 1u);
+        if (got && it >= kStages) got = wait_phase(&empty[st], ((it / kStages) & 1u) ^ 1u);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -469,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&free_a[sa]);  // the h slice may be refilled
-          mbar_arrive(&ready_t[st]);
+          mbar_arrive(&full[st]);
         }
       }
     }
@@ -479,8 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int ch = (warp - kFirstEpilogueWarp) >> 2;
     int n = 0;
-    for (int tile = pair; tile < total && ok; tile += npairs, ++n) {
-      const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile, rank);
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+      const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile);
       if (!__all_sync(0xffffffffu, wait_phase(acc_full, n & 1u))) {
         ok = false;
         break;
@@ -495,12 +439,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // is handed back to the MMAs before the (slower) stores to HBM
       uint32_t packed[kBN / 4];
 #pragma unroll
-      for (int c = 0; c < kBN / 2 / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(taddr + c * 32, v);
+      for (int c = 0; c < kBN / 2 / 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16(taddr + c * 16, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          packed[c * 16 + j] =
+        for (int j = 0; j < 8; ++j)
+          packed[c * 8 + j] =
               real ? pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])) : 0u;
       }
       tc_fence_before();  // the loads above precede the MMAs that reuse the columns
@@ -521,8 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (!ok) raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
   tc_fence_before();
-  // neither CTA leaves while the other may still reach its shared memory
-  cluster_sync();
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     // every MMA must be complete before the columns are released: wait for
@@ -587,7 +530,7 @@ cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, co
   if (rows_cap <= 0) return cudaSuccess;
   CUtensorMap tm_h, tm_w2;
   if (!encode_rows(&tm_h, hrows, static_cast<uint64_t>(rows_cap), I, kBM) ||
-      !encode_rows(&tm_w2, w2, static_cast<uint64_t>(E) * H, I, kBN / 2))
+      !encode_rows(&tm_w2, w2, static_cast<uint64_t>(E) * H, I, kBN))
     return cudaErrorInvalidValue;
   W2Args a;
   a.recv_w = recv_w;
@@ -599,31 +542,16 @@ cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, co
   a.I = I;
   a.H = H;
   a.n_tiles = H / kBN;
+  // sum over experts of ceil(segment / kBM) <= (rows + E * (kBM - 1)) / kBM
+  const long long m_tiles = (rows_cap + static_cast<long long>(E) * (kBM - 1)) / kBM;
+  const long long tiles = m_tiles * a.n_tiles;
   if (static_cast<long long>(E) * H > 0x7fffffffLL) return cudaErrorInvalidValue;
-  // pairs of CTAs in clusters of two, as many as can be resident at once
-  static int max_pairs[64] = {0};
-  const int dev = h->device >= 0 && h->device < 64 ? h->device : 0;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (max_pairs[dev] == 0) {
-    cfg.gridDim = dim3(2 * (h->num_sms / 2), 1, 1);
-    int n = 0;
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, w2_absorbed_kernel, &cfg);
-    if (e != cudaSuccess) return e;
-    if (n < 1) return cudaErrorInvalidConfiguration;
-    max_pairs[dev] = n;
-  }
-  cfg.gridDim = dim3(2 * max_pairs[dev], 1, 1);
-  return cudaLaunchKernelEx(&cfg, w2_absorbed_kernel, tm_h, tm_w2, a);
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // one CTA per SM (the operand ring fills its shared memory), never more
+  // CTAs than tiles could exist
+  const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
+  w2_absorbed_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w2, a);
+  return cudaGetLastError();
 }
 
 }  // namespace moe
