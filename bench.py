@@ -38,6 +38,8 @@ DOMINANT = "combine_bwd"
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e data-sheet bandwidth, for context beside the measured peak
 KERNEL_SOURCES = ("combine_moe_route_05_gb300/csrc/rows.cu", "combine_moe_route_05_gb300/csrc/common.cuh")
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "combine_bwd_deepseek_v3.md")
+W2_SOURCES = ("combine_moe_route_05_gb300/csrc/w2_gemm.cu", "combine_moe_route_05_gb300/csrc/common.cuh")
+W2_TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "w2_absorbed_qwen3_235b.md")
 
 
 # ----------------------------------------------------------------------------
@@ -134,27 +136,32 @@ def w2_absorbed_extra(device, stream, reps, tokens=None):
         "fused_ms": t_fused, "unfused_ms": t_unfused, "scale_rows_plus_cublas_per_expert_ms": t_unfused,
         "bitwise_equal_to_unfused": same,
         "roofline": {"kernel": "w2_absorbed", "bound": "tensor", "achieved": achieved, "peak": peak,
-                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
-                     "algorithmic_flops": flop, "peak_source": src},
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "traffic": (measured_traffic_per_launch(wl.name, W2_TRAFFIC_SUMMARY, W2_SOURCES)
+                                 if T == wl.T else None),
+                     "algorithmic_flops": flop,
+                     "algorithmic_bytes": rows * I * 2 + E * H * I * 2 + rows * H * 2 + rows * 4,
+                     "peak_source": src},
+        "kernel_source": kernel_source_hash(W2_SOURCES),
     }
 
 
-def kernel_source_hash():
+def kernel_source_hash(sources=KERNEL_SOURCES):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def measured_traffic_per_launch(workload_name):
-    """DRAM bytes (read + write) per launch of the dominant kernel, from the
-    committed ncu summary, if it was taken on the current kernel source."""
-    if not os.path.exists(TRAFFIC_SUMMARY):
+def measured_traffic_per_launch(workload_name, summary=TRAFFIC_SUMMARY, sources=KERNEL_SOURCES):
+    """DRAM bytes (read + write) per launch of a kernel, from its committed
+    ncu summary, if that was taken on the current kernel source."""
+    if not os.path.exists(summary):
         return None
-    txt = open(TRAFFIC_SUMMARY).read()
+    txt = open(summary).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+workload:\s*(\S+)\s+source:\s*(\w+)", txt)
-    if not m or m.group(2) != workload_name or m.group(3) != kernel_source_hash():
+    if not m or m.group(2) != workload_name or m.group(3) != kernel_source_hash(sources):
         return None
     return float(m.group(1))
 
