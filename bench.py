@@ -510,7 +510,8 @@ def run_gpu(args, wl):
     total_bytes = sum(sb.values())
     dom_ms = stage_ms[DOMINANT]
     achieved = sb[DOMINANT] / (dom_ms / 1e3) / 1e9
-    traffic = measured_traffic_per_launch(wl.name)
+    # the committed summary is for the full-size workload
+    traffic = measured_traffic_per_launch(wl.name) if not args.tokens else None
     cpu = None
     if world == 1 and not args.no_cpu:
         cpu = cpu_baseline(wl, args.cpu_tokens)
