@@ -1,6 +1,6 @@
 // Router-score absorption fused into the W2 grouped GEMM, on the fifth-
-// generation tensor cores (tcgen05 MMA on a CTA pair, accumulators in tensor
-// memory, TMA operand loads).
+// generation tensor cores (tcgen05 MMA, accumulators in tensor memory, TMA
+// operand loads).
 //
 // What it computes ([Titan-absorb] "Implementation": the W2 input is scaled by
 // the routed score in float32 and restored to its dtype before the grouped
@@ -11,31 +11,22 @@
 // with W2 stored [E][H][I].  The scaling is the GEMM's prologue: the scaled
 // rows never reach HBM.  A pad row of a padded layout gets y = 0.
 //
-// Persistent clusters of two CTAs (a CTA pair) walk 256 x 256 output tiles:
-// each CTA owns 128 rows (adjacent m-tiles of one expert; each expert's
-// segment is cut into 128-row tiles, the last one ragged) and half of the
-// 256 W2 columns in shared memory; one MMA instruction of the pair (issued by
-// the even CTA) multiplies the 256 rows by all 256 columns, each CTA keeping
-// its 128 x 256 accumulator in its own tensor memory.  Shared-memory traffic
-// per CTA and 64-wide K slice: 16 KB h + 16 KB W2 landed by TMA, 16 KB of h
-// read by the prologue, 16 KB of W2 read by the tensor cores.  Warp roles,
-// in both CTAs:
+// A persistent CTA per SM walks 128 x 256 output tiles of the experts (a tile
+// never straddles two experts: each expert's segment is cut into 128-row
+// tiles, the last one ragged).  The scaled h slice is the MMA's A operand in
+// TENSOR memory, so shared memory carries only the TMA landings, the
+// prologue's read of h and the tensor cores' read of W2.  Warp roles:
 //   warp 2      TMA: h slices [128 x 64] into a 3-stage ring (128-byte
-//               swizzle), freed once the prologue has consumed them;
-//   warp 0      TMA: this CTA's half [128 x 64] of each W2 slice into an
-//               8-stage ring;
+//               swizzle), freed as soon as the prologue has read them;
+//   warp 0      TMA: W2 slices [256 x 64] into a 5-stage ring;
 //   warps 3-10  prologue: read an h slice (one row per thread, half of its K
 //               range per warp), scale it by the row's score (fp32 product,
 //               bf16 round-to-nearest-even) and store it into the 32-column A
 //               stage in tensor memory that pairs with the W2 stage of the
-//               same index; then tell the even CTA (one barrier there counts
-//               all sixteen prologue warps of the pair, each after its own
-//               CTA's W2 half has landed);
-//   warp 1      tensor memory (both CTAs, allocated as a pair: one 256-column
-//               accumulator + eight A stages); in the even CTA one thread
-//               issues the pair's MMAs (four K=16 steps per slice) and the
-//               commits that free both CTAs' stages and hand over both
-//               accumulators;
+//               same index (one barrier: both operands in place);
+//   warp 1      tensor memory (one 256-column accumulator + five A stages)
+//               and one thread issuing the MMAs (four K=16 steps per slice)
+//               and one commit per slice, freeing both operand stages;
 //   warps 11-18 epilogue: accumulator -> registers (two warps per lane
 //               quarter, half the columns each), accumulator handed back, then
 //               bf16 rows to HBM while the next tile's MMAs run.
@@ -49,43 +40,39 @@
 namespace moe {
 namespace {
 
-constexpr int kBM = 128;     // rows per CTA tile: one tensor-memory lane per row
-constexpr int kBN = 256;     // output columns per tile (both CTAs)
-constexpr int kBNHalf = kBN / 2;  // W2 rows held by one CTA
+constexpr int kBM = 128;     // rows per tile: the MMA's M, one tensor-memory lane per row
+constexpr int kBN = 256;     // output columns per tile: the MMA's N
 constexpr int kBK = 64;      // contraction per stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;   // contraction per MMA instruction (16-bit operands)
-constexpr int kStagesA = 3;  // h slices in shared memory
-// W2 half-slices in shared memory and scaled h slices in tensor memory share
-// one ring index
-constexpr int kStages = 8;
+constexpr int kStagesA = 3;       // h slices in shared memory
+// W2 slices in shared memory and scaled h slices in tensor memory share one
+// ring index, so one barrier says "both operands of slice j are in place" and
+// one commit frees both
+constexpr int kStages = 5;
 constexpr int kPrologueWarps = 8; // two per lane quarter, half the K range each
 constexpr int kEpilogueWarps = 8; // two per lane quarter, half the columns each
 constexpr int kFirstPrologueWarp = 3;
 constexpr int kFirstEpilogueWarp = kFirstPrologueWarp + kPrologueWarps;
 constexpr int kThreads = 32 * (kFirstEpilogueWarp + kEpilogueWarps);
 constexpr uint32_t kABytes = kBM * kBK * 2;
-constexpr uint32_t kBBytes = kBNHalf * kBK * 2;
+constexpr uint32_t kBBytes = kBN * kBK * 2;
 constexpr uint32_t kAccCols = kBN;         // fp32 accumulator: a column per output column
 constexpr uint32_t kACols = kBK / 2;       // a scaled h slice: two bf16 per 32-bit column
 constexpr uint32_t kTmemCols = 512;        // accumulator + kStages A stages (power of 2)
 static_assert(kAccCols + kStages * kACols <= kTmemCols, "tensor memory budget");
-// registers are granted to warps in groups of four: one block per SM needs
-// (warps rounded up to 4) * 32 * registers <= 65536
-constexpr int kMaxRegs = 96;
-static_assert((kThreads / 32 + 3) / 4 * 4 * 32 * kMaxRegs <= 65536, "register budget");
-constexpr size_t kBarrierBytes = 512;
-static_assert(8 * (2 * kStagesA + 3 * kStages + 2) + 16 <= kBarrierBytes, "barrier area");
+static_assert(8 * (2 * kStagesA + 2 * kStages + 2) + 16 <= 512, "barrier area");
 // operand rings, barriers and the tables of at most MOE_MAX_EXPERTS experts
+constexpr size_t kBarrierBytes = 512;  // 34 mbarriers and the tensor-memory address
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStagesA * kABytes + kStages * kBBytes +
                               kBarrierBytes + sizeof(int32_t) * (3 * MOE_MAX_EXPERTS + 2);
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A
 // and B bf16 (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
-// in bits 17-22, M >> 4 in bits 24-28; M = 256 rows over the CTA pair.
+// in bits 17-22, M >> 4 in bits 24-28.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             (static_cast<uint32_t>(kBN >> 3) << 17) |
-                            (static_cast<uint32_t>((2 * kBM) >> 4) << 24);
+                            (static_cast<uint32_t>(kBM >> 4) << 24);
 
 struct W2Args {
   const float* recv_w;
@@ -118,53 +105,15 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-// Cluster-scope test of a phase (the barrier receives arrivals from the peer
-// CTA or from the pair's MMA commits).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
 // Wait for the phase of `bar` with the given parity; false after ~1 s.
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (;;) {
     for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait_cluster(bar, parity)) return true;
+      if (mbar_try_wait(bar, parity)) return true;
     if (global_ns() - t0 > kWaitLimitNs) return false;
   }
-}
-
-// Shared-memory address of the same variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
-  return r;
-}
-
-// Arrive on a barrier of any CTA of the cluster (release at cluster scope).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-               : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// All threads of both CTAs of the pair.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
@@ -187,17 +136,14 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T over the CTA pair (issued by the even
-// CTA): A rows 0-127 from this CTA's tensor memory and 128-255 from the
-// peer's, B columns 0-127 from this CTA's shared memory and 128-255 from the
-// peer's (same addresses); each CTA's tensor memory receives its 128 rows.
-// A in tensor memory: lane = row, 32-bit column j = bf16 elements 2j, 2j+1.
-__device__ __forceinline__ void umma_pair(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc,
-                                          uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]^T: A from tensor memory (lane = row, 32-bit
+// column j = bf16 elements 2j, 2j+1 of the row's K range).
+__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc,
+                                                 uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %3, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %4, p;\n\t}" ::"r"(tmem_d),
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t}" ::"r"(tmem_d),
       "r"(tmem_a), "l"(b_desc), "r"(accumulate), "r"(kIdesc)
       : "memory");
 }
@@ -216,13 +162,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       : "memory");
 }
 
-// Arrive on the barrier at the same offset in both CTAs of the pair once
-// every MMA this thread issued so far has completed.
-__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+// Arrive on `bar` once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(smem_addr(bar)),
-      "h"(static_cast<uint16_t>(0x3))
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
       : "memory");
 }
 
@@ -248,8 +192,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Shared-memory tables of one CTA: the layout's expert segments and, per
-// expert, the index of its first pair of 128-row m-tiles (tile_first[E] = all
-// pairs).
+// expert, the index of its first 128-row m-tile (tile_first[E] = all m-tiles).
 struct Tables {
   int32_t* tile_first;  // [E + 1]
   int32_t* off;         // [E + 1]
@@ -262,13 +205,10 @@ struct Tile {
   int real_end;  // end of the expert's real rows
 };
 
-// Pair tile `tile` (n-tile fastest) -> expert and this CTA's rows: the last
-// expert whose first pair is <= the tile's pair (an empty expert shares its
-// first pair with the next expert and is never the last such one).  CTA
-// `rank` takes m-tile 2 * pair + rank of the expert; past the expert's last
-// m-tile it has no rows (row0 >= seg_end) but still holds its W2 half.
-__device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles, int tile,
-                                            int rank) {
+// Tile `tile` (n-tile fastest) -> expert and rows: the last expert whose first
+// m-tile is <= the tile's m-tile (an empty expert shares its first m-tile with
+// the next expert and is never the last such one).
+__device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles, int tile) {
   const int mt = tile / n_tiles;
   int lo = 0, hi = E - 1;
   while (lo < hi) {
@@ -281,33 +221,31 @@ __device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles
   Tile t;
   t.expert = lo;
   t.nt = tile - mt * n_tiles;
-  t.row0 = tb.off[lo] + (2 * (mt - tb.tile_first[lo]) + rank) * kBM;
+  t.row0 = tb.off[lo] + (mt - tb.tile_first[lo]) * kBM;
   t.seg_end = tb.off[lo + 1];
   t.real_end = tb.off[lo] + tb.cnt[lo];
   return t;
 }
 
-// Persistent: pair p takes pair tiles p, p + npairs, ... in every role of
-// both CTAs, so all roles walk the same sequence of (tile, K slice) jobs;
-// each ring runs on across tiles.
-__global__ void __maxnreg__(kMaxRegs)
+// Persistent: CTA b takes tiles b, b + gridDim.x, ... in every role, so the
+// roles walk the same sequence of (tile, K slice) jobs; each ring runs on
+// across tiles.
+__global__ void __launch_bounds__(kThreads, 1)
     w2_absorbed_kernel(const __grid_constant__ CUtensorMap tm_h,
                        const __grid_constant__ CUtensorMap tm_w2, W2Args a) {
   extern __shared__ uint8_t smem_raw[];
   // operand tiles start on 1024-byte shared-memory boundaries (the swizzle
-  // pattern repeats every 8 rows of 128 bytes); the offsets are the same in
-  // both CTAs, as the pair's MMA requires
+  // pattern repeats every 8 rows of 128 bytes)
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;                       // [kStagesA][kBM x kBK] bf16, swizzled
-  uint8_t* sB = smem + kStagesA * kABytes;  // [kStages][kBNHalf x kBK] bf16, swizzled
+  uint8_t* sB = smem + kStagesA * kABytes;  // [kStages][kBN x kBK] bf16, swizzled
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
   uint64_t* full_a = bars;                   // [kStagesA] h slice landed
-  uint64_t* free_a = full_a + kStagesA;      // [kStagesA] h slice consumed by the prologue
-  uint64_t* full_b = free_a + kStagesA;      // [kStages] this CTA's W2 half landed
-  uint64_t* empty = full_b + kStages;        // [kStages] the pair's MMAs done with the stage
-  uint64_t* full = empty + kStages;          // [kStages] even CTA: both CTAs' operands in place
-  uint64_t* acc_full = full + kStages;       // accumulator complete
-  uint64_t* acc_empty = acc_full + 1;        // even CTA: both CTAs' accumulators drained
+  uint64_t* free_a = full_a + kStagesA;      // [kStagesA] h slice read by the prologue
+  uint64_t* full = free_a + kStagesA;       // [kStages] W2 slice landed, scaled h slice stored
+  uint64_t* empty = full + kStages;         // [kStages] MMAs done with both
+  uint64_t* acc_full = empty + kStages;     // accumulator complete
+  uint64_t* acc_empty = acc_full + 1;        // accumulator drained
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
   Tables tb;
   tb.tile_first = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(bars) + kBarrierBytes);
@@ -316,8 +254,6 @@ __global__ void __maxnreg__(kMaxRegs)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (a.I + kBK - 1) / kBK;
-  const int rank = static_cast<int>(cluster_rank());
-  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   for (int e = threadIdx.x; e <= a.E; e += kThreads) {
     tb.off[e] = a.off_e[e];
@@ -325,11 +261,11 @@ __global__ void __maxnreg__(kMaxRegs)
   }
   __syncthreads();
   if (warp == 0) {
-    // exclusive scan of the per-expert counts of m-tile pairs
+    // exclusive scan of the per-expert m-tile counts
     int running = 0;
     for (int base = 0; base < a.E; base += 32) {
       const int e = base + lane;
-      const int tiles = e < a.E ? ((tb.off[e + 1] - tb.off[e] + kBM - 1) / kBM + 1) / 2 : 0;
+      const int tiles = e < a.E ? (tb.off[e + 1] - tb.off[e] + kBM - 1) / kBM : 0;
       int incl = tiles;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -346,43 +282,39 @@ __global__ void __maxnreg__(kMaxRegs)
         mbar_init(&free_a[s], kPrologueWarps);
       }
       for (int s = 0; s < kStages; ++s) {
-        mbar_init(&full_b[s], 1);
-        mbar_init(&empty[s], 1);                    // the pair's commit
-        mbar_init(&full[s], 2 * kPrologueWarps);    // prologue warps of both CTAs
+        mbar_init(&full[s], 1 + kPrologueWarps);  // W2 producer + prologue warps
+        mbar_init(&empty[s], 1);
       }
-      mbar_init(acc_full, 1);                       // the pair's commit
-      mbar_init(acc_empty, 2 * kEpilogueWarps);     // epilogue warps of both CTAs
+      mbar_init(acc_full, 1);
+      mbar_init(acc_empty, kEpilogueWarps);
       fence_mbar_init();
     }
   } else if (warp == 1) {
-    // the pair allocates together: one warp of each CTA
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
   }
   tc_fence_before();
-  // the peer's barriers must be initialised before its arrivals and commits
-  // can reach them
-  cluster_sync();
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;     // accumulator: columns [0, 256)
   const uint32_t tmem_a = tmem + kAccCols;  // A stages: 32 columns each
   const int total = tb.tile_first[a.E] * a.n_tiles;
-  const int my_tiles = pair < total ? (total - pair + npairs - 1) / npairs : 0;
+  const int my_tiles =
+      blockIdx.x < total ? (total - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x : 0;
 
   bool ok = true;
   if (warp == 0 || warp == 2) {
-    // TMA producers: warp 0 this CTA's halves of the W2 slices, warp 2 the h
-    // slices
+    // TMA producers: warp 0 the W2 slices, warp 2 the h slices
     if (lane == 0) {
       const bool is_b = warp == 0;
       const int stages = is_b ? kStages : kStagesA;
-      uint64_t* landed = is_b ? full_b : full_a;
+      uint64_t* landed = is_b ? full : full_a;
       uint64_t* freed = is_b ? empty : free_a;
       int it = 0;
-      for (int tile = pair; tile < total && ok; tile += npairs) {
-        const Tile t = decode_tile(tb, a.E, a.n_tiles, tile, rank);
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const Tile t = decode_tile(tb, a.E, a.n_tiles, tile);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % stages;
           const uint32_t ph = (it / stages) & 1u;
@@ -392,25 +324,23 @@ __global__ void __maxnreg__(kMaxRegs)
           }
           if (is_b) {
             mbar_arrive_expect_tx(&landed[s], kBBytes);
-            tma_load_2d(sB + s * kBBytes, &tm_w2, kb * kBK,
-                        t.expert * a.H + t.nt * kBN + rank * kBNHalf, &landed[s]);
+            tma_load_2d(sB + s * kBBytes, &tm_w2, kb * kBK, t.expert * a.H + t.nt * kBN, &landed[s]);
           } else {
             mbar_arrive_expect_tx(&landed[s], kABytes);
             tma_load_2d(sA + s * kABytes, &tm_h, kb * kBK, t.row0, &landed[s]);
           }
         }
       }
-      // the last copies must have landed before the CTA may exit, and the
-      // pair's last commits on this CTA's W2 stages must have arrived
-      for (int j = it - stages < 0 ? 0 : it - stages; j < it; ++j) {
+      // the last copies must have landed before the CTA may exit
+      // (the W2 barrier also needs the prologue's arrivals; its phases for the
+      // last slices complete once the prologue has stored them)
+      for (int j = it - stages < 0 ? 0 : it - stages; j < it; ++j)
         if (!wait_phase(&landed[j % stages], (j / stages) & 1u)) ok = false;
-        if (is_b && !wait_phase(&freed[j % stages], (j / stages) & 1u)) ok = false;
-      }
     }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
+    if (lane == 0) {
       int it = 0, n = 0;
-      for (int tile = pair; tile < total && ok; tile += npairs, ++n) {
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
         if (n >= 1 && !wait_phase(acc_empty, (n - 1) & 1u)) {
           ok = false;
           break;
@@ -426,11 +356,11 @@ __global__ void __maxnreg__(kMaxRegs)
           const uint32_t b0 = smem_addr(sB + s * kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k)
-            umma_pair(tmem, tmem_a + s * kACols + k * (kUmmaK / 2), sw128_desc(b0 + k * kUmmaK * 2),
-                      (kb | k) != 0);
-          umma_commit_pair(&empty[s]);  // frees the stage in both CTAs
+            umma_bf16_tmem_a(tmem, tmem_a + s * kACols + k * (kUmmaK / 2),
+                             sw128_desc(b0 + k * kUmmaK * 2), (kb | k) != 0);
+          umma_commit(&empty[s]);
         }
-        umma_commit_pair(acc_full);
+        umma_commit(acc_full);
       }
     }
   } else if (warp < kFirstEpilogueWarp) {
@@ -442,20 +372,20 @@ __global__ void __maxnreg__(kMaxRegs)
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
     auto score_of = [&](int tile) {
       if (tile >= total) return 0.0f;
-      const Tile t = decode_tile(tb, a.E, a.n_tiles, tile, rank);
+      const Tile t = decode_tile(tb, a.E, a.n_tiles, tile);
       const int row = t.row0 + prow;
       return row < t.real_end ? __ldg(a.recv_w + row) : 0.0f;
     };
-    float next_score = score_of(pair);
+    float next_score = score_of(blockIdx.x);
     int it = 0;
-    for (int tile = pair; tile < total && ok; tile += npairs) {
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       const float score = next_score;
-      next_score = score_of(tile + npairs);
+      next_score = score_of(tile + gridDim.x);
       for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int sa = it % kStagesA, s = it % kStages;
+        const int sa = it % kStagesA, st = it % kStages;
         // each lane waits itself (acquiring the copy); the warp leaves together
         bool got = wait_phase(&full_a[sa], (it / kStagesA) & 1u);
-        if (got && it >= kStages) got = wait_phase(&empty[s], ((it / kStages) & 1u) ^ 1u);
+        if (got && it >= kStages) got = wait_phase(&empty[st], ((it / kStages) & 1u) ^ 1u);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -478,18 +408,13 @@ __global__ void __maxnreg__(kMaxRegs)
             packed[c * 4 + j] = pack_bf16x2(lo, hi);
           }
         }
-        tmem_st16(tmem_a + lane_bits + s * kACols + kh * 16, packed);
+        tmem_st16(tmem_a + lane_bits + st * kACols + kh * 16, packed);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          // the h slice may be refilled only after the store above consumed
-          // the loaded values
-          mbar_arrive(&free_a[sa]);
-          // the even CTA's MMA needs this CTA's A stage and W2 half
-          if (!wait_phase(&full_b[s], (it / kStages) & 1u)) ok = false;
-          mbar_arrive_cluster(cluster_addr(&full[s], 0));
+          mbar_arrive(&free_a[sa]);  // the h slice may be refilled
+          mbar_arrive(&full[st]);
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
     }
   } else {
@@ -497,10 +422,9 @@ __global__ void __maxnreg__(kMaxRegs)
     // ch of the accumulator
     const int q = warp & 3;
     const int ch = (warp - kFirstEpilogueWarp) >> 2;
-    const uint32_t acc_empty_even = cluster_addr(acc_empty, 0);
     int n = 0;
-    for (int tile = pair; tile < total && ok; tile += npairs, ++n) {
-      const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile, rank);
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+      const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile);
       if (!__all_sync(0xffffffffu, wait_phase(acc_full, n & 1u))) {
         ok = false;
         break;
@@ -525,7 +449,7 @@ __global__ void __maxnreg__(kMaxRegs)
       }
       tc_fence_before();  // the loads above precede the MMAs that reuse the columns
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty_even);
+      if (lane == 0) mbar_arrive(acc_empty);
       if (real || pad) {
 #pragma unroll
         for (int j = 0; j < kBN / 2 / 8; ++j) {
@@ -541,8 +465,7 @@ __global__ void __maxnreg__(kMaxRegs)
   }
   if (!ok) raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
   tc_fence_before();
-  // neither CTA leaves while the other may still reach its shared memory
-  cluster_sync();
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     // every MMA must be complete before the columns are released: wait for
@@ -551,7 +474,7 @@ __global__ void __maxnreg__(kMaxRegs)
     if (lane == 0 && my_tiles > 0 && !wait_phase(acc_full, (my_tiles - 1) & 1u))
       raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
     __syncwarp();
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
   }
@@ -605,10 +528,9 @@ cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, co
   const long long rows_cap = static_cast<long long>(h->T) * c.top_k +
                              static_cast<long long>(E) * (h->pad - 1);
   if (rows_cap <= 0) return cudaSuccess;
-  if (static_cast<long long>(E) * H > 0x7fffffffLL) return cudaErrorInvalidValue;
   CUtensorMap tm_h, tm_w2;
   if (!encode_rows(&tm_h, hrows, static_cast<uint64_t>(rows_cap), I, kBM) ||
-      !encode_rows(&tm_w2, w2, static_cast<uint64_t>(E) * H, I, kBNHalf))
+      !encode_rows(&tm_w2, w2, static_cast<uint64_t>(E) * H, I, kBN))
     return cudaErrorInvalidValue;
   W2Args a;
   a.recv_w = recv_w;
@@ -620,31 +542,16 @@ cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, co
   a.I = I;
   a.H = H;
   a.n_tiles = H / kBN;
-  // CTA pairs in clusters of two, as many as can be resident at once (one
-  // CTA per SM: the rings fill its shared memory)
-  static int max_pairs[64] = {0};
-  const int dev = h->device >= 0 && h->device < 64 ? h->device : 0;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (max_pairs[dev] == 0) {
-    cfg.gridDim = dim3(2 * (h->num_sms / 2), 1, 1);
-    int n = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, w2_absorbed_kernel, &cfg);
-    if (e != cudaSuccess) return e;
-    if (n < 1) return cudaErrorInvalidConfiguration;
-    max_pairs[dev] = n;
-  }
-  cfg.gridDim = dim3(2 * max_pairs[dev], 1, 1);
-  return cudaLaunchKernelEx(&cfg, w2_absorbed_kernel, tm_h, tm_w2, a);
+  // sum over experts of ceil(segment / kBM) <= (rows + E * (kBM - 1)) / kBM
+  const long long m_tiles = (rows_cap + static_cast<long long>(E) * (kBM - 1)) / kBM;
+  const long long tiles = m_tiles * a.n_tiles;
+  if (static_cast<long long>(E) * H > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // one CTA per SM (the operand ring fills its shared memory), never more
+  // CTAs than tiles could exist
+  const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
+  w2_absorbed_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w2, a);
+  return cudaGetLastError();
 }
 
 }  // namespace moe
