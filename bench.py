@@ -310,7 +310,7 @@ def run_reference(args, wl):
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic", "config": workload_config(wl, extra={"sample_tokens_per_step": tokens}),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "first %d of %d tokens per step, whole path, single-threaded "
@@ -365,14 +365,16 @@ def run_gpu(args, wl):
     h = r.h
     logits, bias, x, y, g = (dev_tensor(inp[k]) for k in ("logits", "bias", "x", "y", "g"))
     bf = torch.bfloat16
+    rd = bf if wl.dtype == "bf16" else torch.float32  # row dtype of the workload
+    bits = (lambda t: t.view(torch.int16)) if rd == bf else (lambda t: t)
     idx = torch.empty(T, K, dtype=torch.int32, device=device)
     w = torch.empty(T, K, dtype=torch.float32, device=device)
-    recv = torch.empty(T * K, H, dtype=bf, device=device)
+    recv = torch.empty(T * K, H, dtype=rd, device=device)
     recv_w = torch.empty(T * K, dtype=torch.float32, device=device)
-    out = torch.empty(T, H, dtype=bf, device=device)
-    gy = torch.empty(T * K, H, dtype=bf, device=device)
+    out = torch.empty(T, H, dtype=rd, device=device)
+    gy = torch.empty(T * K, H, dtype=rd, device=device)
     gw = torch.empty(T, K, dtype=torch.float32, device=device)
-    gx = torch.empty(T, H, dtype=bf, device=device)
+    gx = torch.empty(T, H, dtype=rd, device=device)
     stream = torch.cuda.current_stream()
     names = ("route_topk", "dispatch_layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd")
     launches_per_step = 7
@@ -403,6 +405,14 @@ def run_gpu(args, wl):
         step()
     torch.cuda.synchronize()
     assert moe.moe_read_device_status(h) == 0
+    # expert load of the routed batch (read outside the timed region); the
+    # skewed workload must put more than 5x the mean load on its heaviest
+    # expert and no token at all on exactly one expert
+    cnt = moe.layout_tensors(h)["cnt_e"].cpu().numpy()
+    load = {"max_over_mean": float(cnt.max() / cnt.mean()), "zero_load_experts": int((cnt == 0).sum()),
+            "histogram_top8": [int(c) for c in np.sort(cnt)[::-1][:8]]}
+    if wl.bias == "zipf" and not args.tokens:
+        assert load["max_over_mean"] > 5 and load["zero_load_experts"] == 1, load
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -432,10 +442,10 @@ def run_gpu(args, wl):
         dev_in = {"logits": logits, "bias": bias, "x": x, "y": y, "g": g}
         host_out = {"idx": torch.empty(T, K, dtype=torch.int32).pin_memory(),
                     "w": torch.empty(T, K, dtype=torch.float32).pin_memory(),
-                    "out": torch.empty(T, H, dtype=torch.int16).pin_memory(),
+                    "out": bits(torch.empty(T, H, dtype=rd)).pin_memory(),
                     "gw": torch.empty(T, K, dtype=torch.float32).pin_memory(),
-                    "gx": torch.empty(T, H, dtype=torch.int16).pin_memory()}
-        dev_out = {"idx": idx, "w": w, "out": out.view(torch.int16), "gw": gw, "gx": gx.view(torch.int16)}
+                    "gx": bits(torch.empty(T, H, dtype=rd)).pin_memory()}
+        dev_out = {"idx": idx, "w": w, "out": bits(out), "gw": gw, "gx": bits(gx)}
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
@@ -506,7 +516,7 @@ def run_gpu(args, wl):
         step()
         glogits = torch.empty(T, E, dtype=torch.float32, device=device)
         t_rb = time_op(lambda: moe.moe_route_bwd(h, logits, idx, gw, glogits))
-        send = torch.empty(T * min(K, R), H, dtype=bf, device=device)
+        send = torch.empty(T * min(K, R), H, dtype=rd, device=device)
         partial = torch.empty_like(send)
         t_ds = time_op(lambda: moe.moe_dispatch(h, x, w, recv, recv_w, send))
         t_ex = time_op(lambda: moe.moe_expand(h, send, recv))
@@ -544,7 +554,7 @@ def run_gpu(args, wl):
     line = {
         "metric": METRIC, "value": world * T / (ms_step / 1e3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
         "data": "synthetic", "config": workload_config(wl),
         "hbm_gbs": total_bytes / (ms_step / 1e3) / 1e9,
         "hbm_frac_of_peak": total_bytes / (ms_step / 1e3) / 1e9 / peak,
@@ -561,6 +571,7 @@ def run_gpu(args, wl):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "kernel_source": kernel_source_hash(),
+        "expert_load": load,
         "extras": extras,
     }
     print(json.dumps(line), flush=True)
