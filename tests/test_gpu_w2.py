@@ -149,6 +149,36 @@ def test_w2_absorbed_full_size_sampled_rows():
     print("full size: %d rows, %.4f%% one ulp off" % (rows.size, 100 * frac))
 
 
+@pytest.mark.parametrize("E,K,R,T,I,H", [(512, 8, 64, 300, 8, 256),   # E at its maximum, I at its minimum
+                                         (8, 2, 2, 1, 64, 256),        # one token
+                                         (16, 4, 4, 257, 72, 768)])    # ragged I past one slice, 3 n-tiles
+def test_w2_absorbed_shapes(E, K, R, T, I, H):
+    wl = dataclasses.replace(synth.WORKLOADS[1], E=E, K=K, R=R).with_tokens(T)
+    wl, r, L, recv_w, h, w2 = problem(wl, I=I, H=H)
+    y = run_gpu(r, h, recv_w, w2, sentinel=0x7FC1)
+    n = int(L.off_e[-1])
+    yb, y64 = oracle.w2_absorbed(h, recv_w, w2, L.off_e, L.cnt_e, rows=np.arange(n))
+    seg_of = np.repeat(np.arange(wl.E), np.diff(L.off_e))
+    check_rows(y[:n], y64, yb, abs_terms(h[:n], recv_w[:n], w2, seg_of), I, "shape")
+
+
+def test_w2_absorbed_pad_rows_ignore_their_input():
+    """Pad rows of a padded layout hold whatever the caller left there (NaN
+    here): they come out 0 and no real row is touched by them."""
+    wl, r, L, recv_w, h, w2 = problem(synth.WORKLOADS[4].with_tokens(300), I=64, H=256, pad=128)
+    n = int(L.off_e[-1])
+    real = np.zeros(h.shape[0], bool)
+    for e in range(wl.E):
+        real[L.off_e[e]:L.off_e[e] + L.cnt_e[e]] = True
+    h = h.copy()
+    h[~real] = 0x7FC0  # bf16 NaN in every pad row
+    y = run_gpu(r, h, recv_w, w2)
+    assert (y[:n][~real[:n]] == 0).all()
+    yb, y64 = oracle.w2_absorbed(h, recv_w, w2, L.off_e, L.cnt_e, rows=np.nonzero(real)[0])
+    seg_of = np.searchsorted(L.off_e, np.nonzero(real)[0], side="right") - 1
+    check_rows(y[real], y64, yb, abs_terms(h[real], recv_w[real], w2, seg_of), 64, "pads")
+
+
 def test_w2_absorbed_argument_checks():
     wl = dataclasses.replace(synth.WORKLOADS[4].with_tokens(64), I=64, H=256)
     r = router(wl)
