@@ -24,6 +24,8 @@
 // Masks are stored word-major with an odd row stride ([word][col], stride
 // cols | 1) so that the lanes of a warp, which share a word index and differ in
 // column, hit different shared-memory banks.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -33,7 +35,6 @@ namespace {
 constexpr int kTile = MOE_LAYOUT_TILE_TOKENS;
 constexpr int kWords = kTile / 32;  // mask words per column
 constexpr int kThreads = kTile;
-constexpr int kWarps = kThreads / 32;
 static_assert(kTile % 32 == 0 && kTile <= 1024, "tile must be whole warps of one block");
 
 struct LayoutArgs {
@@ -42,7 +43,7 @@ struct LayoutArgs {
   int pad;       // receive segments rounded up to a multiple of pad rows
   int recv_cap;  // receive rows: T*K + E*(pad-1)
   uint32_t* flags;
-  uint32_t* ticket;
+  uint32_t* ticket;  // [0] arrival counter, [1] epoch of the single-pass kernel
   int32_t* cnt_e;
   int32_t* off_e;
   int32_t* cnt_send_r;
@@ -98,34 +99,11 @@ __device__ __forceinline__ uint32_t mark_token(const LayoutArgs& a, int t, uint3
   return valid;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a) {
-  extern __shared__ uint32_t lsm[];
+// The last block to arrive: exclusive scan of each column over the tiles (in
+// place in tile_hist), then exclusive scans over experts and over ranks into
+// the count and offset arrays.  `tot` is [E + R] shared-memory scratch.
+__device__ void scan_tiles(const LayoutArgs& a, int32_t* tot) {
   const int cols = a.E + a.R;
-  const int cp = col_stride(cols);
-  uint32_t* masks = lsm;  // [kWords][cp]
-  const int tile = blockIdx.x;
-  for (int i = threadIdx.x; i < kWords * cp; i += kThreads) masks[i] = 0;
-  __syncthreads();
-  int ek[MOE_MAX_TOPK];
-  mark_token(a, tile * kTile + threadIdx.x, masks, cp, nullptr, ek);
-  __syncthreads();
-  for (int col = threadIdx.x; col < cols; col += kThreads) {
-    int c = 0;
-#pragma unroll 8
-    for (int w = 0; w < kWords; ++w) c += __popc(masks[w * cp + col]);
-    a.tile_hist[static_cast<size_t>(tile) * cols + col] = c;
-  }
-  __threadfence();
-  __syncthreads();
-  __shared__ int is_last;
-  if (threadIdx.x == 0) is_last = atomicAdd(a.ticket, 1u) == static_cast<uint32_t>(a.ntiles - 1);
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-
-  // Last block: exclusive scan of each column over the tiles (in place), then
-  // exclusive scans over experts and over ranks.
-  int32_t* tot = reinterpret_cast<int32_t*>(masks);  // [cols], masks are dead now
   for (int col = threadIdx.x; col < cols; col += kThreads) {
     int run = 0;
     for (int t0 = 0; t0 < a.ntiles; t0 += 16) {
@@ -182,10 +160,36 @@ __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a)
     a.off_recv_r[r] = a.off_e[r * a.epr];
     a.cnt_recv_r[r] = n;
   }
-  if (threadIdx.x == 0) {
-    a.off_recv_r[a.R] = a.off_e[a.E];
-    *a.ticket = 0;  // ready for the next layout
+  if (threadIdx.x == 0) a.off_recv_r[a.R] = a.off_e[a.E];
+}
+
+__global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a) {
+  extern __shared__ uint32_t lsm[];
+  const int cols = a.E + a.R;
+  const int cp = col_stride(cols);
+  uint32_t* masks = lsm;  // [kWords][cp]
+  const int tile = blockIdx.x;
+  for (int i = threadIdx.x; i < kWords * cp; i += kThreads) masks[i] = 0;
+  __syncthreads();
+  int ek[MOE_MAX_TOPK];
+  mark_token(a, tile * kTile + threadIdx.x, masks, cp, nullptr, ek);
+  __syncthreads();
+  for (int col = threadIdx.x; col < cols; col += kThreads) {
+    int c = 0;
+#pragma unroll 8
+    for (int w = 0; w < kWords; ++w) c += __popc(masks[w * cp + col]);
+    a.tile_hist[static_cast<size_t>(tile) * cols + col] = c;
   }
+  __threadfence();
+  __syncthreads();
+  __shared__ int is_last;
+  if (threadIdx.x == 0) is_last = atomicAdd(a.ticket, 1u) == static_cast<uint32_t>(a.ntiles - 1);
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  scan_tiles(a, reinterpret_cast<int32_t*>(masks));  // masks are dead now
+  if (threadIdx.x == 0) *a.ticket = 0;  // ready for the next layout
 }
 
 // shared memory of the scatter kernel, in order
@@ -199,7 +203,11 @@ struct ScatterSmem {
   __host__ __device__ size_t sst() const { return rst() + sizeof(uint32_t) * kTile * K; }
   __host__ __device__ size_t base() const { return sst() + sizeof(uint32_t) * kTile * KR; }
   __host__ __device__ size_t off() const { return base() + sizeof(int32_t) * cols; }
-  __host__ __device__ size_t bytes() const { return off() + sizeof(int32_t) * (cols + 2); }
+  __host__ __device__ size_t tot() const { return off() + sizeof(int32_t) * (cols + 2); }
+  // the single-pass kernel also needs the column totals of its scan
+  __host__ __device__ size_t bytes(bool with_tot = false) const {
+    return tot() + (with_tot ? sizeof(int32_t) * cols : 0);
+  }
   __host__ __device__ static size_t align(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
 };
 
@@ -211,6 +219,26 @@ __device__ __forceinline__ uint32_t pack_send(int r, int tl) {
   return static_cast<uint32_t>(r) | (static_cast<uint32_t>(tl) << 9);
 }
 
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// kSinglePass = false: the second of two launches (the counts and their
+// scan come from layout_count_kernel).  kSinglePass = true: the whole layout
+// in one cooperative launch (all tiles resident at once): each block counts
+// its tile, the last block to arrive scans the counts and publishes them by
+// bumping an epoch that the other blocks wait for (at most 1 s, then the
+// status word's time-out bit and no writes), and every block goes on to place
+// its tile with the masks still in shared memory.
+template <bool kSinglePass>
 __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs a) {
   extern __shared__ __align__(16) uint8_t ssm[];
   const int cols = a.E + a.R;
@@ -231,14 +259,17 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   const int tile_n = max(0, min(kTile, a.T - tile_t0));  // tokens in this tile
 
   for (int i = threadIdx.x; i < kWords * cp; i += kThreads) masks[i] = 0;
-  for (int c = threadIdx.x; c < cols; c += kThreads) {
-    base[c] = a.tile_hist[static_cast<size_t>(tile) * cols + c];
-    off[c + (c >= a.E ? 1 : 0)] = c < a.E ? a.off_e[c] : a.off_send_r[c - a.E];
-  }
-  if (threadIdx.x == 0) {
-    off[a.E] = a.off_e[a.E];
-    off[cols + 1] = a.off_send_r[a.R];
-  }
+  auto load_bases = [&]() {
+    for (int c = threadIdx.x; c < cols; c += kThreads) {
+      base[c] = __ldcg(a.tile_hist + static_cast<size_t>(tile) * cols + c);
+      off[c + (c >= a.E ? 1 : 0)] = c < a.E ? __ldcg(a.off_e + c) : __ldcg(a.off_send_r + c - a.E);
+    }
+    if (threadIdx.x == 0) {
+      off[a.E] = __ldcg(a.off_e + a.E);
+      off[cols + 1] = __ldcg(a.off_send_r + a.R);
+    }
+  };
+  if (!kSinglePass) load_bases();
   __syncthreads();
   const int t = tile_t0 + threadIdx.x;
   int ek[MOE_MAX_TOPK];
@@ -254,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
       run += __popc(masks[w * cp + col]);
     }
     seg[col + (col >= a.E ? 1 : 0)] = run;
+    if (kSinglePass) a.tile_hist[static_cast<size_t>(tile) * cols + col] = run;
   }
   __syncthreads();
   if (warp < 2) {
@@ -279,6 +311,45 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
     if (lane == 31) v[n] = incl;
   }
   __syncthreads();
+
+  if (kSinglePass) {
+    // grid-wide hand-over of the tile counts
+    __shared__ uint32_t epoch0;
+    __shared__ int last, failed;
+    __threadfence();  // this tile's counts are visible device-wide
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      epoch0 = ld_acquire(a.ticket + 1);  // read before arriving
+      last = atomicAdd(a.ticket, 1u) == static_cast<uint32_t>(a.ntiles - 1);
+      failed = 0;
+    }
+    __syncthreads();
+    if (last) {
+      __threadfence();
+      scan_tiles(a, reinterpret_cast<int32_t*>(ssm + L.tot()));
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        *a.ticket = 0;  // ready for the next layout
+        __threadfence();
+        atomicAdd(a.ticket + 1, 1u);  // publish
+      }
+    } else if (threadIdx.x == 0) {
+      const unsigned long long t0 = global_ns();
+      while (ld_acquire(a.ticket + 1) == epoch0) {
+        if (global_ns() - t0 > 1000000000ull) {
+          raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
+          failed = 1;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __syncthreads();
+    if (failed) return;
+    load_bases();
+    __syncthreads();
+  }
 
   const int32_t* off_e = off;
   const int32_t* off_s = off + a.E + 1;
@@ -368,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   // and send rows past S
   if (a.pad > 1) {
     for (int e = blockIdx.x; e < a.E; e += gridDim.x) {
-      const int lo = off_e[e] + a.cnt_e[e], hi = off_e[e + 1];
+      const int lo = off_e[e] + __ldcg(a.cnt_e + e), hi = off_e[e + 1];
       for (int p = lo + threadIdx.x; p < hi; p += kThreads) {
         a.recv_token[p] = -1;
         a.recv_k[p] = -1;
@@ -388,14 +459,14 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
 
 size_t count_smem(int cols) { return static_cast<size_t>(kWords) * col_stride(cols) * sizeof(uint32_t); }
 
-size_t scatter_smem(int cols, int K, int R) {
-  return ScatterSmem{cols, col_stride(cols), K, K < R ? K : R}.bytes();
+size_t scatter_smem(int cols, int K, int R, bool single_pass = false) {
+  return ScatterSmem{cols, col_stride(cols), K, K < R ? K : R}.bytes(single_pass);
 }
 
 }  // namespace
 
 size_t layout_smem_bytes(int E, int R) {
-  const size_t a = count_smem(E + R), b = scatter_smem(E + R, MOE_MAX_TOPK, R);
+  const size_t a = count_smem(E + R), b = scatter_smem(E + R, MOE_MAX_TOPK, R, true);
   return a > b ? a : b;
 }
 
@@ -404,11 +475,43 @@ cudaError_t prepare_layout_kernels() {
   cudaError_t e = cudaFuncSetAttribute(layout_count_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(layout_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              max_smem);
+  e = cudaFuncSetAttribute(layout_scatter_kernel<false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(layout_scatter_kernel<true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
 }
 
 int layout_tiles(int T) { return T > 0 ? (T + kTile - 1) / kTile : 1; }
+
+namespace {
+// Blocks of the single-pass kernel that fit on the current device at once
+// for a given shared-memory size (0 if the query fails); cached, since the
+// layout is launched every step.
+int resident_single_pass_blocks(size_t smem) {
+  struct Entry {
+    int dev;
+    size_t smem;
+    int blocks;
+  };
+  static std::mutex mu;
+  static Entry cache[16];
+  static int used = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].dev == dev && cache[i].smem == smem) return cache[i].blocks;
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, layout_scatter_kernel<true>, kThreads,
+                                                    smem) != cudaSuccess)
+    return 0;
+  const int blocks = per_sm * sms;
+  if (used < 16) cache[used++] = Entry{dev, smem, blocks};
+  return blocks;
+}
+}  // namespace
 
 // The two launches over caller-chosen buffers: the outputs in `out`, the
 // status word `flags` (may be null), and the scratch (arrival ticket, zero on
@@ -444,10 +547,21 @@ cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T
   a.recv_send_row = out.recv_send_row;
   a.tile_hist = tile_hist;
   const int cols = a.E + a.R;
+  // one cooperative launch when every tile's block can be resident at once
+  // (the blocks wait for the last one's scan), else two launches
+  const size_t one_smem = scatter_smem(cols, a.K, a.R, true);
+  if (a.ntiles <= resident_single_pass_blocks(one_smem)) {
+    void* params[] = {&a};
+    const cudaError_t e = cudaLaunchCooperativeKernel(
+        reinterpret_cast<const void*>(layout_scatter_kernel<true>), dim3(a.ntiles), dim3(kThreads),
+        params, one_smem, s);
+    if (e == cudaSuccess) return cudaSuccess;
+    (void)cudaGetLastError();  // not launched: take the two-launch path
+  }
   layout_count_kernel<<<a.ntiles, kThreads, count_smem(cols), s>>>(a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  layout_scatter_kernel<<<a.ntiles, kThreads, scatter_smem(cols, a.K, a.R), s>>>(a);
+  layout_scatter_kernel<false><<<a.ntiles, kThreads, scatter_smem(cols, a.K, a.R), s>>>(a);
   return cudaGetLastError();
 }
 
