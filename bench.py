@@ -377,7 +377,7 @@ def run_gpu(args, wl):
     gx = torch.empty(T, H, dtype=rd, device=device)
     stream = torch.cuda.current_stream()
     names = ("route_topk", "dispatch_layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd")
-    launches_per_step = 7
+    launches_per_step = 5 + moe.moe_dispatch_layout_launches(h, T)
 
     def step(ev=None, logits=logits, bias=bias, x=x, y=y, g=g):
         if ev is not None:

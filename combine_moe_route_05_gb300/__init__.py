@@ -33,7 +33,7 @@ EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_handle_create", "moe
            "moe_combine", "moe_combine_bwd", "moe_dispatch_bwd", "moe_scale_rows",
            "moe_scale_rows_bwd", "moe_read_device_status", "moe_clear_device_status",
            "moe_dispatch_layout_static", "moe_route_bwd", "moe_expand", "moe_combine_partial",
-           "moe_combine_reduce", "moe_w2_absorbed")
+           "moe_combine_reduce", "moe_w2_absorbed", "moe_dispatch_layout_launches")
 MOE_LAYOUT_STATIC_COUNTERS = 65536
 MOE_LAYOUT_TILE_TOKENS = 512
 
@@ -94,6 +94,7 @@ def lib():
             "moe_combine_partial": ([P, P, i32, i32, P, P, P], st),
             "moe_combine_reduce": ([P, P, i32, i32, P, P], st),
             "moe_w2_absorbed": ([P, P, i32, P, P, i32, P, P], st),
+            "moe_dispatch_layout_launches": ([P, i32, P], st),
         }
         for name, (args, res) in sigs.items():
             f = getattr(L, name)
@@ -342,6 +343,14 @@ def moe_w2_absorbed(h, hrows, recv_w, w2, y, stream=None):
     _req(y, torch.bfloat16, (h.recv_rows, H), "y")
     _check("moe_w2_absorbed", lib().moe_w2_absorbed(h.ptr, _ptr(hrows), I, _ptr(recv_w), _ptr(w2),
                                                     H, _ptr(y), _stream(stream)))
+
+
+def moe_dispatch_layout_launches(h, T):
+    """Kernel launches moe_dispatch_layout makes for T tokens (1 or 2)."""
+    n = ctypes.c_int32(0)
+    _check("moe_dispatch_layout_launches",
+           lib().moe_dispatch_layout_launches(h.ptr, T, ctypes.byref(n)))
+    return n.value
 
 
 def moe_read_device_status(h):

@@ -330,6 +330,17 @@ moe_status moe_scale_rows_bwd(const moe_handle* h, const void* d_ghs, const void
                                               as_stream(stream)));
 }
 
+moe_status moe_dispatch_layout_launches(const moe_handle* h, int32_t T, int32_t* n_launches) {
+  if (!h || !n_launches || T < 0) return MOE_ERR_INVALID;
+  if (T > h->cfg.max_tokens) return MOE_ERR_CAPACITY;
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (prev != h->device && cudaSetDevice(h->device) != cudaSuccess) return MOE_ERR_CUDA;
+  *n_launches = moe::layout_launches(h->cfg, T);
+  if (prev != h->device) cudaSetDevice(prev);
+  return MOE_OK;
+}
+
 moe_status moe_w2_absorbed(const moe_handle* h, const void* d_h, int32_t I, const float* d_recv_w,
                            const void* d_w2, int32_t H, void* d_y, void* stream) {
   if (!h) return MOE_ERR_INVALID;

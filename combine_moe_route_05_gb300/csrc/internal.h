@@ -71,6 +71,7 @@ cudaError_t launch_scale_rows_bwd(const moe_handle* h, const void* ghs, const vo
                                   int dtype, const float* recv_w, void* gh, float* gw,
                                   cudaStream_t s);
 
+int layout_launches(const moe_config& c, int T);
 cudaError_t prepare_w2_kernel();
 bool w2_shape_ok(int I, int H);
 cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, const float* recv_w,

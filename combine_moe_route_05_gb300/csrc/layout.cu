@@ -565,6 +565,12 @@ cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T
   return cudaGetLastError();
 }
 
+int layout_launches(const moe_config& c, int T) {
+  const int cols = c.num_experts + c.num_ranks;
+  const size_t one_smem = scatter_smem(cols, c.top_k, c.num_ranks, true);
+  return layout_tiles(T) <= resident_single_pass_blocks(one_smem) ? 1 : 2;
+}
+
 cudaError_t launch_layout(const moe_handle* h, const int32_t* idx, int T, cudaStream_t s) {
   moe_layout out{};
   out.cnt_e = h->cnt_e;

@@ -215,6 +215,14 @@ moe_status moe_route_bwd(const moe_handle* h, const float* d_logits, const int32
 moe_status moe_dispatch_layout(moe_handle* h, const int32_t* d_idx, int32_t T, void* stream);
 
 /*
+ * Number of kernel launches moe_dispatch_layout makes for T tokens on the
+ * handle's device: 1 when all its 512-token tiles can be resident at once
+ * (a single cooperative launch), else 2.  Host-only query; *n_launches is
+ * written on MOE_OK.
+ */
+moe_status moe_dispatch_layout_launches(const moe_handle* h, int32_t T, int32_t* n_launches);
+
+/*
  * Allocation-free dispatch layout.  The web pages have no counterpart: this
  * entry point exists for callers that are not allowed to allocate device
  * memory, for example a plugin whose host framework hands it only its input

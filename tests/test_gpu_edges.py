@@ -61,6 +61,27 @@ def test_extremes_of_E_K_R(E, K, R, T):
         assert L.S == T * K
 
 
+@pytest.mark.parametrize("E,K,R,T", [(64, 4, 8, 4096), (16, 2, 4, 160000)])
+def test_layout_single_and_two_launch_paths(E, K, R, T):
+    """The layout runs as one cooperative launch when all its tiles fit on the
+    GPU at once and as two launches otherwise (here T = 160000: 313 tiles);
+    both give the oracle's layout bit for bit, twice in a row (the arrival
+    ticket and the epoch are reset / advanced correctly)."""
+    wl = synth.Workload("edge", T=T, H=64, E=E, K=K, R=R)
+    rng = np.random.default_rng(7)
+    idx = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int32)
+    r = router(wl)
+    n = moe.moe_dispatch_layout_launches(r.h, T)
+    assert n == (1 if T <= 4096 else 2)
+    L = oracle.layout(idx, E, R)
+    for _ in range(2):
+        r.layout(to_dev(idx))
+        got = layout_host(r)
+        for f in oracle.Layout.FIELDS:
+            assert np.array_equal(got[f].reshape(-1), getattr(L, f).reshape(-1)), f
+    assert moe.moe_read_device_status(r.h) == 0
+
+
 def test_empty_batch():
     wl, logits, x, y, g = small(16, 4, 4, 8)
     r = router(wl)
