@@ -126,7 +126,16 @@ def w2_absorbed_extra(device, stream, reps, tokens=None):
 
     t_fused = timed(lambda: moe.moe_w2_absorbed(r.h, hrows, recv_w, w2, y))
     t_unfused = timed(unfused)
+    # the absorption row on its own: scale_rows forward and backward
+    ghs = torch.randn(rows, I, device=device, generator=g).to(torch.bfloat16)
+    gh = torch.empty_like(hrows)
+    gws = torch.empty(T, K, dtype=torch.float32, device=device)
+    t_sr = timed(lambda: moe.moe_scale_rows(r.h, hrows, recv_w, hs))
+    t_srb = timed(lambda: moe.moe_scale_rows_bwd(r.h, ghs, hrows, recv_w, gh, gws))
     assert moe.moe_read_device_status(r.h) == 0
+    hbm_peak, hbm_src = read_peaks()
+    sr_bytes = rows * I * 2 * 2 + rows * 4
+    srb_bytes = rows * I * 2 * 3 + rows * 4 + T * K * 8
     same = bool(torch.equal(y, y_ref))
     flop = 2.0 * T * K * H * I
     peak, src = read_bf16_peak()
@@ -143,6 +152,10 @@ def w2_absorbed_extra(device, stream, reps, tokens=None):
                      "algorithmic_bytes": rows * I * 2 + E * H * I * 2 + rows * H * 2 + rows * 4,
                      "peak_source": src},
         "kernel_source": kernel_source_hash(W2_SOURCES),
+        "scale_rows": {"rows": rows, "I": I, "ms": t_sr, "gbs": sr_bytes / (t_sr / 1e3) / 1e9,
+                       "frac_of_hbm_peak": sr_bytes / (t_sr / 1e3) / 1e9 / hbm_peak},
+        "scale_rows_bwd": {"ms": t_srb, "gbs": srb_bytes / (t_srb / 1e3) / 1e9,
+                           "frac_of_hbm_peak": srb_bytes / (t_srb / 1e3) / 1e9 / hbm_peak},
     }
 
 
@@ -523,7 +536,7 @@ def run_gpu(args, wl):
         t_cp = time_op(lambda: moe.moe_combine_partial(h, y, w, partial))
         t_cr = time_op(lambda: moe.moe_combine_reduce(h, partial, out))
         S = int(moe.layout_tensors(h)["S"].item())
-        row = H * 2
+        row = H * (2 if wl.dtype == "bf16" else 4)
         extras = {
             "route_bwd": {"ms": t_rb, "gbs": (T * E * 4 + T * K * 12) / (t_rb / 1e3) / 1e9},
             "staged": {
@@ -536,6 +549,21 @@ def run_gpu(args, wl):
                 "combine_reduce_gbs": (S + T) * row / (t_cr / 1e3) / 1e9},
         }
         assert moe.moe_read_device_status(h) == 0
+        # the padded, capacity-aligned layout (segments rounded up to 128 rows)
+        rp = moe.MoeRouter(E, K, R, T, score_fn=wl.score_fn, num_groups=wl.n_groups,
+                           topk_groups=wl.topk_groups, group_score_topk=wl.group_score_topk,
+                           renorm=wl.renorm, route_scale=wl.route_scale, pad_align=128)
+        moe.moe_dispatch_layout(rp.h, idx)
+        recv_p = torch.empty(rp.h.recv_rows, H, dtype=rd, device=device)
+        recv_wp = torch.empty(rp.h.recv_rows, dtype=torch.float32, device=device)
+        t_lp = time_op(lambda: moe.moe_dispatch_layout(rp.h, idx))
+        t_dp = time_op(lambda: moe.moe_dispatch(rp.h, x, w, recv_p, recv_wp))
+        assert moe.moe_read_device_status(rp.h) == 0
+        extras["padded_layout"] = {
+            "pad_align": 128, "receive_rows": rp.h.recv_rows, "layout_ms": t_lp,
+            "dispatch_ms": t_dp,
+            "dispatch_gbs": (T * row + rp.h.recv_rows * row) / (t_dp / 1e3) / 1e9}
+        del recv_p, recv_wp
         extras["w2_absorbed"] = w2_absorbed_extra(device, stream, max(5, args.steps // 5),
                                                   tokens=args.tokens or None)
 
