@@ -277,19 +277,25 @@ __device__ __forceinline__ uint32_t load_send_entries(const StagedArgs& a, int t
 
 // recv[pos[t,k]] = send[send_row_of[t,k]]: each send row read once
 template <int KMAX>
-__global__ void __launch_bounds__(1024) expand_kernel(StagedArgs a) {
+__global__ void __launch_bounds__(kGatherMaxThreads) expand_kernel(StagedArgs a) {
   for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
     int p[KMAX], sr[KMAX];
     const uint32_t first = load_send_entries<KMAX>(a, t, p, sr);
     for (int v = threadIdx.x; v < a.nvec; v += blockDim.x) {
+      // all of the token's send-row loads first, so they are in flight
+      // together (the loads and stores are ordered asm statements)
+      Vec16 val[KMAX];
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if ((first >> k) & 1u)
+          val[k] = ld_stream(a.src + static_cast<int64_t>(sr[k]) * a.row_bytes + v * 16);
 #pragma unroll
       for (int k = 0; k < KMAX; ++k) {
         if (!((first >> k) & 1u)) continue;
-        const Vec16 val = ld_stream(a.src + static_cast<int64_t>(sr[k]) * a.row_bytes + v * 16);
 #pragma unroll
         for (int j = k; j < KMAX; ++j)
           if (sr[j] == sr[k] && p[j] >= 0)
-            st_vec(a.dst + static_cast<int64_t>(p[j]) * a.row_bytes + v * 16, val);
+            st_vec(a.dst + static_cast<int64_t>(p[j]) * a.row_bytes + v * 16, val[k]);
       }
     }
   }
@@ -647,8 +653,8 @@ cudaError_t launch_staged(int op, const moe_handle* h, const void* src, int H, i
   a.K = h->cfg.top_k;
   if (a.T == 0) return cudaSuccess;
   const bool k8 = a.K <= 8;
-  if (op == 0) {  // expand: one block per token, a thread per vector
-    const int block = threads_for(a.nvec, 1);
+  if (op == 0) {  // expand: one block per token, about two vectors per thread
+    const int block = gather_threads(a.nvec);
     const int grid = a.T < 1048576 ? a.T : 1048576;
     if (k8) expand_kernel<8><<<grid, block, 0, s>>>(a);
     else expand_kernel<16><<<grid, block, 0, s>>>(a);
