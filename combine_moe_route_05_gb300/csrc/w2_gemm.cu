@@ -17,7 +17,9 @@
 // TENSOR memory, so shared memory carries only the TMA landings, the
 // prologue's read of h and the tensor cores' read of W2.  Warp roles:
 //   warp 2      TMA: h slices [128 x 64] into a 3-stage ring (128-byte
-//               swizzle), freed as soon as the prologue has read them;
+//               swizzle), freed once the prologue has consumed them (after
+//               its tensor-memory store: the refill must not overtake the
+//               prologue's shared-memory loads);
 //   warp 0      TMA: W2 slices [256 x 64] into a 5-stage ring;
 //   warps 3-10  prologue: read an h slice (one row per thread, half of its K
 //               range per warp), scale it by the row's score (fp32 product,
