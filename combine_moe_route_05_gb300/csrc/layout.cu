@@ -62,11 +62,11 @@ struct LayoutArgs {
 
 __host__ __device__ constexpr int col_stride(int cols) { return cols | 1; }
 
-// Loads this thread's token (if any), validates it, keeps its row in
-// `idx_s` (if not null) and sets its bits in the tile's expert and rank masks.
+// Loads this thread's token (if any), validates it and sets its bits in the
+// tile's expert and rank masks.
 // Returns the valid-entry bitmask; ek holds the expert of each entry.
 __device__ __forceinline__ uint32_t mark_token(const LayoutArgs& a, int t, uint32_t* masks, int cp,
-                                               int* idx_s, int (&ek)[MOE_MAX_TOPK]) {
+                                               int (&ek)[MOE_MAX_TOPK]) {
   uint32_t valid = 0;
   if (t >= a.T) return 0;
   const int word = threadIdx.x >> 5;
@@ -78,7 +78,6 @@ __device__ __forceinline__ uint32_t mark_token(const LayoutArgs& a, int t, uint3
     if (k >= a.K) break;
     const int e = __ldg(row + k);
     ek[k] = e;
-    if (idx_s) idx_s[threadIdx.x * a.K + k] = e;
     bool ok = e >= 0 && e < a.E;
     if (!ok) bad |= MOE_DEVERR_BAD_EXPERT;
 #pragma unroll
@@ -172,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a)
   for (int i = threadIdx.x; i < kWords * cp; i += kThreads) masks[i] = 0;
   __syncthreads();
   int ek[MOE_MAX_TOPK];
-  mark_token(a, tile * kTile + threadIdx.x, masks, cp, nullptr, ek);
+  mark_token(a, tile * kTile + threadIdx.x, masks, cp, ek);
   __syncthreads();
   for (int col = threadIdx.x; col < cols; col += kThreads) {
     int c = 0;
@@ -273,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   __syncthreads();
   const int t = tile_t0 + threadIdx.x;
   int ek[MOE_MAX_TOPK];
-  const uint32_t valid = mark_token(a, t, masks, cp, nullptr, ek);
+  const uint32_t valid = mark_token(a, t, masks, cp, ek);
   __syncthreads();
   // exclusive prefix of the popcounts over the words of each column; the
   // column's count in this tile goes to seg (scanned below)
