@@ -47,18 +47,29 @@ W2_TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "w2_absorbed_qwen3_235b.md")
 
 
 def step_bytes(wl):
-    """Algorithmic HBM bytes of each stage of one step."""
+    """Algorithmic HBM bytes of each stage of one step.  With absorbed scores
+    the combine is a plain sum, its backward copies g (no score gradient
+    there), and scale_rows / scale_rows_bwd apply the scores to the W2 input
+    rows (I wide) and produce the score gradient."""
     T, H, E, K, R = wl.T, wl.H, wl.E, wl.K, wl.R
     eb = 2 if wl.dtype == "bf16" else 4
     row, tk = H * eb, T * K
-    return {
+    b = {
         "route_topk": T * E * 4 + (E * 4 if wl.bias == "normal" else 0) + tk * 8,
         "dispatch_layout": tk * 4 + 6 * tk * 4 + T * min(K, R) * 4,
         "dispatch": T * row + tk * row + tk * 4 * 3,
-        "combine": tk * row + T * row + tk * 8,
-        "combine_bwd": T * row + 2 * tk * row + tk * 12,
-        "dispatch_bwd": tk * row + T * row + tk * 4,
     }
+    if wl.absorb:
+        irow = wl.I * eb
+        b["scale_rows"] = 2 * tk * irow + tk * 4
+        b["combine"] = tk * row + T * row + tk * 4
+        b["combine_bwd"] = T * row + tk * row + tk * 4
+        b["scale_rows_bwd"] = 3 * tk * irow + tk * 4 + tk * 8
+    else:
+        b["combine"] = tk * row + T * row + tk * 8
+        b["combine_bwd"] = T * row + 2 * tk * row + tk * 12
+    b["dispatch_bwd"] = tk * row + T * row + tk * 4
+    return b
 
 
 def read_peaks():
@@ -278,15 +289,26 @@ def oracle_chain(wl, inp):
                                               wl.topk_groups, wl.group_score_topk, wl.renorm,
                                               wl.route_scale)
     L = oracle.layout(idx, wl.E, wl.R)
-    oracle.dispatch(inp["x"], L, w)
-    oracle.combine(inp["y"], L, w)
-    gy, _ = oracle.combine_bwd(inp["g"], inp["y"], L, w)
+    _, recv_w, _ = oracle.dispatch(inp["x"], L, w)
+    if wl.absorb:
+        oracle.scale_rows(inp["h"], recv_w)
+        oracle.combine(inp["y"], L)
+        gy, _ = oracle.combine_bwd(inp["g"], inp["y"], L)
+        oracle.scale_rows_bwd(inp["ghs"], inp["h"], recv_w, L)
+    else:
+        oracle.combine(inp["y"], L, w)
+        gy, _ = oracle.combine_bwd(inp["g"], inp["y"], L, w)
     oracle.dispatch_bwd(gy, L)
+
+
+def oracle_inputs(wl, seed):
+    want = ("logits", "bias", "x", "y", "g") + (("h", "ghs") if wl.absorb else ())
+    return synth.make_inputs(wl, seed=seed, want=want)
 
 
 def time_oracle(wl, tokens, reps=1):
     sub = wl.with_tokens(tokens)
-    inp = synth.make_inputs(sub, seed=wl.seed)
+    inp = oracle_inputs(sub, wl.seed)
     times = []
     for _ in range(reps):
         t0 = time.perf_counter()
@@ -312,7 +334,7 @@ def run_reference(args, wl):
     ob.build()
     tokens = args.ref_tokens
     sub = wl.with_tokens(tokens)
-    inp = synth.make_inputs(sub, seed=wl.seed)
+    inp = oracle_inputs(sub, wl.seed)
     for _ in range(args.warmup):
         oracle_chain(sub, inp)
     t0 = time.perf_counter()
@@ -362,7 +384,8 @@ def run_gpu(args, wl):
         dist.init_process_group("nccl", device_id=device)
 
     seed = replica_seed(wl.seed, rank, world)
-    inp = synth.make_inputs(wl, seed=seed, want=("logits", "bias", "x", "y", "g"))
+    want = ("logits", "bias", "x", "y", "g") + (("h", "ghs") if wl.absorb else ())
+    inp = synth.make_inputs(wl, seed=seed, want=want)
 
     def dev_tensor(a):
         if a is None:
@@ -377,6 +400,8 @@ def run_gpu(args, wl):
                       renorm=wl.renorm, route_scale=wl.route_scale)
     h = r.h
     logits, bias, x, y, g = (dev_tensor(inp[k]) for k in ("logits", "bias", "x", "y", "g"))
+    hrows = dev_tensor(inp["h"]) if wl.absorb else None
+    ghs = dev_tensor(inp["ghs"]) if wl.absorb else None
     bf = torch.bfloat16
     rd = bf if wl.dtype == "bf16" else torch.float32  # row dtype of the workload
     bits = (lambda t: t.view(torch.int16)) if rd == bf else (lambda t: t)
@@ -389,30 +414,40 @@ def run_gpu(args, wl):
     gw = torch.empty(T, K, dtype=torch.float32, device=device)
     gx = torch.empty(T, H, dtype=rd, device=device)
     stream = torch.cuda.current_stream()
-    names = ("route_topk", "dispatch_layout", "dispatch", "combine", "combine_bwd", "dispatch_bwd")
-    launches_per_step = 5 + moe.moe_dispatch_layout_launches(h, T)
+    if wl.absorb:
+        hs = torch.empty_like(hrows)
+        gh = torch.empty_like(hrows)
 
-    def step(ev=None, logits=logits, bias=bias, x=x, y=y, g=g):
+    def stages(logits, bias, x, y, g, h_in=None, ghs_in=None):
+        """The step's calls in order, as (name, call)."""
+        st = [("route_topk", lambda: moe.moe_route_topk(h, logits, bias, idx, w)),
+              ("dispatch_layout", lambda: moe.moe_dispatch_layout(h, idx)),
+              ("dispatch", lambda: moe.moe_dispatch(h, x, w, recv, recv_w))]
+        if wl.absorb:
+            # scores go into the W2 input; the W2 GEMM itself (y from hs) and
+            # its backward (ghs from g) sit between these calls and are not
+            # part of the path: y and ghs are synthetic inputs
+            st += [("scale_rows", lambda: moe.moe_scale_rows(h, h_in, recv_w, hs)),
+                   ("combine", lambda: moe.moe_combine(h, y, None, out)),
+                   ("combine_bwd", lambda: moe.moe_combine_bwd(h, g, y, None, gy, None)),
+                   ("scale_rows_bwd", lambda: moe.moe_scale_rows_bwd(h, ghs_in, h_in, recv_w, gh, gw))]
+        else:
+            st += [("combine", lambda: moe.moe_combine(h, y, w, out)),
+                   ("combine_bwd", lambda: moe.moe_combine_bwd(h, g, y, w, gy, gw))]
+        st.append(("dispatch_bwd", lambda: moe.moe_dispatch_bwd(h, gy, gx)))
+        return st
+
+    main_stages = stages(logits, bias, x, y, g, hrows, ghs)
+    names = tuple(n for n, _ in main_stages)
+    launches_per_step = len(main_stages) - 1 + moe.moe_dispatch_layout_launches(h, T)
+
+    def step(ev=None, st=main_stages):
+        for j, (_, call) in enumerate(st):
+            if ev is not None:
+                ev[j].record(stream)
+            call()
         if ev is not None:
-            ev[0].record(stream)
-        moe.moe_route_topk(h, logits, bias, idx, w)
-        if ev is not None:
-            ev[1].record(stream)
-        moe.moe_dispatch_layout(h, idx)
-        if ev is not None:
-            ev[2].record(stream)
-        moe.moe_dispatch(h, x, w, recv, recv_w)
-        if ev is not None:
-            ev[3].record(stream)
-        moe.moe_combine(h, y, w, out)
-        if ev is not None:
-            ev[4].record(stream)
-        moe.moe_combine_bwd(h, g, y, w, gy, gw)
-        if ev is not None:
-            ev[5].record(stream)
-        moe.moe_dispatch_bwd(h, gy, gx)
-        if ev is not None:
-            ev[6].record(stream)
+            ev[len(st)].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -427,7 +462,8 @@ def run_gpu(args, wl):
     if wl.bias == "zipf" and not args.tokens:
         assert load["max_over_mean"] > 5 and load["zero_load_experts"] == 1, load
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+           for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -451,8 +487,10 @@ def run_gpu(args, wl):
     e2e = None
     if not args.no_e2e:
         host_in = {k: torch.from_numpy(inp[k].view(np.int16) if inp[k].dtype == np.uint16 else inp[k])
-                   .pin_memory() for k in ("logits", "bias", "x", "y", "g") if inp[k] is not None}
+                   .pin_memory() for k in want if inp[k] is not None}
         dev_in = {"logits": logits, "bias": bias, "x": x, "y": y, "g": g}
+        if wl.absorb:
+            dev_in.update({"h": hrows, "ghs": ghs})
         host_out = {"idx": torch.empty(T, K, dtype=torch.int32).pin_memory(),
                     "w": torch.empty(T, K, dtype=torch.float32).pin_memory(),
                     "out": bits(torch.empty(T, H, dtype=rd)).pin_memory(),
@@ -467,6 +505,8 @@ def run_gpu(args, wl):
         # step i's outputs come back on a third stream
         dev_sets = [dev_in, {k: (torch.empty_like(v) if v is not None else None)
                              for k, v in dev_in.items()}]
+        set_stages = [stages(d["logits"], d["bias"], d["x"], d["y"], d["g"], d.get("h"), d.get("ghs"))
+                      for d in dev_sets]
         s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
         ev_in = [torch.cuda.Event(), torch.cuda.Event()]
         ev_comp = [torch.cuda.Event(), torch.cuda.Event()]
@@ -487,7 +527,7 @@ def run_gpu(args, wl):
                 stream.wait_event(ev_in[b])
                 if i >= 1:
                     stream.wait_event(ev_out)  # the previous outputs are read back
-                step(logits=din["logits"], bias=din["bias"], x=din["x"], y=din["y"], g=din["g"])
+                step(st=set_stages[b])
                 ev_comp[b].record(stream)
                 s_out.wait_event(ev_comp[b])
                 with torch.cuda.stream(s_out):
