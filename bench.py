@@ -36,7 +36,8 @@ METRIC = "dispatch+combine fwd+bwd tokens/s and achieved HBM GB/s (% of GB300 pe
 UNIT = "tokens/s"
 DOMINANT = "combine_bwd"
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e data-sheet bandwidth, for context beside the measured peak
-KERNEL_SOURCES = ("combine_moe_route_05_gb300/csrc/rows.cu", "combine_moe_route_05_gb300/csrc/common.cuh")
+KERNEL_SOURCES = ("combine_moe_route_05_gb300/csrc/rows.cu", "combine_moe_route_05_gb300/csrc/common.cuh",
+                  "combine_moe_route_05_gb300/csrc/router_grad.cuh")
 TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "combine_bwd_deepseek_v3.md")
 W2_SOURCES = ("combine_moe_route_05_gb300/csrc/w2_gemm.cu", "combine_moe_route_05_gb300/csrc/common.cuh")
 W2_TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "w2_absorbed_qwen3_235b.md")
@@ -569,6 +570,9 @@ def run_gpu(args, wl):
         step()
         glogits = torch.empty(T, E, dtype=torch.float32, device=device)
         t_rb = time_op(lambda: moe.moe_route_bwd(h, logits, idx, gw, glogits))
+        # the same router backward fused into the dispatch backward
+        t_db = time_op(lambda: moe.moe_dispatch_bwd(h, gy, gx))
+        t_dbr = time_op(lambda: moe.moe_dispatch_bwd_route(h, gy, logits, idx, gw, gx, glogits))
         send = torch.empty(T * min(K, R), H, dtype=rd, device=device)
         partial = torch.empty_like(send)
         t_ds = time_op(lambda: moe.moe_dispatch(h, x, w, recv, recv_w, send))
@@ -579,6 +583,9 @@ def run_gpu(args, wl):
         row = H * (2 if wl.dtype == "bf16" else 4)
         extras = {
             "route_bwd": {"ms": t_rb, "gbs": (T * E * 4 + T * K * 12) / (t_rb / 1e3) / 1e9},
+            "dispatch_bwd_route": {
+                "fused_ms": t_dbr, "dispatch_bwd_ms": t_db, "separate_ms": t_db + t_rb,
+                "launches": moe.moe_dispatch_bwd_route_launches(h)},
             "staged": {
                 "dedup_factor": T * K / S, "send_rows": S,
                 "dispatch_with_send_ms": t_ds, "expand_ms": t_ex, "combine_partial_ms": t_cp,

@@ -33,7 +33,8 @@ EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_handle_create", "moe
            "moe_combine", "moe_combine_bwd", "moe_dispatch_bwd", "moe_scale_rows",
            "moe_scale_rows_bwd", "moe_read_device_status", "moe_clear_device_status",
            "moe_dispatch_layout_static", "moe_route_bwd", "moe_expand", "moe_combine_partial",
-           "moe_combine_reduce", "moe_w2_absorbed", "moe_dispatch_layout_launches")
+           "moe_combine_reduce", "moe_w2_absorbed", "moe_dispatch_layout_launches",
+           "moe_dispatch_bwd_route", "moe_dispatch_bwd_route_launches")
 MOE_LAYOUT_STATIC_COUNTERS = 65536
 MOE_LAYOUT_TILE_TOKENS = 512
 
@@ -95,6 +96,8 @@ def lib():
             "moe_combine_reduce": ([P, P, i32, i32, P, P], st),
             "moe_w2_absorbed": ([P, P, i32, P, P, i32, P, P], st),
             "moe_dispatch_layout_launches": ([P, i32, P], st),
+            "moe_dispatch_bwd_route": ([P, P, i32, i32, P, P, P, P, P, P], st),
+            "moe_dispatch_bwd_route_launches": ([P, P], st),
         }
         for name, (args, res) in sigs.items():
             f = getattr(L, name)
@@ -286,6 +289,28 @@ def moe_dispatch_bwd(h, grecv, gx, stream=None):
                                                       _ptr(gx), _stream(stream)))
 
 
+def moe_dispatch_bwd_route(h, grecv, logits, idx, gw, gx, glogits, stream=None):
+    H = grecv.shape[1]
+    _req(grecv, None, (h.recv_rows, H), "grecv")
+    _req(logits, torch.float32, (h.T, h.E), "logits")
+    _req(idx, torch.int32, (h.T, h.K), "idx")
+    _req(gw, torch.float32, (h.T, h.K), "gw")
+    _req(gx, grecv.dtype, (h.T, H), "gx")
+    _req(glogits, torch.float32, (h.T, h.E), "glogits")
+    _check("moe_dispatch_bwd_route",
+           lib().moe_dispatch_bwd_route(h.ptr, _ptr(grecv), H, _row_dtype(grecv), _ptr(logits),
+                                        _ptr(idx), _ptr(gw), _ptr(gx), _ptr(glogits),
+                                        _stream(stream)))
+
+
+def moe_dispatch_bwd_route_launches(h):
+    """Kernel launches moe_dispatch_bwd_route makes for the handle's routing."""
+    n = ctypes.c_int32(0)
+    _check("moe_dispatch_bwd_route_launches",
+           lib().moe_dispatch_bwd_route_launches(h.ptr, ctypes.byref(n)))
+    return n.value
+
+
 def moe_expand(h, send, recv, stream=None):
     H = send.shape[1]
     _req(send, None, (h.T * min(h.K, h.R), H), "send")
@@ -459,6 +484,14 @@ class MoeRouter:
         gx = torch.empty(max(self.h.T, 0), grecv.shape[1], dtype=grecv.dtype, device=grecv.device)
         moe_dispatch_bwd(self.h, grecv, gx, stream)
         return gx
+
+    def dispatch_bwd_route(self, grecv, logits, idx, gw, stream=None):
+        """Dispatch backward and router backward to the logits in one call:
+        (gx, glogits)."""
+        gx = torch.empty(max(self.h.T, 0), grecv.shape[1], dtype=grecv.dtype, device=grecv.device)
+        glogits = torch.empty(max(self.h.T, 0), self.h.E, dtype=torch.float32, device=grecv.device)
+        moe_dispatch_bwd_route(self.h, grecv, logits, idx, gw, gx, glogits, stream)
+        return gx, glogits
 
     def expand(self, send, stream=None):
         recv = torch.empty(max(self.h.recv_rows, 0), send.shape[1], dtype=send.dtype,

@@ -279,6 +279,26 @@ moe_status moe_dispatch_bwd(const moe_handle* h, const void* d_grecv, int32_t H,
   return from_cuda(moe::launch_combine(h, d_grecv, H, dtype, nullptr, d_gx, as_stream(stream)));
 }
 
+moe_status moe_dispatch_bwd_route(const moe_handle* h, const void* d_grecv, int32_t H,
+                                  int32_t dtype, const float* d_logits, const int32_t* d_idx,
+                                  const float* d_gw, void* d_gx, float* d_glogits, void* stream) {
+  if (!h) return MOE_ERR_INVALID;
+  if (h->T < 0) return MOE_ERR_STATE;
+  if (h->T == 0) return empty_rows_ok(H, dtype) ? MOE_OK : MOE_ERR_INVALID;
+  if (!row_ok(d_grecv, H, dtype) || !row_ok(d_gx, H, dtype)) return MOE_ERR_INVALID;
+  if (!d_logits || !d_idx || !d_gw || !d_glogits) return MOE_ERR_INVALID;
+  if (!aligned(d_logits, 4) || !aligned(d_idx, 4) || !aligned(d_gw, 4) || !aligned(d_glogits, 4))
+    return MOE_ERR_INVALID;
+  return from_cuda(moe::launch_dispatch_bwd_route(h, d_grecv, H, dtype, d_logits, d_idx, d_gw,
+                                                  d_gx, d_glogits, as_stream(stream)));
+}
+
+moe_status moe_dispatch_bwd_route_launches(const moe_handle* h, int32_t* n_launches) {
+  if (!h || !n_launches) return MOE_ERR_INVALID;
+  *n_launches = moe::dispatch_bwd_route_launches(h->cfg);
+  return MOE_OK;
+}
+
 moe_status moe_expand(const moe_handle* h, const void* d_send, int32_t H, int32_t dtype,
                       void* d_recv, void* stream) {
   if (!h) return MOE_ERR_INVALID;

@@ -55,6 +55,25 @@ cudaError_t launch_combine(const moe_handle* h, const void* y, int H, int dtype,
 cudaError_t launch_combine_bwd(const moe_handle* h, const void* g, const void* y, int H, int dtype,
                                const float* w, void* gy, float* gw, cudaStream_t s);
 
+// Router inputs and output of the dispatch backward with the router backward
+// to the logits fused in (softmax with renormalisation or sigmoid).
+struct RouterBwdRows {
+  const float* logits;  // [T, E]
+  const int32_t* idx;   // [T, K]
+  const float* gw;      // [T, K], complete
+  float* glogits;       // [T, E]
+};
+
+// dispatch backward (unit-weight combine of grecv into gx) and router
+// backward in one launch when the configuration allows it (every routing but
+// softmax without renormalisation), else the two kernels back to back
+cudaError_t launch_dispatch_bwd_route(const moe_handle* h, const void* grecv, int H, int dtype,
+                                      const float* logits, const int32_t* idx, const float* gw,
+                                      void* gx, float* glogits, cudaStream_t s);
+
+// launches launch_dispatch_bwd_route makes (1 or 2) for the handle's routing
+int dispatch_bwd_route_launches(const moe_config& c);
+
 // op 0: expand send rows to receive rows; 1: combine into per-send-row
 // partials; 2: reduce the partials to token rows
 cudaError_t launch_staged(int op, const moe_handle* h, const void* src, int H, int dtype,

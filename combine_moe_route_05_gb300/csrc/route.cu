@@ -33,6 +33,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "router_grad.cuh"
 
 namespace moe {
 namespace {
@@ -623,21 +624,12 @@ void launch_one(const RouteArgs& a, int num_sms, size_t smem, cudaStream_t s) {
 }
 
 // ---------------------------------------------------------------------------
-// Router backward to the logits (DeepSpeed "Avoid collective token preparation
-// for AutoEP DeepEP", "Testing Done": routing-score and router-parameter
-// gradients).  With the selection fixed, the weights are
-//   softmax, renorm:     w_k = c q_k,   q_k = exp(l_k) / sum_{j in sel} exp(l_j)
-//   softmax, no renorm:  w_k = c p_k,   p = softmax(l) over all E
-//   sigmoid, renorm:     w_k = c s_k / S,  S = sum_{j in sel} s_j
-//   sigmoid, no renorm:  w_k = c s_k
-// (the correction bias selects only and gets no gradient), so
-//   softmax renorm:     dL/dl_j = c q_j (gw_j - sum_k q_k gw_k)
-//   softmax no renorm:  dL/dl_e = c p_e (gw_e - sum_k p_k gw_k)   (every e)
-//   sigmoid renorm:     dL/dl_j = s_j (1 - s_j) (c / S) (gw_j - sum_k gw_k s_k / S)
-//   sigmoid no renorm:  dL/dl_j = c gw_j s_j (1 - s_j)
-// computed in fp64 with sums in k order, rounded once to fp32; every other
-// entry of the row is 0.  Lane j*K + k handles entry k of token j, TB = 32/K
-// tokens per warp pass.
+// Router backward to the logits: the per-entry derivative is
+// router_grad_entry (router_grad.cuh), rounded once to fp32; every other entry
+// of the row is 0.  Lane j*K + k handles entry k of token j, TB = 32/K tokens
+// per warp pass.  Softmax without renormalisation moves every logit of the
+// row, dL/dl_e = c p_e (gw_e - sum_k p_k gw_k) with p the full softmax and
+// gw_e = 0 for unselected e; it has its own kernel below.
 
 struct RouteBwdArgs {
   const float* logits;
@@ -680,28 +672,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_bwd_kernel(RouteBwdArg
       g = static_cast<double>(__ldg(a.gw + static_cast<size_t>(t) * a.K + k));
     }
     const int b = (j * a.K) & 31;  // lane of entry 0 of this token
-    double out;
-    if (!a.sigmoid) {
-      const double lmax = __shfl_sync(kFull, l, b);
-      const double ex = exp(l - lmax);
-      double den = 0.0;
-      for (int kk = 0; kk < a.K; ++kk) den += __shfl_sync(kFull, ex, (b + kk) & 31);
-      const double q = ex / den;
-      double dot = 0.0;
-      for (int kk = 0; kk < a.K; ++kk) dot += __shfl_sync(kFull, q * g, (b + kk) & 31);
-      out = a.scale * q * (g - dot);
-    } else {
-      const double sg = 1.0 / (1.0 + exp(-l));
-      if (a.renorm) {
-        double S = 0.0;
-        for (int kk = 0; kk < a.K; ++kk) S += __shfl_sync(kFull, sg, (b + kk) & 31);
-        double dot = 0.0;
-        for (int kk = 0; kk < a.K; ++kk) dot += __shfl_sync(kFull, g * sg / S, (b + kk) & 31);
-        out = sg * (1.0 - sg) * (a.scale / S) * (g - dot);
-      } else {
-        out = a.scale * g * sg * (1.0 - sg);
-      }
-    }
+    const double out = router_grad_entry(l, g, b, a.K, a.sigmoid, a.renorm, a.scale);
     __syncwarp();  // the zero fill above is ordered before these writes
     if (valid) a.glogits[static_cast<size_t>(t) * a.E + e] = static_cast<float>(out);
     __syncwarp();

@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "router_grad.cuh"
 
 namespace moe {
 namespace {
@@ -97,6 +98,13 @@ struct RowArgs {
   int64_t row_bytes;
   int nvec;           // 16-byte vectors per row
   int T, K;
+  // router backward fused into the dispatch backward (else unused)
+  const float* logits;  // [T, E]
+  const int32_t* idx;   // [T, K]
+  float* glogits;       // [T, E]
+  int E;
+  int sigmoid, renorm, vec4_e;
+  double scale;
 };
 
 template <int KMAX>
@@ -113,11 +121,65 @@ __device__ __forceinline__ void load_entries(const int32_t* pos, const float* w,
   }
 }
 
-template <typename Elt, int KMAX, bool WEIGHTED>
-__global__ void __launch_bounds__(kGatherMaxThreads) combine_kernel(RowArgs<Elt> a) {
+// Router backward to the logits for TB = 32/K tokens of this block, its
+// tokens j0 .. j0+TB-1 (t = blockIdx.x + j*gridDim.x, j < ntok), by one warp:
+// lane jj*K + k takes entry k of token j0 + jj.  The tokens' rows of glogits
+// are zeroed, then their K entries written (router_grad_entry: fp64, rounded
+// once), from the complete score gradient gw.
+template <typename Elt>
+__device__ __noinline__ void router_bwd_pass(const RowArgs<Elt>& a, int j0, int ntok) {
+  const int lane = threadIdx.x & 31;
+  const int TB = 32 / a.K;
+  const int jj = lane / a.K, k = lane % a.K;
+  for (int u = 0; u < TB && j0 + u < ntok; ++u) {
+    float* row = a.glogits + static_cast<size_t>(blockIdx.x + (j0 + u) * gridDim.x) * a.E;
+    if (a.vec4_e) {
+      for (int e = lane * 4; e < a.E; e += 128)
+        *reinterpret_cast<float4*>(row + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      for (int e = lane; e < a.E; e += 32) row[e] = 0.f;
+    }
+  }
+  const int j = j0 + jj;
+  const bool valid = jj < TB && j < ntok;
+  const int t = blockIdx.x + j * gridDim.x;
+  int e = 0;
+  double l = 0.0, g = 0.0;
+  if (valid) {
+    const size_t tk = static_cast<size_t>(t) * a.K + k;
+    e = __ldg(a.idx + tk);
+    if (e < 0 || e >= a.E) e = 0;  // as the separate router backward
+    l = static_cast<double>(__ldg(a.logits + static_cast<size_t>(t) * a.E + e));
+    g = static_cast<double>(__ldg(a.gw + tk));
+  }
+  const double d = router_grad_entry(l, g, (jj * a.K) & 31, a.K, a.sigmoid != 0, a.renorm != 0,
+                                     a.scale);
+  __syncwarp();  // the zero fill above is ordered before these writes
+  if (valid) a.glogits[static_cast<size_t>(t) * a.E + e] = static_cast<float>(d);
+}
+
+// combine: out[t] = round(sum_k w_k y[pos[t,k]]) (or the plain sum) in fp32,
+// k in order.  ROUTE (the dispatch backward with the router backward fused
+// in) also runs the router backward of the block's tokens, TB = 32/K tokens
+// per pass, each pass by the next warp in turn before its rows of the pass's
+// first token: there is no barrier between the warps, so the fp64 latency of
+// a pass hides behind the other warps' row traffic.
+template <typename Elt, int KMAX, bool WEIGHTED, bool ROUTE>
+__device__ __forceinline__ void combine_body(const RowArgs<Elt>& a) {
   using VT = VecTraits<Elt>;
   constexpr int N = VT::N;
-  for (int t = blockIdx.x; t < a.T; t += gridDim.x) {
+  int ntok = 0, TB = 1, nw = 1;
+  if (ROUTE) {
+    ntok = a.T > static_cast<int>(blockIdx.x)
+               ? (a.T - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+               : 0;
+    TB = 32 / a.K;
+    nw = blockDim.x >> 5;
+  }
+  int it = 0;
+  for (int t = blockIdx.x; t < a.T; t += gridDim.x, ++it) {
+    if (ROUTE && it % TB == 0 && static_cast<int>(threadIdx.x >> 5) == (it / TB) % nw)
+      router_bwd_pass(a, it, ntok);
     int p[KMAX];
     float wk[KMAX];
     load_entries<KMAX>(a.pos, WEIGHTED ? a.w : nullptr, t, a.K, p, wk);
@@ -144,60 +206,85 @@ __global__ void __launch_bounds__(kGatherMaxThreads) combine_kernel(RowArgs<Elt>
   }
 }
 
-// combine backward: gy[pos[t,k]] = round(w_k * g[t]) (or g[t]), and
-// gw[t,k] = <g[t], y[pos[t,k]]> reduced over the block in a fixed order.
+template <typename Elt, int KMAX, bool WEIGHTED>
+__global__ void __launch_bounds__(kGatherMaxThreads) combine_kernel(RowArgs<Elt> a) {
+  combine_body<Elt, KMAX, WEIGHTED, false>(a);
+}
+
+// the dispatch backward with the router backward fused in: two blocks per SM
+// (the row loop's occupancy), the router pass out of line
+template <typename Elt, int KMAX>
+__global__ void __launch_bounds__(kGatherMaxThreads, 2) dispatch_bwd_route_kernel(RowArgs<Elt> a) {
+  combine_body<Elt, KMAX, false, true>(a);
+}
+
+// One token of the combine backward for the row threads tid = 0 .. nthr-1 of
+// the block: gy[pos[t,k]] = round(w_k * g[t]) (or g[t]) for its 16-byte
+// vectors v = tid, tid + nthr, ..., and (DOT) its fp32 partial dot products
+// <g[t], y[pos[t,k]]> over those vectors, reduced across the warp.
 template <typename Elt, int KMAX, bool WEIGHTED, bool DOT>
-__global__ void __launch_bounds__(kGatherMaxThreads, 2) combine_bwd_kernel(RowArgs<Elt> a) {
+__device__ __forceinline__ void combine_bwd_token(const RowArgs<Elt>& a, int t, int tid, int nthr,
+                                                  float (&dot)[KMAX]) {
   using VT = VecTraits<Elt>;
   constexpr int N = VT::N;
+  int p[KMAX];
+  float wk[KMAX];
+  load_entries<KMAX>(a.pos, WEIGHTED ? a.w : nullptr, t, a.K, p, wk);
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) dot[k] = 0.0f;
+  const uint8_t* grow = a.g + static_cast<int64_t>(t) * a.row_bytes;
+  for (int v = tid; v < a.nvec; v += nthr) {
+    const Vec16 gv = ld_stream(grow + v * 16);
+    Vec16 yv[KMAX];
+    if (DOT) {
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if (p[k] >= 0) yv[k] = ld_stream(a.y + static_cast<int64_t>(p[k]) * a.row_bytes + v * 16);
+    }
+    float gf[N];
+    VT::to_f32(gv, gf);
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      if (p[k] < 0) continue;
+      uint8_t* dst = a.out + static_cast<int64_t>(p[k]) * a.row_bytes + v * 16;
+      if (WEIGHTED) {
+        float o[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) o[i] = __fmul_rn(wk[k], gf[i]);
+        st_vec(dst, VT::from_f32(o));
+      } else {
+        st_vec(dst, gv);
+      }
+      if (DOT) {
+        float yf[N];
+        VT::to_f32(yv[k], yf);
+#pragma unroll
+        for (int i = 0; i < N; ++i) dot[k] = __fmaf_rn(gf[i], yf[i], dot[k]);
+      }
+    }
+  }
+  if (DOT) {
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dot[k] += __shfl_xor_sync(kFull, dot[k], off);
+    }
+  }
+}
+
+// combine backward: gy[pos[t,k]] = round(w_k * g[t]) (or g[t]), and
+// gw[t,k] = <g[t], y[pos[t,k]]> reduced over the block in a fixed order
+// (warp partials summed in warp order).
+template <typename Elt, int KMAX, bool WEIGHTED, bool DOT>
+__global__ void __launch_bounds__(kGatherMaxThreads, 2) combine_bwd_kernel(RowArgs<Elt> a) {
   __shared__ float red[2][kGatherMaxThreads / 32][KMAX];
   const int nw = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int it = 0;
   for (int t = blockIdx.x; t < a.T; t += gridDim.x, ++it) {
-    int p[KMAX];
-    float wk[KMAX];
-    load_entries<KMAX>(a.pos, WEIGHTED ? a.w : nullptr, t, a.K, p, wk);
     float dot[KMAX];
-#pragma unroll
-    for (int k = 0; k < KMAX; ++k) dot[k] = 0.0f;
-    const uint8_t* grow = a.g + static_cast<int64_t>(t) * a.row_bytes;
-    for (int v = threadIdx.x; v < a.nvec; v += blockDim.x) {
-      const Vec16 gv = ld_stream(grow + v * 16);
-      Vec16 yv[KMAX];
-      if (DOT) {
-#pragma unroll
-        for (int k = 0; k < KMAX; ++k)
-          if (p[k] >= 0) yv[k] = ld_stream(a.y + static_cast<int64_t>(p[k]) * a.row_bytes + v * 16);
-      }
-      float gf[N];
-      VT::to_f32(gv, gf);
-#pragma unroll
-      for (int k = 0; k < KMAX; ++k) {
-        if (p[k] < 0) continue;
-        uint8_t* dst = a.out + static_cast<int64_t>(p[k]) * a.row_bytes + v * 16;
-        if (WEIGHTED) {
-          float o[N];
-#pragma unroll
-          for (int i = 0; i < N; ++i) o[i] = __fmul_rn(wk[k], gf[i]);
-          st_vec(dst, VT::from_f32(o));
-        } else {
-          st_vec(dst, gv);
-        }
-        if (DOT) {
-          float yf[N];
-          VT::to_f32(yv[k], yf);
-#pragma unroll
-          for (int i = 0; i < N; ++i) dot[k] = __fmaf_rn(gf[i], yf[i], dot[k]);
-        }
-      }
-    }
+    combine_bwd_token<Elt, KMAX, WEIGHTED, DOT>(a, t, threadIdx.x, blockDim.x, dot);
     if (DOT) {
-#pragma unroll
-      for (int k = 0; k < KMAX; ++k) {
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) dot[k] += __shfl_xor_sync(kFull, dot[k], off);
-      }
       if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < KMAX; ++k) red[it & 1][warp][k] = dot[k];
@@ -482,7 +569,7 @@ int gather_threads(int nvec) {
 
 template <typename Elt, int KMAX>
 cudaError_t launch_combine_t(const moe_handle* h, const void* y, int H, const float* w, void* out,
-                             cudaStream_t s) {
+                             cudaStream_t s, const RouterBwdRows* rt = nullptr) {
   RowArgs<Elt> a{};
   a.y = static_cast<const uint8_t*>(y);
   a.w = w;
@@ -494,7 +581,19 @@ cudaError_t launch_combine_t(const moe_handle* h, const void* y, int H, const fl
   a.K = h->cfg.top_k;
   if (a.T == 0) return cudaSuccess;
   const int block = gather_threads(a.nvec);
-  if (w) {
+  if (rt) {
+    a.logits = rt->logits;
+    a.idx = rt->idx;
+    a.gw = const_cast<float*>(rt->gw);
+    a.glogits = rt->glogits;
+    a.E = h->cfg.num_experts;
+    a.sigmoid = h->cfg.score_fn == MOE_SCORE_SIGMOID;
+    a.renorm = h->cfg.renorm;
+    a.scale = h->cfg.route_scale;
+    a.vec4_e = (a.E % 4) == 0 && (reinterpret_cast<uintptr_t>(rt->glogits) & 15) == 0;
+    auto k = dispatch_bwd_route_kernel<Elt, KMAX>;
+    k<<<grid_for(reinterpret_cast<const void*>(k), block, 0, h->num_sms, a.T), block, 0, s>>>(a);
+  } else if (w) {
     auto k = combine_kernel<Elt, KMAX, true>;
     k<<<grid_for(reinterpret_cast<const void*>(k), block, 0, h->num_sms, a.T), block, 0, s>>>(a);
   } else {
@@ -590,6 +689,26 @@ cudaError_t launch_combine_bwd(const moe_handle* h, const void* g, const void* y
               : launch_combine_bwd_t<__nv_bfloat16, 16>(h, g, y, H, w, gy, gw, s);
   return k8 ? launch_combine_bwd_t<float, 8>(h, g, y, H, w, gy, gw, s)
             : launch_combine_bwd_t<float, 16>(h, g, y, H, w, gy, gw, s);
+}
+
+int dispatch_bwd_route_launches(const moe_config& c) {
+  return c.score_fn == MOE_SCORE_SOFTMAX && !c.renorm ? 2 : 1;
+}
+
+cudaError_t launch_dispatch_bwd_route(const moe_handle* h, const void* grecv, int H, int dtype,
+                                      const float* logits, const int32_t* idx, const float* gw,
+                                      void* gx, float* glogits, cudaStream_t s) {
+  if (dispatch_bwd_route_launches(h->cfg) == 2) {
+    const cudaError_t e = launch_combine(h, grecv, H, dtype, nullptr, gx, s);
+    return e != cudaSuccess ? e : launch_route_bwd(h, logits, idx, gw, h->T, glogits, s);
+  }
+  const RouterBwdRows rt{logits, idx, gw, glogits};
+  const bool k8 = h->cfg.top_k <= 8;
+  if (dtype == MOE_BF16)
+    return k8 ? launch_combine_t<__nv_bfloat16, 8>(h, grecv, H, nullptr, gx, s, &rt)
+              : launch_combine_t<__nv_bfloat16, 16>(h, grecv, H, nullptr, gx, s, &rt);
+  return k8 ? launch_combine_t<float, 8>(h, grecv, H, nullptr, gx, s, &rt)
+            : launch_combine_t<float, 16>(h, grecv, H, nullptr, gx, s, &rt);
 }
 
 cudaError_t launch_scale_rows(const moe_handle* h, const void* hrows, int I, int dtype,

@@ -304,6 +304,31 @@ moe_status moe_dispatch_bwd(const moe_handle* h, const void* d_grecv, int32_t H,
                             void* d_gx, void* stream);
 
 /*
+ * Dispatch backward with the router backward to the logits fused in
+ * ([AutoEP-prep] "Testing Done": router-parameter gradients): computes
+ * exactly what moe_dispatch_bwd and moe_route_bwd compute, bit for bit, in
+ * one launch:
+ *   d_gx [T,H]           as moe_dispatch_bwd(d_grecv);
+ *   d_glogits [T,E] fp32 as moe_route_bwd(d_logits, d_idx, d_gw),
+ * where d_gw [T,K] is the complete router-score gradient (moe_combine_bwd or
+ * moe_scale_rows_bwd, earlier on the stream) and d_logits [T,E], d_idx [T,K]
+ * the forward routing's logits and selection, for the T of the handle's
+ * layout.  The router's fp64 work runs beside the row traffic of the
+ * dispatch backward, which has no cross-warp dependency (the combine
+ * backward would hold it behind its per-token reduction).  Softmax routing
+ * without renormalisation moves every logit of the row and runs as the two
+ * separate kernels (moe_dispatch_bwd_route_launches says which).  All
+ * pointers are required.
+ */
+moe_status moe_dispatch_bwd_route(const moe_handle* h, const void* d_grecv, int32_t H,
+                                  int32_t dtype, const float* d_logits, const int32_t* d_idx,
+                                  const float* d_gw, void* d_gx, float* d_glogits, void* stream);
+
+/* Launches moe_dispatch_bwd_route makes for the handle's routing: 1, or 2 for
+ * softmax without renormalisation.  Host-only query. */
+moe_status moe_dispatch_bwd_route_launches(const moe_handle* h, int32_t* n_launches);
+
+/*
  * Staged (wire-faithful) mode ([AutoEP-DeepEP] "Why": a token is sent once
  * per destination rank rather than once per selected expert, the receiving
  * side groups arrivals by expert, and the combine brings back one reduced row
