@@ -62,22 +62,38 @@ struct LayoutArgs {
 
 __host__ __device__ constexpr int col_stride(int cols) { return cols | 1; }
 
-// Loads this thread's token (if any), validates it and sets its bits in the
-// tile's expert and rank masks.
-// Returns the valid-entry bitmask; ek holds the expert of each entry.
+// Fills rank_of[e] = e / epr (shared memory, all threads of the block).
+__device__ __forceinline__ void fill_rank_table(const LayoutArgs& a, int32_t* rank_of) {
+  for (int e = threadIdx.x; e < a.E; e += blockDim.x) rank_of[e] = e / a.epr;
+}
+
+// Loads the experts of this thread's token t (if t < T) into ek; issued
+// before the shared-memory set-up so that its latency overlaps it.
+__device__ __forceinline__ void load_token(const LayoutArgs& a, int t, int (&ek)[MOE_MAX_TOPK]) {
+  if (t >= a.T) return;
+  const int32_t* row = a.idx + static_cast<size_t>(t) * a.K;
+#pragma unroll
+  for (int k = 0; k < MOE_MAX_TOPK; ++k) {
+    if (k >= a.K) break;
+    ek[k] = __ldg(row + k);
+  }
+}
+
+// Validates this thread's token t (experts in ek, from load_token) and sets
+// its bits in the tile's expert and rank masks (rank_of: the expert -> rank
+// table).  Returns the valid-entry bitmask.
 __device__ __forceinline__ uint32_t mark_token(const LayoutArgs& a, int t, uint32_t* masks, int cp,
-                                               int (&ek)[MOE_MAX_TOPK]) {
+                                               const int32_t* rank_of,
+                                               const int (&ek)[MOE_MAX_TOPK]) {
   uint32_t valid = 0;
   if (t >= a.T) return 0;
   const int word = threadIdx.x >> 5;
   const uint32_t bit = 1u << (threadIdx.x & 31);
-  const int32_t* row = a.idx + static_cast<size_t>(t) * a.K;
   uint32_t bad = 0;
 #pragma unroll
   for (int k = 0; k < MOE_MAX_TOPK; ++k) {
     if (k >= a.K) break;
-    const int e = __ldg(row + k);
-    ek[k] = e;
+    const int e = ek[k];
     bool ok = e >= 0 && e < a.E;
     if (!ok) bad |= MOE_DEVERR_BAD_EXPERT;
 #pragma unroll
@@ -91,18 +107,77 @@ __device__ __forceinline__ uint32_t mark_token(const LayoutArgs& a, int t, uint3
     if (ok) {
       valid |= 1u << k;
       atomicOr(&masks[word * cp + e], bit);
-      atomicOr(&masks[word * cp + a.E + e / a.epr], bit);
+      atomicOr(&masks[word * cp + a.E + rank_of[e]], bit);
     }
   }
   if (bad) raise_flag(a.flags, bad);
   return valid;
 }
 
-// The last block to arrive: exclusive scan of each column over the tiles (in
-// place in tile_hist), then exclusive scans over experts and over ranks into
-// the count and offset arrays.  `tot` is [E + R] shared-memory scratch.
-__device__ void scan_tiles(const LayoutArgs& a, int32_t* tot) {
+// Exclusive scans of the column totals, tot[0, E) (expert segments rounded up
+// to the padding) and tot[E, E + R) (ranks), into off_e[0..E] and off_s[0..R]
+// (shared memory; warp 0 scans the experts, warp 1 the ranks).  With
+// `publish`, also writes the layout's count and offset arrays and S.  Ends
+// with a barrier.
+__device__ void scan_totals(const LayoutArgs& a, const int32_t* tot, int32_t* off_e, int32_t* off_s,
+                            bool publish) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < 2) {
+    const int n = warp == 0 ? a.E : a.R;
+    const int32_t* src = tot + (warp == 0 ? 0 : a.E);
+    int32_t* off = warp == 0 ? off_e : off_s;
+    int32_t* cnt_g = warp == 0 ? a.cnt_e : a.cnt_send_r;
+    int32_t* off_g = warp == 0 ? a.off_e : a.off_send_r;
+    // expert segments are rounded up to the padding; rank counts are not
+    const int pad = warp == 0 ? a.pad : 1;
+    const int per = (n + 31) / 32;
+    const int lo = lane * per, hi = min(n, lo + per);
+    int local = 0;
+    for (int i = lo; i < hi; ++i) local += (src[i] + pad - 1) / pad * pad;
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    int run = incl - local;
+    for (int i = lo; i < hi; ++i) {
+      off[i] = run;
+      if (publish) {
+        cnt_g[i] = src[i];
+        off_g[i] = run;
+      }
+      run += (src[i] + pad - 1) / pad * pad;
+    }
+    const int total = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 0) {
+      off[n] = total;
+      if (publish) {
+        off_g[n] = total;
+        if (warp == 1) *a.S = total;
+      }
+    }
+  }
+  __syncthreads();
+  if (publish) {
+    for (int r = threadIdx.x; r < a.R; r += blockDim.x) {
+      // rows that arrive at rank r (pads excluded); its region starts at the
+      // padded offset of its first expert
+      int n = 0;
+      for (int e = r * a.epr; e < (r + 1) * a.epr; ++e) n += tot[e];
+      a.off_recv_r[r] = off_e[r * a.epr];
+      a.cnt_recv_r[r] = n;
+    }
+    if (threadIdx.x == 0) a.off_recv_r[a.R] = off_e[a.E];
+  }
+}
+
+// The last block of the two-launch path: exclusive scan of each column over
+// the tiles (in place in tile_hist), then the scans of the column totals.
+// `scratch`: 2 (E + R) + 2 ints of shared memory.
+__device__ void scan_tiles(const LayoutArgs& a, int32_t* scratch) {
   const int cols = a.E + a.R;
+  int32_t* tot = scratch;
   for (int col = threadIdx.x; col < cols; col += kThreads) {
     int run = 0;
     for (int t0 = 0; t0 < a.ntiles; t0 += 16) {
@@ -119,47 +194,7 @@ __device__ void scan_tiles(const LayoutArgs& a, int32_t* tot) {
     tot[col] = run;
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < 2) {
-    // warp 0 scans the E expert totals, warp 1 the R rank totals
-    const int n = warp == 0 ? a.E : a.R;
-    const int32_t* src = tot + (warp == 0 ? 0 : a.E);
-    int32_t* cnt = warp == 0 ? a.cnt_e : a.cnt_send_r;
-    int32_t* off = warp == 0 ? a.off_e : a.off_send_r;
-    // expert segments are rounded up to the padding; rank counts are not
-    const int pad = warp == 0 ? a.pad : 1;
-    const int per = (n + 31) / 32;
-    const int lo = lane * per, hi = min(n, lo + per);
-    int local = 0;
-    for (int i = lo; i < hi; ++i) local += (src[i] + pad - 1) / pad * pad;
-    int incl = local;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += o;
-    }
-    int run = incl - local;
-    for (int i = lo; i < hi; ++i) {
-      cnt[i] = src[i];
-      off[i] = run;
-      run += (src[i] + pad - 1) / pad * pad;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    if (lane == 0) {
-      off[n] = total;
-      if (warp == 1) *a.S = total;
-    }
-  }
-  __syncthreads();
-  for (int r = threadIdx.x; r < a.R; r += kThreads) {
-    // rows that arrive at rank r (pads excluded); its region starts at the
-    // padded offset of its first expert
-    int n = 0;
-    for (int e = r * a.epr; e < (r + 1) * a.epr; ++e) n += tot[e];
-    a.off_recv_r[r] = a.off_e[r * a.epr];
-    a.cnt_recv_r[r] = n;
-  }
-  if (threadIdx.x == 0) a.off_recv_r[a.R] = a.off_e[a.E];
+  scan_totals(a, tot, scratch + cols, scratch + cols + a.E + 1, true);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a) {
@@ -167,11 +202,14 @@ __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a)
   const int cols = a.E + a.R;
   const int cp = col_stride(cols);
   uint32_t* masks = lsm;  // [kWords][cp]
+  int32_t* rank_of = reinterpret_cast<int32_t*>(lsm + kWords * cp);  // [E]
   const int tile = blockIdx.x;
-  for (int i = threadIdx.x; i < kWords * cp; i += kThreads) masks[i] = 0;
-  __syncthreads();
   int ek[MOE_MAX_TOPK];
-  mark_token(a, tile * kTile + threadIdx.x, masks, cp, ek);
+  load_token(a, tile * kTile + threadIdx.x, ek);
+  for (int i = threadIdx.x; i < kWords * cp; i += kThreads) masks[i] = 0;
+  fill_rank_table(a, rank_of);
+  __syncthreads();
+  mark_token(a, tile * kTile + threadIdx.x, masks, cp, rank_of, ek);
   __syncthreads();
   for (int col = threadIdx.x; col < cols; col += kThreads) {
     int c = 0;
@@ -187,13 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a)
   if (!is_last) return;
   __threadfence();
 
-  scan_tiles(a, reinterpret_cast<int32_t*>(masks));  // masks are dead now
+  scan_tiles(a, reinterpret_cast<int32_t*>(masks));  // masks are dead now (16 (E + R + 1) ints)
   if (threadIdx.x == 0) *a.ticket = 0;  // ready for the next layout
 }
 
 // shared memory of the scatter kernel, in order
 struct ScatterSmem {
-  int cols, cp, K, KR;  // KR = min(K, R): send entries per token at most
+  int cols, cp, K, KR, E;  // KR = min(K, R): send entries per token at most
   __host__ __device__ size_t masks() const { return 0; }
   __host__ __device__ size_t pre() const { return masks() + sizeof(uint32_t) * kWords * cp; }
   __host__ __device__ size_t seg() const { return align(pre() + sizeof(uint16_t) * kWords * cp); }
@@ -202,7 +240,8 @@ struct ScatterSmem {
   __host__ __device__ size_t sst() const { return rst() + sizeof(uint32_t) * kTile * K; }
   __host__ __device__ size_t base() const { return sst() + sizeof(uint32_t) * kTile * KR; }
   __host__ __device__ size_t off() const { return base() + sizeof(int32_t) * cols; }
-  __host__ __device__ size_t tot() const { return off() + sizeof(int32_t) * (cols + 2); }
+  __host__ __device__ size_t rank_of() const { return off() + sizeof(int32_t) * (cols + 2); }
+  __host__ __device__ size_t tot() const { return rank_of() + sizeof(int32_t) * E; }
   // the single-pass kernel also needs the column totals of its scan
   __host__ __device__ size_t bytes(bool with_tot = false) const {
     return tot() + (with_tot ? sizeof(int32_t) * cols : 0);
@@ -243,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   const int cols = a.E + a.R;
   const int cp = col_stride(cols);
   const int KR = a.K < a.R ? a.K : a.R;
-  const ScatterSmem L{cols, cp, a.K, KR};
+  const ScatterSmem L{cols, cp, a.K, KR, a.E};
   uint32_t* masks = reinterpret_cast<uint32_t*>(ssm + L.masks());  // [kWords][cp]
   uint16_t* pre = reinterpret_cast<uint16_t*>(ssm + L.pre());      // [kWords][cp]
   int32_t* seg = reinterpret_cast<int32_t*>(ssm + L.seg());        // seg_e[E+1] | seg_r[R+1]
@@ -252,12 +291,17 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   uint32_t* sst = reinterpret_cast<uint32_t*>(ssm + L.sst());      // send entries, by column
   int32_t* base = reinterpret_cast<int32_t*>(ssm + L.base());      // [cols] tile bases
   int32_t* off = reinterpret_cast<int32_t*>(ssm + L.off());        // off_e[E+1] | off_s[R+1]
+  int32_t* rank_of = reinterpret_cast<int32_t*>(ssm + L.rank_of()); // [E] expert -> rank
   const int tile = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_t0 = tile * kTile;
   const int tile_n = max(0, min(kTile, a.T - tile_t0));  // tokens in this tile
 
+  const int t = tile_t0 + threadIdx.x;
+  int ek[MOE_MAX_TOPK];
+  load_token(a, t, ek);
   for (int i = threadIdx.x; i < kWords * cp; i += kThreads) masks[i] = 0;
+  fill_rank_table(a, rank_of);
   auto load_bases = [&]() {
     for (int c = threadIdx.x; c < cols; c += kThreads) {
       base[c] = __ldcg(a.tile_hist + static_cast<size_t>(tile) * cols + c);
@@ -270,9 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   };
   if (!kSinglePass) load_bases();
   __syncthreads();
-  const int t = tile_t0 + threadIdx.x;
-  int ek[MOE_MAX_TOPK];
-  const uint32_t valid = mark_token(a, t, masks, cp, ek);
+  const uint32_t valid = mark_token(a, t, masks, cp, rank_of, ek);
   __syncthreads();
   // exclusive prefix of the popcounts over the words of each column; the
   // column's count in this tile goes to seg (scanned below)
@@ -312,7 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   __syncthreads();
 
   if (kSinglePass) {
-    // grid-wide hand-over of the tile counts
+    // grid-wide hand-over of the tile counts: the last block to arrive
+    // publishes a new epoch at once; then every block reads all the tiles'
+    // counts itself (its tile bases and the column totals), so no block waits
+    // on another's scan
     __shared__ uint32_t epoch0;
     __shared__ int last, failed;
     __threadfence();  // this tile's counts are visible device-wide
@@ -321,37 +366,53 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
       epoch0 = ld_acquire(a.ticket + 1);  // read before arriving
       last = atomicAdd(a.ticket, 1u) == static_cast<uint32_t>(a.ntiles - 1);
       failed = 0;
-    }
-    __syncthreads();
-    if (last) {
-      __threadfence();
-      scan_tiles(a, reinterpret_cast<int32_t*>(ssm + L.tot()));
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) {
+      if (last) {
         *a.ticket = 0;  // ready for the next layout
         __threadfence();
         atomicAdd(a.ticket + 1, 1u);  // publish
-      }
-    } else if (threadIdx.x == 0) {
-      const unsigned long long t0 = global_ns();
-      while (ld_acquire(a.ticket + 1) == epoch0) {
-        if (global_ns() - t0 > 1000000000ull) {
-          raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
-          failed = 1;
-          break;
+      } else {
+        const unsigned long long t0 = global_ns();
+        while (ld_acquire(a.ticket + 1) == epoch0) {
+          if (global_ns() - t0 > 1000000000ull) {
+            raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
+            failed = 1;
+            break;
+          }
         }
-        __nanosleep(64);
       }
     }
     __syncthreads();
     if (failed) return;
-    load_bases();
+    // per column: the counts of the tiles before this one (its base) and of
+    // all tiles (the column total), 16 loads in flight per thread
+    int32_t* tot = reinterpret_cast<int32_t*>(ssm + L.tot());
+    for (int col = threadIdx.x; col < cols; col += kThreads) {
+      int before = 0, all = 0;
+      for (int t0 = 0; t0 < a.ntiles; t0 += 16) {
+        int v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          v[i] = t0 + i < a.ntiles ? __ldcg(a.tile_hist + static_cast<size_t>(t0 + i) * cols + col)
+                                   : 0;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (t0 + i < tile) before += v[i];
+          all += v[i];
+        }
+      }
+      base[col] = before;
+      tot[col] = all;
+    }
     __syncthreads();
+    // offsets in shared memory; block 0 also publishes the count arrays
+    scan_totals(a, tot, off, off + a.E + 1, tile == 0);
   }
 
+  // base[c] becomes the first global row of this tile's run of column c
+  for (int c = threadIdx.x; c < cols; c += kThreads) base[c] += c < a.E ? off[c] : off[c + 1];
+  __syncthreads();
   const int32_t* off_e = off;
-  const int32_t* off_s = off + a.E + 1;
+  const int32_t* tot_s = reinterpret_cast<const int32_t*>(ssm + L.tot());  // single pass only
   const int32_t* seg_e = seg;
   const int32_t* seg_r = seg + a.E + 1;
   const int n_recv_rows = a.recv_cap;
@@ -362,19 +423,21 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   // arrays (an entry's slot is its column's segment start plus its rank)
   if (t < a.T) {
     int32_t* pos_g = a.pos + static_cast<size_t>(t) * a.K;
+    int rk[MOE_MAX_TOPK];  // rank of each valid entry's expert
 #pragma unroll
     for (int k = 0; k < MOE_MAX_TOPK; ++k) {
       if (k >= a.K) break;
       int p = -1, srow = -1;
       if ((valid >> k) & 1u) {
         const int e = ek[k];
-        const int r = e / a.epr;
+        const int r = rank_of[e];
+        rk[k] = r;
         const int ce = warp * cp + e;
         const int cr = warp * cp + a.E + r;
         const int rank_e = pre[ce] + __popc(masks[ce] & lt);
         const int rank_r = pre[cr] + __popc(masks[cr] & lt);
-        p = off_e[e] + base[e] + rank_e;
-        srow = off_s[r] + base[a.E + r] + rank_r;
+        p = base[e] + rank_e;
+        srow = base[a.E + r] + rank_r;
         // the scan guarantees p < T*K and srow < S; a violation (inconsistent
         // counts) is reported and the entry dropped instead of written
         if (p < 0 || p >= n_recv_rows || srow < 0 || srow >= n_send_rows) {
@@ -387,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
 #pragma unroll
           for (int j = 0; j < MOE_MAX_TOPK; ++j) {
             if (j >= k) break;
-            if (((valid >> j) & 1u) && ek[j] / a.epr == r) first = false;
+            if (((valid >> j) & 1u) && rk[j] == r) first = false;
           }
           if (first) sst[seg_r[r] + rank_r] = pack_send(r, threadIdx.x);
         }
@@ -413,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
       raise_flag(a.flags, MOE_DEVERR_INTERNAL);
       continue;
     }
-    const int row = off_e[e] + base[e] + (i - seg_e[e]);
+    const int row = base[e] + (i - seg_e[e]);
     if (row < 0 || row >= n_recv_rows) {
       raise_flag(a.flags, MOE_DEVERR_INTERNAL);
       continue;
@@ -425,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   for (int i = threadIdx.x; i < seg_r[a.R]; i += kThreads) {
     const uint32_t u = sst[i];
     const int r = u & 511u, tl = u >> 9;
-    const int row = r < a.R ? off_s[r] + base[a.E + r] + (i - seg_r[r]) : -1;
+    const int row = r < a.R ? base[a.E + r] + (i - seg_r[r]) : -1;
     if (tl >= tile_n || row < 0 || row >= n_send_rows) {
       raise_flag(a.flags, MOE_DEVERR_INTERNAL);
       continue;
@@ -438,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   // and send rows past S
   if (a.pad > 1) {
     for (int e = blockIdx.x; e < a.E; e += gridDim.x) {
-      const int lo = off_e[e] + __ldcg(a.cnt_e + e), hi = off_e[e + 1];
+      const int lo = off_e[e] + (kSinglePass ? tot_s[e] : __ldcg(a.cnt_e + e)), hi = off_e[e + 1];
       for (int p = lo + threadIdx.x; p < hi; p += kThreads) {
         a.recv_token[p] = -1;
         a.recv_k[p] = -1;
@@ -456,16 +519,18 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   for (long long s = off[cols + 1] + gtid; s < n_send_rows; s += gsize) a.send_token[s] = -1;
 }
 
-size_t count_smem(int cols) { return static_cast<size_t>(kWords) * col_stride(cols) * sizeof(uint32_t); }
+size_t count_smem(int cols, int E) {
+  return (static_cast<size_t>(kWords) * col_stride(cols) + E) * sizeof(uint32_t);
+}
 
 size_t scatter_smem(int cols, int K, int R, bool single_pass = false) {
-  return ScatterSmem{cols, col_stride(cols), K, K < R ? K : R}.bytes(single_pass);
+  return ScatterSmem{cols, col_stride(cols), K, K < R ? K : R, cols - R}.bytes(single_pass);
 }
 
 }  // namespace
 
 size_t layout_smem_bytes(int E, int R) {
-  const size_t a = count_smem(E + R), b = scatter_smem(E + R, MOE_MAX_TOPK, R, true);
+  const size_t a = count_smem(E + R, E), b = scatter_smem(E + R, MOE_MAX_TOPK, R, true);
   return a > b ? a : b;
 }
 
@@ -557,7 +622,7 @@ cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T
     if (e == cudaSuccess) return cudaSuccess;
     (void)cudaGetLastError();  // not launched: take the two-launch path
   }
-  layout_count_kernel<<<a.ntiles, kThreads, count_smem(cols), s>>>(a);
+  layout_count_kernel<<<a.ntiles, kThreads, count_smem(cols, a.E), s>>>(a);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   layout_scatter_kernel<false><<<a.ntiles, kThreads, scatter_smem(cols, a.K, a.R), s>>>(a);
