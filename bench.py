@@ -463,8 +463,24 @@ def run_gpu(args, wl):
     if wl.bias == "zipf" and not args.tokens:
         assert load["max_over_mean"] > 5 and load["zero_load_experts"] == 1, load
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
-           for _ in range(args.steps)]
+    # the step as one CUDA graph (captured once, replayed every step): the same
+    # kernels and work, without the per-launch host and driver overhead
+    graph = None
+    if not args.eager:
+        side = torch.cuda.Stream(device)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert moe.moe_read_device_status(h) == 0
+
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -473,15 +489,29 @@ def run_gpu(args, wl):
     time.sleep(0.3)
     start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
     end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     barrier(world)
     el_ms = start.elapsed_time(end)
     ms_step = reduce_max(el_ms / args.steps, world, device)
+
+    # stage times: a second pass of K eager steps with CUDA events between the
+    # calls (the events themselves cost about 2 us each, so this pass runs a
+    # little slower than the timed one)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+           for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize()
     stage_ms = {n: float(np.mean([e[j].elapsed_time(e[j + 1]) for e in evs])) for j, n in enumerate(names)}
     step_median_ms = float(np.median([e[0].elapsed_time(e[-1]) for e in evs]))
+    stage_pass_ms = float(np.mean([e[0].elapsed_time(e[-1]) for e in evs]))
 
     # end to end through the same public calls, inputs from pinned host memory
     # and outputs read back every step
@@ -634,8 +664,10 @@ def run_gpu(args, wl):
         "hbm_gbs": total_bytes / (ms_step / 1e3) / 1e9,
         "hbm_frac_of_peak": total_bytes / (ms_step / 1e3) / 1e9 / peak,
         "hbm_frac_of_nominal": total_bytes / (ms_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
-        "ms_per_step_median": step_median_ms,
+        "launch": "eager" if args.eager else "cuda_graph",
         "bytes_per_step": total_bytes,
+        "stage_pass": {"launch": "eager, CUDA events between the calls", "steps": args.steps,
+                       "ms_per_step": stage_pass_ms, "ms_per_step_median": step_median_ms},
         "stage_ms": stage_ms,
         "stage_gbs": {n: sb[n] / (stage_ms[n] / 1e3) / 1e9 for n in names},
         "roofline": {"kernel": DOMINANT, "bound": "hbm", "achieved": achieved, "peak": peak,
@@ -666,6 +698,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager launches instead of the step replayed as a CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
