@@ -549,6 +549,54 @@ __device__ __forceinline__ bool select_fp32(const RouteArgs& a, int t, int lane,
   return true;
 }
 
+// The weights' e^x and 1/d, accurate to about 2^-41 and 2^-46 (far below the
+// half ulp of the fp32 weights they end in) with fewer fp64 instructions than
+// the correctly rounded library functions; fp64 issue is the scarce resource
+// of this kernel.  The selection's fp64 keys keep the library exp, since
+// their order must match the reference's.
+//
+// e^x: Cody and Waite's range reduction x = n ln2 + r, |r| <= ln2 / 2, with
+// ln2 split into a head of 32 significant bits (so that n * head is exact
+// for |n| < 2^21) and the rest rounded to double; then the Taylor polynomial
+// of degree 10 in Horner form, whose truncation error is below
+// 0.35^11 / 11! * e^0.35 = 3e-13 relative; then the factor 2^n through the
+// exponent field.  Below -708 the result is 0 (e^x < 2^-1021, far below any
+// fp32 weight), above 709 infinity.
+constexpr double kInvLn2 = 1.4426950408889634;
+constexpr double kLn2Head = 0x1.62e42ff000000p-1;
+constexpr double kLn2Tail = -0x1.718432a1b0e26p-35;
+
+__device__ __forceinline__ double exp_weight(double x) {
+  if (x != x) return x;  // NaN (-inf - -inf) stays NaN, as in the reference
+  if (!(x > -708.0)) return 0.0;  // also -inf
+  if (x > 709.0) return INFINITY;
+  const double n = rint(x * kInvLn2);
+  const double r = fma(-n, kLn2Tail, fma(-n, kLn2Head, x));
+  double p = 1.0 / 3628800.0;  // 1/10!
+  p = fma(p, r, 1.0 / 362880.0);
+  p = fma(p, r, 1.0 / 40320.0);
+  p = fma(p, r, 1.0 / 5040.0);
+  p = fma(p, r, 1.0 / 720.0);
+  p = fma(p, r, 1.0 / 120.0);
+  p = fma(p, r, 1.0 / 24.0);
+  p = fma(p, r, 1.0 / 6.0);
+  p = fma(p, r, 0.5);
+  p = fma(p, r, 1.0);
+  p = fma(p, r, 1.0);
+  const long long bits = static_cast<long long>(static_cast<int>(n) + 1023) << 52;  // 2^n, n in [-1022, 1023]
+  return p * __longlong_as_double(bits);
+}
+
+// 1/d: the correctly rounded fp32 reciprocal of d rounded to fp32 (relative
+// error below 2^-23), then one Newton step in fp64, which squares the error
+// (below 2^-46, plus the step's own rounding).  Outside the fp32 range the
+// full division.
+__device__ __forceinline__ double rcp_weight(double d) {
+  if (!(d > 1e-30 && d < 1e30)) return 1.0 / d;
+  const double r0 = static_cast<double>(__frcp_rn(static_cast<float>(d)));
+  return fma(r0, fma(-d, r0, 1.0), r0);
+}
+
 template <int VPL, bool SIGMOID>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
   extern __shared__ double route_smem[];
@@ -594,15 +642,22 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
     const int t = wid + (i0 + j_of_lane) * W;
     double val;
     if (SIGMOID) {
-      val = 1.0 / (1.0 + exp(-static_cast<double>(my_logit)));
+      val = rcp_weight(1.0 + exp_weight(-static_cast<double>(my_logit)));
     } else {
       const float top = __shfl_sync(kFull, my_logit, (j_of_lane * a.K) & 31);
-      val = exp(static_cast<double>(my_logit) - static_cast<double>(top));
+      val = exp_weight(static_cast<double>(my_logit) - static_cast<double>(top));
     }
+    // the sum over the token's K lanes: a butterfly when K is a power of two
+    // (every lane then holds the same bits), else in k order
     double den = 0.0;
-    for (int k = 0; k < a.K; ++k) den += __shfl_sync(kFull, val, (j_of_lane * a.K + k) & 31);
+    if ((a.K & (a.K - 1)) == 0) {
+      den = val;
+      for (int off = 1; off < a.K; off <<= 1) den += __shfl_xor_sync(kFull, den, off);
+    } else {
+      for (int k = 0; k < a.K; ++k) den += __shfl_sync(kFull, val, (j_of_lane * a.K + k) & 31);
+    }
     if (my_fast && j_of_lane < TB && t < a.T) {
-      const double p = (SIGMOID && !a.renorm) ? val : val / den;
+      const double p = (SIGMOID && !a.renorm) ? val : val * rcp_weight(den);
       a.idx[static_cast<size_t>(t) * a.K + k_of_lane] = my_idx;
       a.w[static_cast<size_t>(t) * a.K + k_of_lane] = static_cast<float>(p * a.scale);
     }

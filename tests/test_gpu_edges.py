@@ -246,3 +246,24 @@ def test_large_random_grouped_routing_matches_fp64_oracle(bias_std):
     gi = to_host(gi)
     assert np.array_equal(gi, idx), "%d tokens differ" % int((gi != idx).any(1).sum())
     assert_ulp(to_host(gw_), w, 1, "w")
+
+
+@pytest.mark.parametrize("score_fn,renorm", [("softmax", True), ("sigmoid", True), ("sigmoid", False)])
+def test_weights_over_the_exponent_range(score_fn, renorm):
+    """Logits of magnitude 1e-3 to 800 with either sign: softmax differences to
+    the top pick run from 0 to beyond the fp64 range of exp, sigmoid scores
+    saturate at both ends.  The weights' exponential and reciprocal are the
+    kernel's own (not the library's), so they must stay within 1 fp32 ulp of
+    the oracle's across that whole range."""
+    rng = np.random.default_rng(31 + (score_fn == "sigmoid") + renorm)
+    T, E, K = 4096, 64, 8
+    mag = 10.0 ** rng.uniform(-3, np.log10(800.0), size=(T, E))
+    logits = (mag * rng.choice([-1.0, 1.0], size=(T, E))).astype(np.float32)
+    wl = synth.Workload("range", T=T, H=16, E=E, K=K, R=8, score_fn=score_fn, renorm=renorm)
+    gi, gw_ = router(wl).route(to_dev(logits))
+    if score_fn == "softmax":
+        idx, w = oracle.route_softmax(logits, K, renorm)
+    else:
+        idx, w = oracle.route_sigmoid_grouped(logits, None, K, 1, 1, 1, renorm)
+    assert np.array_equal(to_host(gi), idx)
+    assert_ulp(to_host(gw_), w, 1, "w")
