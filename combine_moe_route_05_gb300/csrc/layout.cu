@@ -7,19 +7,27 @@
 // grouped by expert; "Avoid collective token preparation for AutoEP DeepEP",
 // "Summary": no argsort and no device-to-host split materialisation.
 //
-// Two launches over tiles of MOE_LAYOUT_TILE_TOKENS tokens (one per thread):
-//   1. count: each block marks, in shared-memory bitmasks, which of its
-//      tokens use each expert and each rank (atomicOr is order-free, so the
-//      result does not depend on thread timing), writes per-tile column
-//      counts, and the block that arrives last (an atomic ticket, no
-//      waiting) scans them into per-tile bases, counts and offsets;
-//   2. scatter: each block rebuilds its bitmasks.  The rank of a token among
-//      the tile's users of a column (expert or rank) is a popcount of the mask
-//      bits before it, so every position is a pure function of idx
-//      (bit-identical on replay).  The tile's entries are counting-sorted in
-//      shared memory by column (slot = the column's segment start in the
-//      tile + the entry's rank), and the receive-row and send-row outputs are
-//      then copied out as one contiguous run of rows per column.
+// Tiles of MOE_LAYOUT_TILE_TOKENS tokens, one block per tile and one thread
+// per token.  When every tile's block can be resident at once, the whole
+// layout is one cooperative launch (layout_scatter_kernel<true>): each block
+// marks, in shared-memory bitmasks, which of its tokens use each expert and
+// each rank (atomicOr is order-free, so the result does not depend on thread
+// timing), publishes its tile's column counts and arrives on an atomic
+// ticket; the last block to arrive bumps an epoch the others wait for; then
+// every block reads all tiles' counts (its tile bases and the column totals)
+// and places its tile with the masks still in shared memory.  Otherwise two
+// launches:
+//   1. count: each block marks its tile, writes the column counts, and the
+//      block that arrives last (an atomic ticket, no waiting) scans them into
+//      per-tile bases, counts and offsets;
+//   2. scatter: each block rebuilds its bitmasks.
+// Placement, in both: the rank of a token among the tile's users of a column
+// (expert or rank) is a popcount of the mask bits before it, so every
+// position is a pure function of idx (bit-identical on replay).  The tile's
+// entries are counting-sorted in shared memory by column (slot = the
+// column's segment start in the tile + the entry's rank), and the
+// receive-row and send-row outputs are then copied out as one contiguous run
+// of rows per column.
 //
 // Masks are stored word-major with an odd row stride ([word][col], stride
 // cols | 1) so that the lanes of a warp, which share a word index and differ in
@@ -57,7 +65,8 @@ struct LayoutArgs {
   int32_t* send_token;
   int32_t* send_row_of;
   int32_t* recv_send_row;
-  int32_t* tile_hist;  // [ntiles][cols], exclusive tile bases after the scan
+  int32_t* tile_hist;  // [ntiles][cols] tile counts (exclusive tile bases after
+                       // the two-launch path's scan)
 };
 
 __host__ __device__ constexpr int col_stride(int cols) { return cols | 1; }
@@ -272,10 +281,11 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // kSinglePass = false: the second of two launches (the counts and their
 // scan come from layout_count_kernel).  kSinglePass = true: the whole layout
 // in one cooperative launch (all tiles resident at once): each block counts
-// its tile, the last block to arrive scans the counts and publishes them by
-// bumping an epoch that the other blocks wait for (at most 1 s, then the
-// status word's time-out bit and no writes), and every block goes on to place
-// its tile with the masks still in shared memory.
+// its tile and arrives; the last block to arrive bumps an epoch that the
+// other blocks wait for (at most 1 s, then the status word's time-out bit and
+// no writes); every block then derives its tile bases and the column offsets
+// from all tiles' counts and places its tile with the masks still in shared
+// memory.
 template <bool kSinglePass>
 __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs a) {
   extern __shared__ __align__(16) uint8_t ssm[];
