@@ -241,8 +241,13 @@ __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a)
 // shared memory of the scatter kernel, in order
 struct ScatterSmem {
   int cols, cp, K, KR, E;  // KR = min(K, R): send entries per token at most
+  // the masks, and after the token pass the tile's positions [kTile][K]
   __host__ __device__ size_t masks() const { return 0; }
-  __host__ __device__ size_t pre() const { return masks() + sizeof(uint32_t) * kWords * cp; }
+  __host__ __device__ size_t masks_bytes() const {
+    const size_t m = sizeof(uint32_t) * kWords * cp, p = sizeof(int32_t) * kTile * K;
+    return m > p ? m : p;
+  }
+  __host__ __device__ size_t pre() const { return masks() + masks_bytes(); }
   __host__ __device__ size_t seg() const { return align(pre() + sizeof(uint16_t) * kWords * cp); }
   __host__ __device__ size_t srow() const { return seg() + sizeof(int32_t) * (cols + 2); }
   __host__ __device__ size_t rst() const { return srow() + sizeof(int32_t) * kTile * K; }
@@ -431,8 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
 
   // token pass: positions, and the tile's counting sort into the staging
   // arrays (an entry's slot is its column's segment start plus its rank)
+  int pk[MOE_MAX_TOPK];  // this token's positions, staged for a coalesced copy-out
   if (t < a.T) {
-    int32_t* pos_g = a.pos + static_cast<size_t>(t) * a.K;
     int rk[MOE_MAX_TOPK];  // rank of each valid entry's expert
 #pragma unroll
     for (int k = 0; k < MOE_MAX_TOPK; ++k) {
@@ -465,18 +470,32 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
           if (first) sst[seg_r[r] + rank_r] = pack_send(r, threadIdx.x);
         }
       }
-      pos_g[k] = p;
+      pk[k] = p;
       srow_s[threadIdx.x * a.K + k] = srow;
     }
   }
   __syncthreads();
+  // the masks are dead: their space takes the positions
+  int32_t* pos_s = reinterpret_cast<int32_t*>(ssm + L.masks());
+  if (t < a.T) {
+#pragma unroll
+    for (int k = 0; k < MOE_MAX_TOPK; ++k) {
+      if (k >= a.K) break;
+      pos_s[threadIdx.x * a.K + k] = pk[k];
+    }
+  }
+  __syncthreads();
 
-  // copy-out: send_row_of (token-major), then receive and send entries, each
-  // a run of consecutive rows per column
+  // copy-out: pos and send_row_of (token-major, contiguous for the tile),
+  // then receive and send entries, each a run of consecutive rows per column
   {
     const int n = tile_n * a.K;
+    int32_t* pos_g = a.pos + static_cast<size_t>(tile_t0) * a.K;
     int32_t* srow_g = a.send_row_of + static_cast<size_t>(tile_t0) * a.K;
-    for (int i = threadIdx.x; i < n; i += kThreads) srow_g[i] = srow_s[i];
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      pos_g[i] = pos_s[i];
+      srow_g[i] = srow_s[i];
+    }
   }
   for (int i = threadIdx.x; i < seg_e[a.E]; i += kThreads) {
     const uint32_t u = rst[i];
