@@ -11,9 +11,13 @@ ranks, bf16 rows.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
 
-Under torchrun (N > 1) every rank runs an independent data-parallel replica on
-its own batch (the path shards by token; there is no exchange), and the step
-time is the max over ranks.  Prints one JSON line on rank 0.
+The timed region replays the step captured as one CUDA graph (the same
+kernels and work, without per-launch host overhead; --eager times eager
+calls); per-stage times come from a second, eager pass with CUDA events
+between the calls.  Under torchrun (N > 1) every rank runs an independent
+data-parallel replica on its own batch (the path shards by token; there is
+no exchange), and the step time is the max over ranks.  Prints one JSON line
+on rank 0.
 """
 import argparse
 import hashlib
