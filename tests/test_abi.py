@@ -45,6 +45,15 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(lib.EXPORTS) == set(names)
 
 
+def test_binding_covers_every_declared_function(lib):
+    """The Python binding names exactly the header's functions, and sets a
+    signature for each (no call goes through ctypes' default int marshalling)."""
+    assert set(declared_functions()) == set(lib.EXPORTS)
+    L = lib.lib()
+    for n in lib.EXPORTS:
+        assert getattr(L, n).argtypes is not None, n
+
+
 def test_library_is_built_for_sm_103a_only():
     """The build compiles every translation unit and links for sm_103a, one
     -gencode and no other architecture flag."""
