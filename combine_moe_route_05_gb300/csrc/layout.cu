@@ -486,43 +486,45 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   }
   __syncthreads();
 
-  // copy-out: pos and send_row_of (token-major, contiguous for the tile),
-  // then receive and send entries, each a run of consecutive rows per column
+  // copy-out, one loop so that each thread has the stores of all three kinds
+  // in flight: pos and send_row_of (token-major, contiguous for the tile),
+  // receive entries and send entries (each a run of consecutive rows per
+  // column)
   {
     const int n = tile_n * a.K;
+    const int n_recv = seg_e[a.E], n_send = seg_r[a.R];
+    const int n_all = max(n, max(n_recv, n_send));
     int32_t* pos_g = a.pos + static_cast<size_t>(tile_t0) * a.K;
     int32_t* srow_g = a.send_row_of + static_cast<size_t>(tile_t0) * a.K;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      pos_g[i] = pos_s[i];
-      srow_g[i] = srow_s[i];
+    for (int i = threadIdx.x; i < n_all; i += kThreads) {
+      if (i < n) {
+        pos_g[i] = pos_s[i];
+        srow_g[i] = srow_s[i];
+      }
+      if (i < n_recv) {
+        const uint32_t u = rst[i];
+        const int e = u & 511u, k = (u >> 9) & 15u, tl = u >> 13;
+        // a slot left empty by a dropped inconsistent entry holds stale data
+        const int row = e < a.E ? base[e] + (i - seg_e[e]) : -1;
+        if (e >= a.E || k >= a.K || tl >= tile_n || row < 0 || row >= n_recv_rows) {
+          raise_flag(a.flags, MOE_DEVERR_INTERNAL);
+        } else {
+          a.recv_token[row] = tile_t0 + tl;
+          a.recv_k[row] = k;
+          a.recv_send_row[row] = srow_s[tl * a.K + k];
+        }
+      }
+      if (i < n_send) {
+        const uint32_t u = sst[i];
+        const int r = u & 511u, tl = u >> 9;
+        const int row = r < a.R ? base[a.E + r] + (i - seg_r[r]) : -1;
+        if (tl >= tile_n || row < 0 || row >= n_send_rows) {
+          raise_flag(a.flags, MOE_DEVERR_INTERNAL);
+        } else {
+          a.send_token[row] = tile_t0 + tl;
+        }
+      }
     }
-  }
-  for (int i = threadIdx.x; i < seg_e[a.E]; i += kThreads) {
-    const uint32_t u = rst[i];
-    const int e = u & 511u, k = (u >> 9) & 15u, tl = u >> 13;
-    // a slot left empty by a dropped inconsistent entry holds stale data
-    if (e >= a.E || k >= a.K || tl >= tile_n) {
-      raise_flag(a.flags, MOE_DEVERR_INTERNAL);
-      continue;
-    }
-    const int row = base[e] + (i - seg_e[e]);
-    if (row < 0 || row >= n_recv_rows) {
-      raise_flag(a.flags, MOE_DEVERR_INTERNAL);
-      continue;
-    }
-    a.recv_token[row] = tile_t0 + tl;
-    a.recv_k[row] = k;
-    a.recv_send_row[row] = srow_s[tl * a.K + k];
-  }
-  for (int i = threadIdx.x; i < seg_r[a.R]; i += kThreads) {
-    const uint32_t u = sst[i];
-    const int r = u & 511u, tl = u >> 9;
-    const int row = r < a.R ? base[a.E + r] + (i - seg_r[r]) : -1;
-    if (tl >= tile_n || row < 0 || row >= n_send_rows) {
-      raise_flag(a.flags, MOE_DEVERR_INTERNAL);
-      continue;
-    }
-    a.send_token[row] = tile_t0 + tl;
   }
 
   // pad rows of the expert segments (this block takes experts blockIdx.x,
