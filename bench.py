@@ -23,7 +23,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import subprocess
 import sys
 import threading
@@ -42,9 +41,10 @@ DOMINANT = "combine_bwd"
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e data-sheet bandwidth, for context beside the measured peak
 KERNEL_SOURCES = ("combine_moe_route_05_gb300/csrc/rows.cu", "combine_moe_route_05_gb300/csrc/common.cuh",
                   "combine_moe_route_05_gb300/csrc/router_grad.cuh")
-TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "combine_bwd_deepseek_v3.md")
 W2_SOURCES = ("combine_moe_route_05_gb300/csrc/w2_gemm.cu", "combine_moe_route_05_gb300/csrc/common.cuh")
-W2_TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "w2_absorbed_qwen3_235b.md")
+# per-launch DRAM traffic of the roofline kernels, from one ncu pass each
+TRAFFIC_RECORDS = os.path.join(ROOT, "profiles", "traffic.json")
+L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
 
 
 # ----------------------------------------------------------------------------
@@ -162,7 +162,7 @@ def w2_absorbed_extra(device, stream, reps, tokens=None):
         "bitwise_equal_to_unfused": same,
         "roofline": {"kernel": "w2_absorbed", "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
-                     "traffic": (measured_traffic_per_launch(wl.name, W2_TRAFFIC_SUMMARY, W2_SOURCES)
+                     "traffic": (measured_traffic_per_launch("w2_absorbed", wl.name, W2_SOURCES)
                                  if T == wl.T else None),
                      "algorithmic_flops": flop,
                      "algorithmic_bytes": rows * I * 2 + E * H * I * 2 + rows * H * 2 + rows * 4,
@@ -183,16 +183,16 @@ def kernel_source_hash(sources=KERNEL_SOURCES):
     return h.hexdigest()[:16]
 
 
-def measured_traffic_per_launch(workload_name, summary=TRAFFIC_SUMMARY, sources=KERNEL_SOURCES):
-    """DRAM bytes (read + write) per launch of a kernel, from its committed
-    ncu summary, if that was taken on the current kernel source."""
-    if not os.path.exists(summary):
+def measured_traffic_per_launch(kernel, workload_name, sources=KERNEL_SOURCES):
+    """DRAM bytes (read + write) per launch of `kernel` on the named workload,
+    from its ncu record, if that was taken on the current kernel source."""
+    if not os.path.exists(TRAFFIC_RECORDS):
         return None
-    txt = open(summary).read()
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+workload:\s*(\S+)\s+source:\s*(\w+)", txt)
-    if not m or m.group(2) != workload_name or m.group(3) != kernel_source_hash(sources):
+    with open(TRAFFIC_RECORDS) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("workload") != workload_name or rec.get("source") != kernel_source_hash(sources):
         return None
-    return float(m.group(1))
+    return float(rec["traffic_bytes_per_launch"])
 
 
 # ----------------------------------------------------------------------------
@@ -273,6 +273,20 @@ def reduce_max(value, world, device=None):
     t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def relaunch_under_torchrun(nproc):
+    """`--gpus N` (N > 1) started as a plain process: run this same command as
+    N ranks, one process per GPU, under torch.distributed.run on this node,
+    and return its exit code."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           "--nproc-per-node", str(nproc), "--master-addr", "127.0.0.1",
+           "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
 
 
 def barrier(world):
@@ -364,14 +378,25 @@ def run_reference(args, wl):
 # GPU leg
 
 
-def workload_config(wl, extra=None):
+L2_BYTES = 129e6
+
+
+def workload_config(wl, extra=None, cold=False):
+    eb = 2 if wl.dtype == "bf16" else 4
+    xb, yb = wl.T * wl.H * eb, wl.T * wl.K * wl.H * eb
+    if cold:
+        l2 = "cold: L2 flushed by a 256 MB device write before every timed step"
+    elif xb > L2_BYTES:
+        l2 = "inputs larger than L2 (x %.0f MB, y %.0f MB per step; L2 129 MB)" % (xb / 1e6, yb / 1e6)
+    else:
+        l2 = ("warm: steps back to back; y (%.0f MB) is larger than L2 (129 MB), x (%.0f MB) "
+              "is not and may stay in L2 across steps" % (yb / 1e6, xb / 1e6))
     c = {"workload": "%s T=%d H=%d E=%d K=%d R=%d %s%s" % (
         wl.name, wl.T, wl.H, wl.E, wl.K, wl.R, wl.score_fn,
         (" groups=%d/%d" % (wl.topk_groups, wl.n_groups)) if wl.n_groups > 1 else ""),
         "tokens_per_gpu": wl.T, "hidden": wl.H, "experts": wl.E, "top_k": wl.K,
         "virtual_ranks": wl.R, "row_dtype": wl.dtype, "parallelism": "replicas",
-        "l2": "inputs larger than L2 (x %.0f MB, y %.0f MB per step; L2 129 MB)" % (
-            wl.T * wl.H * 2 / 1e6, wl.T * wl.K * wl.H * 2 / 1e6)}
+        "l2": l2}
     if extra:
         c.update(extra)
     return c
@@ -382,6 +407,9 @@ def run_gpu(args, wl):
     import combine_moe_route_05_gb300 as moe
 
     rank, world, local = dist_env()
+    if torch.cuda.device_count() <= local:
+        raise SystemExit("rank %d needs GPU %d, but %d are visible" % (rank, local,
+                                                                      torch.cuda.device_count()))
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     if world > 1:
@@ -485,23 +513,41 @@ def run_gpu(args, wl):
         torch.cuda.synchronize()
         assert moe.moe_read_device_status(h) == 0
 
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device) if args.cold else None
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    start.record(stream)
-    for i in range(args.steps):
-        if graph is not None:
-            graph.replay()
-        else:
-            step()
-    end.record(stream)
-    torch.cuda.synchronize()
+    if flush is None:
+        # inputs larger than L2 (or warm L2, see the line's config): back to back
+        start.record(stream)
+        for i in range(args.steps):
+            run_step()
+        end.record(stream)
+        torch.cuda.synchronize()
+        el_ms = start.elapsed_time(end)
+    else:
+        # cold L2: every step runs after a write of twice the L2 size, which
+        # sits between the step's own events
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i)
+            ev[i][0].record(stream)
+            run_step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        el_ms = sum(a_.elapsed_time(b_) for a_, b_ in ev)
     clk = clocks.stop()
     barrier(world)
-    el_ms = start.elapsed_time(end)
     ms_step = reduce_max(el_ms / args.steps, world, device)
 
     # stage times: a second pass of K eager steps with CUDA events between the
@@ -656,7 +702,7 @@ def run_gpu(args, wl):
     dom_ms = stage_ms[DOMINANT]
     achieved = sb[DOMINANT] / (dom_ms / 1e3) / 1e9
     # the committed summary is for the full-size workload
-    traffic = measured_traffic_per_launch(wl.name) if not args.tokens else None
+    traffic = measured_traffic_per_launch(DOMINANT, wl.name) if not args.tokens else None
     cpu = None
     if world == 1 and not args.no_cpu:
         cpu = cpu_baseline(wl, args.cpu_tokens)
@@ -664,7 +710,7 @@ def run_gpu(args, wl):
         "metric": METRIC, "value": world * T / (ms_step / 1e3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
-        "data": "synthetic", "config": workload_config(wl),
+        "data": "synthetic", "config": workload_config(wl, cold=args.cold),
         "hbm_gbs": total_bytes / (ms_step / 1e3) / 1e9,
         "hbm_frac_of_peak": total_bytes / (ms_step / 1e3) / 1e9 / peak,
         "hbm_frac_of_nominal": total_bytes / (ms_step / 1e3) / 1e9 / NOMINAL_HBM_GBS,
@@ -704,9 +750,19 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="time eager launches instead of the step replayed as a CUDA graph")
+    ap.add_argument("--cold", action="store_true",
+                    help="flush L2 (a 256 MB device write) before every timed step, outside "
+                         "the step's own events")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(relaunch_under_torchrun(args.gpus))
+    world = dist_env()[1]
+    if world != args.gpus:
+        ap.error("--gpus %d but %d ranks were started" % (args.gpus, world))
     wl = synth.WORKLOADS[args.workload]
     if args.tokens:
         wl = wl.with_tokens(args.tokens)

@@ -25,7 +25,7 @@ MOE_OK, MOE_ERR_INVALID, MOE_ERR_CAPACITY, MOE_ERR_CUDA, MOE_ERR_STATE = range(5
 MOE_BF16, MOE_F32 = 0, 1
 MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID = 0, 1
 MOE_DEVERR_BAD_EXPERT, MOE_DEVERR_DUP_EXPERT, MOE_DEVERR_NONFINITE, MOE_DEVERR_TIMEOUT = 1, 2, 4, 8
-MOE_DEVERR_INTERNAL = 16
+MOE_DEVERR_INTERNAL, MOE_DEVERR_BAD_LAYOUT = 16, 32
 MOE_MAX_EXPERTS, MOE_MAX_TOPK = 512, 16
 
 EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_handle_create", "moe_handle_destroy",
@@ -34,7 +34,7 @@ EXPORTS = ("moe_status_string", "moe_workspace_bytes", "moe_handle_create", "moe
            "moe_scale_rows_bwd", "moe_read_device_status", "moe_clear_device_status",
            "moe_dispatch_layout_static", "moe_route_bwd", "moe_expand", "moe_combine_partial",
            "moe_combine_reduce", "moe_w2_absorbed", "moe_dispatch_layout_launches",
-           "moe_dispatch_bwd_route", "moe_dispatch_bwd_route_launches")
+           "moe_dispatch_bwd_route", "moe_dispatch_bwd_route_launches", "moe_set_wait_limit")
 MOE_LAYOUT_STATIC_COUNTERS = 65536
 MOE_LAYOUT_TILE_TOKENS = 512
 
@@ -98,6 +98,7 @@ def lib():
             "moe_dispatch_layout_launches": ([P, i32, P], st),
             "moe_dispatch_bwd_route": ([P, P, i32, i32, P, P, P, P, P, P], st),
             "moe_dispatch_bwd_route_launches": ([P, P], st),
+            "moe_set_wait_limit": ([P, ctypes.c_uint64], st),
         }
         for name, (args, res) in sigs.items():
             f = getattr(L, name)
@@ -386,6 +387,11 @@ def moe_read_device_status(h):
 
 def moe_clear_device_status(h, stream=None):
     _check("moe_clear_device_status", lib().moe_clear_device_status(h.ptr, _stream(stream)))
+
+
+def moe_set_wait_limit(h, limit_ns):
+    """Limit of the kernels' bounded waits on this handle (0: the 1 s default)."""
+    _check("moe_set_wait_limit", lib().moe_set_wait_limit(h.ptr, int(limit_ns)))
 
 
 LAYOUT_FIELDS = ("cnt_e", "off_e", "cnt_send_r", "off_send_r", "cnt_recv_r", "off_recv_r", "pos",

@@ -155,6 +155,7 @@ moe_status moe_handle_create(const moe_config* c, void* d_workspace, size_t work
   h->T = -1;
   h->max_tiles = p.max_tiles;
   h->pad = c->pad_align > 1 ? c->pad_align : 1;
+  h->wait_ns = MOE_DEFAULT_WAIT_LIMIT_NS;
   h->flags = reinterpret_cast<uint32_t*>(ws + p.flags);
   h->ticket = reinterpret_cast<uint32_t*>(ws + p.ticket);
   h->cnt_e = reinterpret_cast<int32_t*>(ws + p.cnt_e);
@@ -388,7 +389,17 @@ moe_status moe_read_device_status(const moe_handle* h, uint32_t* host_flags) {
 
 moe_status moe_clear_device_status(moe_handle* h, void* stream) {
   if (!h) return MOE_ERR_INVALID;
-  return from_cuda(cudaMemsetAsync(h->flags, 0, sizeof(uint32_t), as_stream(stream)));
+  cudaError_t e = cudaMemsetAsync(h->flags, 0, sizeof(uint32_t), as_stream(stream));
+  // a layout whose hand-over timed out left its arrival counter short of
+  // zero-on-exit: re-arm it (the epoch word is only ever compared relatively)
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->ticket, 0, sizeof(uint32_t), as_stream(stream));
+  return from_cuda(e);
+}
+
+moe_status moe_set_wait_limit(moe_handle* h, uint64_t limit_ns) {
+  if (!h) return MOE_ERR_INVALID;
+  h->wait_ns = limit_ns ? limit_ns : MOE_DEFAULT_WAIT_LIMIT_NS;
+  return MOE_OK;
 }
 
 }  // extern "C"

@@ -16,6 +16,16 @@ __device__ __forceinline__ void raise_flag(uint32_t* flags, uint32_t bit) {
   if (flags) atomicOr(flags, bit);
 }
 
+// A row index read from the layout (a receive row, a send row), checked
+// against the n rows of the tensor it indexes: -1 (a dropped entry) stays -1;
+// any other index outside [0, n) raises MOE_DEVERR_BAD_LAYOUT and reads as -1,
+// so that the entry is skipped instead of reaching outside the tensor.
+__device__ __forceinline__ int checked_row(int r, int n, uint32_t* flags) {
+  if (static_cast<unsigned>(r) < static_cast<unsigned>(n)) return r;
+  if (r != -1) raise_flag(flags, MOE_DEVERR_BAD_LAYOUT);
+  return -1;
+}
+
 // ---------------------------------------------------------------------------
 // 16-byte vector rows
 

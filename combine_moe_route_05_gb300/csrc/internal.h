@@ -14,8 +14,9 @@ struct moe_handle {
   int T;  // tokens of the current layout, -1 before the first
   int max_tiles;
   int pad;  // receive segments rounded up to a multiple of pad rows (>= 1)
+  unsigned long long wait_ns;  // limit of the kernels' bounded waits
   uint32_t* flags;   // device status word (MOE_DEVERR_* bits)
-  uint32_t* ticket;  // arrival counter of the layout's last-block scan
+  uint32_t* ticket;  // [0] arrival counter of the layout's tile hand-over, [1] its epoch
   int32_t* cnt_e;
   int32_t* off_e;
   int32_t* cnt_send_r;
@@ -93,6 +94,9 @@ cudaError_t launch_scale_rows_bwd(const moe_handle* h, const void* ghs, const vo
 int layout_launches(const moe_config& c, int T);
 cudaError_t prepare_w2_kernel();
 bool w2_shape_ok(int I, int H);
+// Bounded waits inside the kernels give up after this long by default (1 s).
+#define MOE_DEFAULT_WAIT_LIMIT_NS 1000000000ull
+
 cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, const float* recv_w,
                                const void* w2, int H, void* y, cudaStream_t s);
 

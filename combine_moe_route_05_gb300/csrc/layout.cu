@@ -52,6 +52,7 @@ struct LayoutArgs {
   int recv_cap;  // receive rows: T*K + E*(pad-1)
   uint32_t* flags;
   uint32_t* ticket;  // [0] arrival counter, [1] epoch of the single-pass kernel
+  unsigned long long wait_ns;  // limit of the single-pass kernel's wait for the epoch
   int32_t* cnt_e;
   int32_t* off_e;
   int32_t* cnt_send_r;
@@ -287,8 +288,8 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // scan come from layout_count_kernel).  kSinglePass = true: the whole layout
 // in one cooperative launch (all tiles resident at once): each block counts
 // its tile and arrives; the last block to arrive bumps an epoch that the
-// other blocks wait for (at most 1 s, then the status word's time-out bit and
-// no writes); every block then derives its tile bases and the column offsets
+// other blocks wait for (at most wait_ns, 1 s unless the handle sets another
+// limit, then the status word's time-out bit and no writes); every block then derives its tile bases and the column offsets
 // from all tiles' counts and places its tile with the masks still in shared
 // memory.
 template <bool kSinglePass>
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
       } else {
         const unsigned long long t0 = global_ns();
         while (ld_acquire(a.ticket + 1) == epoch0) {
-          if (global_ns() - t0 > 1000000000ull) {
+          if (global_ns() - t0 > a.wait_ns) {
             raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
             failed = 1;
             break;
@@ -613,7 +614,8 @@ int resident_single_pass_blocks(size_t smem) {
 // entry, and tiles * (E + R) tile counters).
 cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T,
                                   const moe_layout& out, uint32_t* flags, uint32_t* ticket,
-                                  int32_t* tile_hist, int max_tiles, cudaStream_t s) {
+                                  int32_t* tile_hist, int max_tiles, unsigned long long wait_ns,
+                                  cudaStream_t s) {
   LayoutArgs a;
   a.idx = idx;
   a.T = T;
@@ -627,6 +629,7 @@ cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T
   a.recv_cap = T * a.K + a.E * (a.pad - 1);
   a.flags = flags;
   a.ticket = ticket;
+  a.wait_ns = wait_ns;
   a.cnt_e = out.cnt_e;
   a.off_e = out.off_e;
   a.cnt_send_r = out.cnt_send_r;
@@ -682,7 +685,7 @@ cudaError_t launch_layout(const moe_handle* h, const int32_t* idx, int T, cudaSt
   out.send_row_of = h->send_row_of;
   out.recv_send_row = h->recv_send_row;
   return launch_layout_buffers(h->cfg, idx, T, out, h->flags, h->ticket, h->tile_hist,
-                               h->max_tiles, s);
+                               h->max_tiles, h->wait_ns, s);
 }
 
 }  // namespace moe

@@ -18,7 +18,8 @@ cudaError_t prepare_layout_kernels();
 int layout_tiles(int T);
 cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T,
                                   const moe_layout& out, uint32_t* flags, uint32_t* ticket,
-                                  int32_t* tile_hist, int max_tiles, cudaStream_t s);
+                                  int32_t* tile_hist, int max_tiles, unsigned long long wait_ns,
+                                  cudaStream_t s);
 }  // namespace moe
 
 namespace {
@@ -87,6 +88,7 @@ extern "C" moe_status moe_dispatch_layout_static(const moe_config* c, const int3
   const int tiles = moe::layout_tiles(T);
   cudaError_t e = moe::launch_layout_buffers(*c, d_idx, T, *out, d_status,
                                              reinterpret_cast<uint32_t*>(scratch),
-                                             scratch + kTicketSlot, tiles, s);
+                                             scratch + kTicketSlot, tiles,
+                                             MOE_DEFAULT_WAIT_LIMIT_NS, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -42,6 +42,8 @@ struct DispatchArgs {
   uint8_t* recv;
   float* recv_w;
   uint8_t* send;
+  int recv_rows, send_rows;  // rows of recv / recv_w and of send
+  uint32_t* flags;
 };
 
 template <int KMAX>
@@ -53,8 +55,10 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(DispatchArgs a) {
       p[k] = -1;
       srow[k] = -1;
       if (k < a.K) {
-        p[k] = __ldg(a.pos + static_cast<size_t>(t) * a.K + k);
-        if (a.send) srow[k] = __ldg(a.send_row_of + static_cast<size_t>(t) * a.K + k);
+        p[k] = checked_row(__ldg(a.pos + static_cast<size_t>(t) * a.K + k), a.recv_rows, a.flags);
+        if (a.send)
+          srow[k] = checked_row(__ldg(a.send_row_of + static_cast<size_t>(t) * a.K + k),
+                                a.send_rows, a.flags);
       }
     }
     if (a.send) {
@@ -67,7 +71,8 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(DispatchArgs a) {
     }
     if (a.recv_w && threadIdx.x < a.K) {
       const int pk = __ldg(a.pos + static_cast<size_t>(t) * a.K + threadIdx.x);
-      if (pk >= 0) a.recv_w[pk] = __ldg(a.w + static_cast<size_t>(t) * a.K + threadIdx.x);
+      if (static_cast<unsigned>(pk) < static_cast<unsigned>(a.recv_rows))
+        a.recv_w[pk] = __ldg(a.w + static_cast<size_t>(t) * a.K + threadIdx.x);
     }
     const uint8_t* xrow = a.x + static_cast<int64_t>(t) * a.row_bytes;
     for (int v = threadIdx.x; v < a.nvec; v += blockDim.x) {
@@ -98,6 +103,8 @@ struct RowArgs {
   int64_t row_bytes;
   int nvec;           // 16-byte vectors per row
   int T, K;
+  int rows;           // receive rows of y / gy (the bound of every pos entry)
+  uint32_t* flags;
   // router backward fused into the dispatch backward (else unused)
   const float* logits;  // [T, E]
   const int32_t* idx;   // [T, K]
@@ -109,13 +116,14 @@ struct RowArgs {
 
 template <int KMAX>
 __device__ __forceinline__ void load_entries(const int32_t* pos, const float* w, int t, int K,
-                                             int (&p)[KMAX], float (&wk)[KMAX]) {
+                                             int rows, uint32_t* flags, int (&p)[KMAX],
+                                             float (&wk)[KMAX]) {
 #pragma unroll
   for (int k = 0; k < KMAX; ++k) {
     p[k] = -1;
     wk[k] = 1.0f;
     if (k < K) {
-      p[k] = __ldg(pos + static_cast<size_t>(t) * K + k);
+      p[k] = checked_row(__ldg(pos + static_cast<size_t>(t) * K + k), rows, flags);
       if (w) wk[k] = __ldg(w + static_cast<size_t>(t) * K + k);
     }
   }
@@ -182,7 +190,7 @@ __device__ __forceinline__ void combine_body(const RowArgs<Elt>& a) {
       router_bwd_pass(a, it, ntok);
     int p[KMAX];
     float wk[KMAX];
-    load_entries<KMAX>(a.pos, WEIGHTED ? a.w : nullptr, t, a.K, p, wk);
+    load_entries<KMAX>(a.pos, WEIGHTED ? a.w : nullptr, t, a.K, a.rows, a.flags, p, wk);
     uint8_t* orow = a.out + static_cast<int64_t>(t) * a.row_bytes;
     for (int v = threadIdx.x; v < a.nvec; v += blockDim.x) {
       Vec16 in[KMAX];
@@ -229,7 +237,7 @@ __device__ __forceinline__ void combine_bwd_token(const RowArgs<Elt>& a, int t, 
   constexpr int N = VT::N;
   int p[KMAX];
   float wk[KMAX];
-  load_entries<KMAX>(a.pos, WEIGHTED ? a.w : nullptr, t, a.K, p, wk);
+  load_entries<KMAX>(a.pos, WEIGHTED ? a.w : nullptr, t, a.K, a.rows, a.flags, p, wk);
 #pragma unroll
   for (int k = 0; k < KMAX; ++k) dot[k] = 0.0f;
   const uint8_t* grow = a.g + static_cast<int64_t>(t) * a.row_bytes;
@@ -293,8 +301,9 @@ __global__ void __launch_bounds__(kGatherMaxThreads, 2) combine_bwd_kernel(RowAr
       if (threadIdx.x < a.K) {
         float s = 0.0f;
         for (int wi = 0; wi < nw; ++wi) s += red[it & 1][wi][threadIdx.x];
-        int pk = __ldg(a.pos + static_cast<size_t>(t) * a.K + threadIdx.x);
-        a.gw[static_cast<size_t>(t) * a.K + threadIdx.x] = pk >= 0 ? s : 0.0f;
+        const int pk = __ldg(a.pos + static_cast<size_t>(t) * a.K + threadIdx.x);
+        a.gw[static_cast<size_t>(t) * a.K + threadIdx.x] =
+            static_cast<unsigned>(pk) < static_cast<unsigned>(a.rows) ? s : 0.0f;
       }
     }
   }
@@ -305,9 +314,16 @@ __global__ void __launch_bounds__(kGatherMaxThreads, 2) combine_bwd_kernel(RowAr
 
 __global__ void __launch_bounds__(256) zero_pad_rows_kernel(uint8_t* rows, int64_t row_bytes,
                                                             const int32_t* off_e,
-                                                            const int32_t* cnt_e, int E) {
+                                                            const int32_t* cnt_e, int E,
+                                                            int nrows, uint32_t* flags) {
   for (int e = blockIdx.x; e < E; e += gridDim.x) {
-    const int64_t lo = static_cast<int64_t>(off_e[e]) + cnt_e[e], hi = off_e[e + 1];
+    int64_t lo = static_cast<int64_t>(off_e[e]) + cnt_e[e], hi = off_e[e + 1];
+    if (lo < 0 || hi > nrows) {
+      // offsets outside the tensor: zero only what lies inside it
+      if (threadIdx.x == 0) raise_flag(flags, MOE_DEVERR_BAD_LAYOUT);
+      lo = lo < 0 ? 0 : lo;
+      hi = hi > nrows ? nrows : hi;
+    }
     uint8_t* base = rows + lo * row_bytes;
     const int64_t bytes = (hi - lo) * row_bytes;
     if ((row_bytes & 15) == 0) {
@@ -336,6 +352,8 @@ struct StagedArgs {
   int64_t row_bytes;
   int nvec;
   int T, K;
+  int recv_rows, send_rows;  // bounds of pos and send_row_of entries
+  uint32_t* flags;
 };
 
 template <int KMAX>
@@ -347,8 +365,9 @@ __device__ __forceinline__ uint32_t load_send_entries(const StagedArgs& a, int t
     p[k] = -1;
     sr[k] = -1;
     if (k < a.K) {
-      p[k] = __ldg(a.pos + static_cast<size_t>(t) * a.K + k);
-      sr[k] = __ldg(a.send_row_of + static_cast<size_t>(t) * a.K + k);
+      p[k] = checked_row(__ldg(a.pos + static_cast<size_t>(t) * a.K + k), a.recv_rows, a.flags);
+      sr[k] = checked_row(__ldg(a.send_row_of + static_cast<size_t>(t) * a.K + k), a.send_rows,
+                          a.flags);
     }
   }
 #pragma unroll
@@ -464,10 +483,15 @@ __global__ void __launch_bounds__(kGatherMaxThreads) combine_reduce_kernel(Stage
 template <typename Elt>
 __global__ void __launch_bounds__(kRowThreads) scale_rows_kernel(const uint8_t* h, const float* rw,
                                                                  uint8_t* hs, int64_t row_bytes,
-                                                                 int nvec, const int32_t* nrows_dev) {
+                                                                 int nvec, const int32_t* nrows_dev,
+                                                                 int rows_cap, uint32_t* flags) {
   using VT = VecTraits<Elt>;
   constexpr int N = VT::N;
-  const int64_t nrows = *nrows_dev;
+  int64_t nrows = *nrows_dev;
+  if (nrows < 0 || nrows > rows_cap) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) raise_flag(flags, MOE_DEVERR_BAD_LAYOUT);
+    nrows = nrows < 0 ? 0 : rows_cap;
+  }
   const int64_t total = nrows * nvec;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * kRowThreads + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * kRowThreads) {
@@ -487,14 +511,15 @@ __global__ void __launch_bounds__(kRowThreads) scale_rows_kernel(const uint8_t* 
 template <typename Elt>
 __global__ void __launch_bounds__(kRowThreads) scale_rows_bwd_kernel(
     const uint8_t* ghs, const uint8_t* h, const float* rw, uint8_t* gh, float* gw,
-    const int32_t* pos, int64_t entries, int64_t row_bytes, int nvec) {
+    const int32_t* pos, int64_t entries, int64_t row_bytes, int nvec, int rows,
+    uint32_t* flags) {
   using VT = VecTraits<Elt>;
   constexpr int N = VT::N;
   const int lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kRowThreads / 32);
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * (kRowThreads / 32) + (threadIdx.x >> 5);
        e < entries; e += nwarps) {
-    const int p = __ldg(pos + e);
+    const int p = checked_row(__ldg(pos + e), rows, flags);
     float dot = 0.0f;
     if (p >= 0) {
       const float s = __ldg(rw + p);
@@ -562,6 +587,16 @@ int grid_for(const void* kernel, int threads, size_t smem, int num_sms, long lon
   return static_cast<int>(g < 1 ? 1 : g);
 }
 
+// Rows of a receive-row tensor (T*K plus the pads) and of a send-row tensor
+// (T*min(K,R)) for the handle's current layout: the bounds of the layout's
+// row indices.
+int recv_rows_of(const moe_handle* h) {
+  return h->T * h->cfg.top_k + h->cfg.num_experts * (h->pad - 1);
+}
+int send_rows_of(const moe_handle* h) {
+  return h->T * (h->cfg.top_k < h->cfg.num_ranks ? h->cfg.top_k : h->cfg.num_ranks);
+}
+
 int gather_threads(int nvec) {
   const int t = threads_for(nvec, 2);
   return t > kGatherMaxThreads ? kGatherMaxThreads : t;
@@ -579,6 +614,8 @@ cudaError_t launch_combine_t(const moe_handle* h, const void* y, int H, const fl
   a.nvec = static_cast<int>(a.row_bytes / 16);
   a.T = h->T;
   a.K = h->cfg.top_k;
+  a.rows = recv_rows_of(h);
+  a.flags = h->flags;
   if (a.T == 0) return cudaSuccess;
   const int block = gather_threads(a.nvec);
   if (rt) {
@@ -617,6 +654,8 @@ cudaError_t launch_combine_bwd_t(const moe_handle* h, const void* g, const void*
   a.nvec = static_cast<int>(a.row_bytes / 16);
   a.T = h->T;
   a.K = h->cfg.top_k;
+  a.rows = recv_rows_of(h);
+  a.flags = h->flags;
   if (a.T == 0) return cudaSuccess;
   const int block = gather_threads(a.nvec);
   const void* kp;
@@ -654,6 +693,9 @@ cudaError_t launch_dispatch(const moe_handle* h, const void* x, int64_t row_byte
   a.recv = static_cast<uint8_t*>(recv);
   a.recv_w = recv_w;
   a.send = static_cast<uint8_t*>(send);
+  a.recv_rows = recv_rows_of(h);
+  a.send_rows = send_rows_of(h);
+  a.flags = h->flags;
   if (a.T == 0) return cudaSuccess;
   // one block per token, a thread per 16-byte vector of the row (many
   // independent stores in flight; measured faster than bulk copies through
@@ -723,12 +765,14 @@ cudaError_t launch_scale_rows(const moe_handle* h, const void* hrows, int I, int
     auto k = scale_rows_kernel<__nv_bfloat16>;
     const int grid = grid_for(reinterpret_cast<const void*>(k), kRowThreads, 0, h->num_sms, blocks);
     k<<<grid, kRowThreads, 0, s>>>(static_cast<const uint8_t*>(hrows), recv_w,
-                                   static_cast<uint8_t*>(hs), row_bytes, nvec, nrows);
+                                   static_cast<uint8_t*>(hs), row_bytes, nvec, nrows,
+                                   recv_rows_of(h), h->flags);
   } else {
     auto k = scale_rows_kernel<float>;
     const int grid = grid_for(reinterpret_cast<const void*>(k), kRowThreads, 0, h->num_sms, blocks);
     k<<<grid, kRowThreads, 0, s>>>(static_cast<const uint8_t*>(hrows), recv_w,
-                                   static_cast<uint8_t*>(hs), row_bytes, nvec, nrows);
+                                   static_cast<uint8_t*>(hs), row_bytes, nvec, nrows,
+                                   recv_rows_of(h), h->flags);
   }
   return cudaGetLastError();
 }
@@ -746,13 +790,15 @@ cudaError_t launch_scale_rows_bwd(const moe_handle* h, const void* ghs, const vo
     const int grid = grid_for(reinterpret_cast<const void*>(k), kRowThreads, 0, h->num_sms, blocks);
     k<<<grid, kRowThreads, 0, s>>>(static_cast<const uint8_t*>(ghs),
                                    static_cast<const uint8_t*>(hrows), recv_w,
-                                   static_cast<uint8_t*>(gh), gw, h->pos, entries, row_bytes, nvec);
+                                   static_cast<uint8_t*>(gh), gw, h->pos, entries, row_bytes, nvec,
+                                   recv_rows_of(h), h->flags);
   } else {
     auto k = scale_rows_bwd_kernel<float>;
     const int grid = grid_for(reinterpret_cast<const void*>(k), kRowThreads, 0, h->num_sms, blocks);
     k<<<grid, kRowThreads, 0, s>>>(static_cast<const uint8_t*>(ghs),
                                    static_cast<const uint8_t*>(hrows), recv_w,
-                                   static_cast<uint8_t*>(gh), gw, h->pos, entries, row_bytes, nvec);
+                                   static_cast<uint8_t*>(gh), gw, h->pos, entries, row_bytes, nvec,
+                                   recv_rows_of(h), h->flags);
   }
   const cudaError_t e = cudaGetLastError();
   return e != cudaSuccess ? e : zero_pad_rows(h, gh, row_bytes, s);
@@ -770,6 +816,9 @@ cudaError_t launch_staged(int op, const moe_handle* h, const void* src, int H, i
   a.nvec = static_cast<int>(a.row_bytes / 16);
   a.T = h->T;
   a.K = h->cfg.top_k;
+  a.recv_rows = recv_rows_of(h);
+  a.send_rows = send_rows_of(h);
+  a.flags = h->flags;
   if (a.T == 0) return cudaSuccess;
   const bool k8 = a.K <= 8;
   if (op == 0) {  // expand: one block per token, about two vectors per thread
@@ -812,7 +861,7 @@ cudaError_t zero_pad_rows(const moe_handle* h, void* rows, int64_t row_bytes, cu
   if (h->pad <= 1 || h->T <= 0 || !rows) return cudaSuccess;
   const int E = h->cfg.num_experts;
   zero_pad_rows_kernel<<<E, 256, 0, s>>>(static_cast<uint8_t*>(rows), row_bytes, h->off_e, h->cnt_e,
-                                          E);
+                                          E, recv_rows_of(h), h->flags);
   return cudaGetLastError();
 }
 

@@ -67,7 +67,6 @@ static_assert(8 * (2 * kStagesA + 2 * kStages + 2) + 16 <= 512, "barrier area");
 constexpr size_t kBarrierBytes = 512;  // 34 mbarriers and the tensor-memory address
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStagesA * kABytes + kStages * kBBytes +
                               kBarrierBytes + sizeof(int32_t) * (3 * MOE_MAX_EXPERTS + 2);
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A
 // and B bf16 (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
@@ -82,6 +81,8 @@ struct W2Args {
   const int32_t* cnt_e;
   __nv_bfloat16* y;
   uint32_t* flags;
+  unsigned long long wait_ns;  // limit of every mbarrier wait
+  int rows;     // receive rows of h and y (T*K plus the pads)
   int E, I, H;
   int n_tiles;  // H / kBN
 };
@@ -107,14 +108,15 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-// Wait for the phase of `bar` with the given parity; false after ~1 s.
-__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity) {
+// Wait for the phase of `bar` with the given parity; false after limit_ns.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity,
+                                           unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (;;) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -257,9 +259,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (a.I + kBK - 1) / kBK;
 
+  // the segments, checked: 0 <= off[e] <= off[e] + cnt[e] <= off[e+1] <=
+  // rows; a layout that breaks this (corrupted or not this handle's) raises
+  // MOE_DEVERR_BAD_LAYOUT and the kernel computes nothing
+  int bad = 0;
   for (int e = threadIdx.x; e <= a.E; e += kThreads) {
-    tb.off[e] = a.off_e[e];
-    if (e < a.E) tb.cnt[e] = a.cnt_e[e];
+    const int lo = a.off_e[e];
+    tb.off[e] = lo;
+    if (e < a.E) {
+      const int c = a.cnt_e[e], hi = a.off_e[e + 1];
+      tb.cnt[e] = c;
+      bad |= lo < 0 || c < 0 || c > hi - lo || hi > a.rows;
+    }
+  }
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) raise_flag(a.flags, MOE_DEVERR_BAD_LAYOUT);
+    for (int e = threadIdx.x; e <= a.E; e += kThreads) {
+      tb.off[e] = 0;
+      if (e < a.E) tb.cnt[e] = 0;
+    }
   }
   __syncthreads();
   if (warp == 0) {
@@ -320,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % stages;
           const uint32_t ph = (it / stages) & 1u;
-          if (it >= stages && !wait_phase(&freed[s], ph ^ 1u)) {
+          if (it >= stages && !wait_phase(&freed[s], ph ^ 1u, a.wait_ns)) {
             ok = false;
             break;
           }
@@ -337,20 +355,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (the W2 barrier also needs the prologue's arrivals; its phases for the
       // last slices complete once the prologue has stored them)
       for (int j = it - stages < 0 ? 0 : it - stages; j < it; ++j)
-        if (!wait_phase(&landed[j % stages], (j / stages) & 1u)) ok = false;
+        if (!wait_phase(&landed[j % stages], (j / stages) & 1u, a.wait_ns)) ok = false;
     }
   } else if (warp == 1) {
     if (lane == 0) {
       int it = 0, n = 0;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
-        if (n >= 1 && !wait_phase(acc_empty, (n - 1) & 1u)) {
+        if (n >= 1 && !wait_phase(acc_empty, (n - 1) & 1u, a.wait_ns)) {
           ok = false;
           break;
         }
         tc_fence_after();
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kStages;
-          if (!wait_phase(&full[s], (it / kStages) & 1u)) {
+          if (!wait_phase(&full[s], (it / kStages) & 1u, a.wait_ns)) {
             ok = false;
             break;
           }
@@ -386,8 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int sa = it % kStagesA, st = it % kStages;
         // each lane waits itself (acquiring the copy); the warp leaves together
-        bool got = wait_phase(&full_a[sa], (it / kStagesA) & 1u);
-        if (got && it >= kStages) got = wait_phase(&empty[st], ((it / kStages) & 1u) ^ 1u);
+        bool got = wait_phase(&full_a[sa], (it / kStagesA) & 1u, a.wait_ns);
+        if (got && it >= kStages) got = wait_phase(&empty[st], ((it / kStages) & 1u) ^ 1u, a.wait_ns);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -427,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int n = 0;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
       const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile);
-      if (!__all_sync(0xffffffffu, wait_phase(acc_full, n & 1u))) {
+      if (!__all_sync(0xffffffffu, wait_phase(acc_full, n & 1u, a.wait_ns))) {
         ok = false;
         break;
       }
@@ -473,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // every MMA must be complete before the columns are released: wait for
     // the last tile's accumulator commit (on the normal path the epilogue
     // already has, and this returns at once)
-    if (lane == 0 && my_tiles > 0 && !wait_phase(acc_full, (my_tiles - 1) & 1u))
+    if (lane == 0 && my_tiles > 0 && !wait_phase(acc_full, (my_tiles - 1) & 1u, a.wait_ns))
       raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
     __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -540,6 +558,8 @@ cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, co
   a.cnt_e = h->cnt_e;
   a.y = static_cast<__nv_bfloat16*>(y);
   a.flags = h->flags;
+  a.wait_ns = h->wait_ns;
+  a.rows = static_cast<int>(rows_cap);
   a.E = E;
   a.I = I;
   a.H = H;

@@ -68,6 +68,9 @@ typedef enum moe_score_fn { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_s
 #define MOE_DEVERR_NONFINITE 0x4u  /* NaN/Inf router logit: token's route unspecified */
 #define MOE_DEVERR_TIMEOUT 0x8u    /* a bounded wait inside a kernel gave up      */
 #define MOE_DEVERR_INTERNAL 0x10u  /* layout counts inconsistent: writes skipped  */
+#define MOE_DEVERR_BAD_LAYOUT 0x20u /* a row index or offset read from the layout
+                                       lies outside the row tensors (a corrupted
+                                       or foreign layout): entry skipped         */
 
 /* Limits checked by moe_handle_create. */
 #define MOE_MAX_EXPERTS 512
@@ -176,7 +179,12 @@ moe_status moe_handle_create(const moe_config* c, void* d_workspace, size_t work
 moe_status moe_handle_destroy(moe_handle* h);
 
 /*
- * Routing: per token, the top-K experts and their weights.
+ * Routing: per token, the top-K experts and their weights ([AutoEP-prep]
+ * "Testing Done": the parity list covers exact routes, the score-correction
+ * bias, routing scores, skewed routing and an empty expert; NeMo Automodel PR
+ * "use the DeepEP dispatcher in the DiffusionGemma recipes", "Why hybridep +
+ * activation checkpointing fails": a recomputed gate reproduces its top-k
+ * indices exactly).
  *   d_logits [T,E] fp32 router logits; d_bias [E] fp32 score-correction bias
  *   (sigmoid only; NULL = none).  Outputs d_idx [T,K] int32 in descending key
  *   order, equal keys to the lower expert index; d_w [T,K] fp32.
@@ -397,8 +405,26 @@ moe_status moe_w2_absorbed(const moe_handle* h, const void* d_h, int32_t I, cons
  */
 moe_status moe_read_device_status(const moe_handle* h, uint32_t* host_flags);
 
-/* Clears the device status word (asynchronous on `stream`). */
+/*
+ * Clears the device status word and re-arms the layout's arrival counter
+ * (asynchronous on `stream`).  After a MOE_DEVERR_TIMEOUT, call it before the
+ * next moe_dispatch_layout on this handle: a layout whose grid-wide hand-over
+ * gave up leaves that counter where no later layout would complete.
+ */
 moe_status moe_clear_device_status(moe_handle* h, void* stream);
+
+/*
+ * Time limit, in nanoseconds, of every bounded wait inside this handle's
+ * kernels: the single-launch layout's wait for all tiles' counts, and the
+ * pipeline waits of moe_w2_absorbed ([AutoEP-DeepEP] review fix: a transport
+ * that runs out of what it needs must fail, not fault).  A wait that gives up
+ * sets MOE_DEVERR_TIMEOUT, and the kernel stops writing and returns (the W2
+ * GEMM first waits, within the same limit, for the copies it has in flight
+ * and releases its tensor memory).  limit_ns = 0 restores the default, one
+ * second; a short limit is for tests that make a wait run out.  Host-only:
+ * applies to launches made after the call.
+ */
+moe_status moe_set_wait_limit(moe_handle* h, uint64_t limit_ns);
 
 #ifdef __cplusplus
 }

@@ -45,9 +45,13 @@ def gw_tolerance_ok(gw, gw_ref, g_norm, y_norm, rel=1e-3, floor=1e-6):
     return np.abs(gw - gw_ref) <= bound
 
 
+def entry_row_norms(rows_f32, pos):
+    """|rows[pos[t,k]]| per entry (0 for a dropped entry)."""
+    n = np.linalg.norm(rows_f32.astype(np.float64), axis=1)
+    return np.where(pos >= 0, n[np.clip(pos, 0, None)], 0.0)
+
+
 def row_norms_for_gw(g_f32, y_f32, pos):
     """|g_t| broadcast over k and |y[pos[t,k]]|, for the gw tolerance floor."""
     gn = np.linalg.norm(g_f32.astype(np.float64), axis=1)[:, None] * np.ones(pos.shape)
-    yn_rows = np.linalg.norm(y_f32.astype(np.float64), axis=1)
-    yn = np.where(pos >= 0, yn_rows[np.clip(pos, 0, None)], 0.0)
-    return gn, yn
+    return gn, entry_row_norms(y_f32, pos)

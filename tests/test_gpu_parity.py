@@ -15,7 +15,8 @@ import torch
 import combine_moe_route_05_gb300 as moe
 import oracle
 import synth
-from tests.common import assert_ulp, gw_tolerance_ok, row_norms_for_gw, ulp_dist
+from tests.common import (assert_ulp, entry_row_norms, gw_tolerance_ok, row_norms_for_gw,
+                          ulp_dist)
 from tests.gpu_util import SubLayout, dev, layout_host, oracle_route, router, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
@@ -265,12 +266,27 @@ def test_whole_path_captures_in_a_cuda_graph():
 # full size, the launch configuration the benchmark times
 
 
-@pytest.mark.parametrize("i", [3, 1])
+def sample_tokens(T, n=96, seed=1234):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([rng.choice(T, n, replace=False), [0, T - 1]]))
+
+
+@pytest.mark.parametrize("i", [3, 1, 2, 4])
 def test_full_size_sampled(i):
+    """Every stage at the workload's full size, in the launch configuration
+    the benchmark times: routing and the whole layout compared in full, the
+    row stages on the rows of 98 sampled tokens (first and last included).
+    Workload 2 keeps its skew at full size (heaviest expert above 5x the mean
+    load, exactly one expert with no token); workload 4 applies the scores to
+    the W2 input rows (scale_rows and its backward over all 262144 x 1536
+    rows) and combines with a plain sum."""
     wl = synth.WORKLOADS[i]
-    inp = synth.make_inputs(wl, want=("logits", "bias", "x", "y", "g"))
+    want = ("logits", "bias", "x", "y", "g") + (("h", "ghs") if wl.absorb else ())
+    inp = synth.make_inputs(wl, want=want)
     idx, w = oracle_route(wl, inp["logits"], inp["bias"])
     L = oracle.layout(idx, wl.E, wl.R)
+    if wl.bias == "zipf":
+        assert L.cnt_e.max() > 5 * wl.T * wl.K / wl.E and int((L.cnt_e == 0).sum()) == 1
     r = router(wl)
     gi, gwt = r.route(to_dev(inp["logits"]), to_dev(inp["bias"]))
     assert np.array_equal(to_host(gi), idx)
@@ -279,25 +295,47 @@ def test_full_size_sampled(i):
     got = layout_host(r)
     for f in oracle.Layout.FIELDS:
         assert np.array_equal(got[f].reshape(-1), getattr(L, f).reshape(-1)), f
+    assert int(got["S"][0]) == L.S
     x, y, g = to_dev(inp["x"]), to_dev(inp["y"]), to_dev(inp["g"])
+    cw = None if wl.absorb else gwt  # absorbed scores: plain-sum combine
     recv, recv_w, _ = r.dispatch(x, gwt)
-    out = r.combine(y, gwt)
-    gy, gw_ = r.combine_bwd(g, y, gwt)
+    out = r.combine(y, cw)
+    gy, gw_ = r.combine_bwd(g, y, cw)
     gx = r.dispatch_bwd(gy)
+    if wl.absorb:
+        hrows, ghs = to_dev(inp["h"]), to_dev(inp["ghs"])
+        hs = r.scale_rows(hrows, recv_w)
+        gh, gws = r.scale_rows_bwd(ghs, hrows, recv_w)
     torch.cuda.synchronize()
     assert moe.moe_read_device_status(r.h) == 0
 
-    rng = np.random.default_rng(1234)
-    tokens = np.unique(np.concatenate([rng.choice(wl.T, 96, replace=False), [0, wl.T - 1]]))
+    tokens = sample_tokens(wl.T)
     sub = SubLayout(L, tokens)
     rows = torch.from_numpy(sub.rows.astype(np.int64)).to(dev())
-    orecv, _, _ = oracle.dispatch(inp["x"][tokens], sub)
+    orecv, orw, _ = oracle.dispatch(inp["x"][tokens], sub, w[tokens])
     assert np.array_equal(to_host(recv.index_select(0, rows)), orecv)
-    oout = oracle.combine(sub.gather(inp["y"]), sub, w[tokens])
-    assert_ulp(to_host(out)[tokens], oout, 1, "out")
-    ogy, ogw = oracle.combine_bwd(inp["g"][tokens], sub.gather(inp["y"]), sub, w[tokens])
+    assert np.array_equal(to_host(recv_w.index_select(0, rows)), orw)
+    ysub = sub.gather(inp["y"])
+    ow = None if wl.absorb else w[tokens]
+    oout = oracle.combine(ysub, sub, ow)
+    d = assert_ulp(to_host(out)[tokens], oout, 1, "out")
+    assert int(d.max()) == 0
+    ogy, ogw = oracle.combine_bwd(inp["g"][tokens], ysub, sub, ow)
     assert_ulp(to_host(gy.index_select(0, rows)), ogy, 1, "gy")
-    gn, yn = row_norms_for_gw(rows_of(inp["g"][tokens]), rows_of(sub.gather(inp["y"])), sub.pos)
-    assert gw_tolerance_ok(to_host(gw_)[tokens], ogw, gn, yn).all()
+    if wl.absorb:
+        assert gw_ is None
+    else:
+        gn, yn = row_norms_for_gw(rows_of(inp["g"][tokens]), rows_of(ysub), sub.pos)
+        assert gw_tolerance_ok(to_host(gw_)[tokens], ogw, gn, yn).all()
     ogx = oracle.dispatch_bwd(ogy, sub)
-    assert_ulp(to_host(gx)[tokens], ogx, 1, "gx")
+    d = assert_ulp(to_host(gx)[tokens], ogx, 1, "gx")
+    assert int(d.max()) == 0
+    if wl.absorb:
+        hsub, ghsub = sub.gather(inp["h"]), sub.gather(inp["ghs"])
+        ohs = oracle.scale_rows(hsub, orw)
+        assert np.array_equal(to_host(hs.index_select(0, rows)), ohs)
+        ogh, ogws = oracle.scale_rows_bwd(ghsub, hsub, orw, sub)
+        assert np.array_equal(to_host(gh.index_select(0, rows)), ogh)
+        gn = entry_row_norms(oracle.bf16_to_f32(ghsub), sub.pos)
+        hn = entry_row_norms(oracle.bf16_to_f32(hsub), sub.pos)
+        assert gw_tolerance_ok(to_host(gws)[tokens], ogws, gn, hn).all()

@@ -86,3 +86,36 @@ def test_replica_seeds_are_deterministic_and_single_rank_keeps_the_base_seed():
 def test_reduce_max_is_identity_for_one_rank():
     import bench
     assert bench.reduce_max(3.5, 1) == 3.5
+
+
+def _env_without_ranks():
+    drop = ("RANK", "WORLD_SIZE", "LOCAL_RANK", "LOCAL_WORLD_SIZE", "MASTER_ADDR", "MASTER_PORT")
+    return {k: v for k, v in os.environ.items() if k not in drop}
+
+
+def test_bench_gpus_flag_starts_one_rank_per_gpu():
+    """`bench.py --gpus 2` started as a plain process runs itself again as two
+    ranks under torch.distributed.run.  The reference arm (the CPU oracle on
+    rank 0; the other ranks exit at once) needs no GPU, so the launch path is
+    exercised here: one JSON line, reporting both ranks."""
+    import json
+    import subprocess
+    import sys
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+           "--steps", "1", "--warmup", "3", "--workload", "1", "--ref-tokens", "16"]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=_env_without_ranks(), timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+
+
+def test_bench_rejects_a_rank_count_that_differs_from_gpus():
+    import subprocess
+    import sys
+    env = dict(_env_without_ranks(), WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+           "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 2 and "ranks were started" in r.stderr

@@ -71,3 +71,37 @@ def test_static_layout_rejects_sizes_beyond_its_scratch():
     st = moe.lib().moe_dispatch_layout_static(
         __import__("ctypes").byref(cfg), None, T, __import__("ctypes").byref(v), None, None)
     assert st == moe.MOE_ERR_CAPACITY
+
+
+def test_static_layout_two_launch_path_on_two_calls_in_a_row():
+    """A batch whose tiles do not all fit on the GPU at once (160000 tokens:
+    313 tiles of 512) takes the two-launch path, in which the count kernel's
+    last block uses and re-arms the arrival counter in the static array.  Two
+    calls in a row must each equal the handle-based layout and the oracle, and
+    a single-launch call after them must still be right."""
+    E, K, R, T = 16, 2, 4, 160000
+    wl = synth.Workload("two_launch", T=T, H=64, E=E, K=K, R=R)
+    assert moe.layout_sizes(T, K, E, R)["pos"] == T * K
+    assert (T + moe.MOE_LAYOUT_TILE_TOKENS - 1) // moe.MOE_LAYOUT_TILE_TOKENS * (E + R) \
+        <= moe.MOE_LAYOUT_STATIC_COUNTERS
+    rng = np.random.default_rng(11)
+    cfg = moe.make_config(E, K, R, T)
+    r = router(wl)
+    assert moe.moe_dispatch_layout_launches(r.h, T) == 2
+    for call in range(2):
+        idx = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int32)
+        d_idx = to_dev(idx)
+        ref = {k: v.clone() for k, v in r.layout(d_idx).items()}
+        out = empty_outputs(wl, T)
+        status = torch.zeros(1, dtype=torch.int32, device=dev())
+        moe.moe_dispatch_layout_static(cfg, d_idx, out, status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        for name in moe.LAYOUT_FIELDS:
+            assert torch.equal(out[name], ref[name].reshape(-1)), (call, name)
+        L = oracle.layout(idx, E, R)
+        for f in oracle.Layout.FIELDS:
+            assert np.array_equal(out[f].cpu().numpy(), getattr(L, f).reshape(-1)), (call, f)
+        assert int(out["S"].item()) == L.S
+    # back to the single launch on the same static array
+    test_static_layout_equals_handle_layout_on_two_calls_in_a_row()
