@@ -1,6 +1,6 @@
 // Router-score absorption fused into the W2 grouped GEMM, on the fifth-
-// generation tensor cores (tcgen05 MMA, accumulators in tensor memory, TMA
-// operand loads).
+// generation tensor cores (tcgen05 MMA on a CTA pair, accumulators in tensor
+// memory, TMA operand loads).
 //
 // What it computes ([Titan-absorb] "Implementation": the W2 input is scaled by
 // the routed score in float32 and restored to its dtype before the grouped
@@ -11,29 +11,46 @@
 // with W2 stored [E][H][I].  The scaling is the GEMM's prologue: the scaled
 // rows never reach HBM.  A pad row of a padded layout gets y = 0.
 //
-// A persistent CTA per SM walks 128 x 256 output tiles of the experts (a tile
-// never straddles two experts: each expert's segment is cut into 128-row
-// tiles, the last one ragged).  The scaled h slice is the MMA's A operand in
-// TENSOR memory, so shared memory carries only the TMA landings, the
-// prologue's read of h and the tensor cores' read of W2.  Warp roles:
-//   warp 2      TMA: h slices [128 x 64] into a 3-stage ring (128-byte
+// Persistent clusters of two CTAs (a CTA pair) walk 256 x 256 output tiles:
+// each CTA owns 128 rows (adjacent 128-row m-tiles of one expert; each
+// expert's segment is cut into 128-row tiles, the last one ragged) and half
+// of the tile's 256 W2 columns in shared memory.  One MMA instruction of the
+// pair, issued by the even CTA, multiplies all 256 rows by all 256 columns;
+// each CTA keeps its 128 x 256 accumulator in its own tensor memory.  Per CTA
+// and 64-wide K slice, shared memory carries 16 KB of h and 16 KB of W2
+// landed by TMA, 16 KB of h read by the prologue and 16 KB of W2 read by the
+// tensor cores: two thirds of what one CTA computing 128 x 256 tiles on its
+// own moves for the same products.
+//
+// Warp roles, in both CTAs:
+//   warp 2      TMA: h slices [128 x 64] into a 4-stage ring (128-byte
 //               swizzle), freed once the prologue has consumed them (after
 //               its tensor-memory store: the refill must not overtake the
 //               prologue's shared-memory loads);
-//   warp 0      TMA: W2 slices [256 x 64] into a 5-stage ring;
+//   warp 0      TMA: this CTA's half [128 x 64] of each W2 slice into an
+//               8-stage ring.  The copies of BOTH CTAs complete on the even
+//               CTA's `full` barrier of the stage (the pair form of the bulk
+//               tensor copy lets the barrier sit in the peer CTA), and the
+//               even CTA's producer announces the bytes of both halves;
 //   warps 3-10  prologue: read an h slice (one row per thread, half of its K
 //               range per warp), scale it by the row's score (fp32 product,
-//               bf16 round-to-nearest-even) and store it into the 32-column A
+//               bf16 round-to-nearest-even), store it into the 32-column A
 //               stage in tensor memory that pairs with the W2 stage of the
-//               same index (one barrier: both operands in place);
-//   warp 1      tensor memory (one 256-column accumulator + five A stages)
-//               and one thread issuing the MMAs (four K=16 steps per slice)
-//               and one commit per slice, freeing both operand stages;
+//               same index, and arrive on the even CTA's `full` barrier;
+//   warp 1      tensor memory (allocated by the pair together: one 256-column
+//               accumulator + eight A stages); in the even CTA one thread
+//               waits on `full` (both W2 halves and all sixteen A stores of
+//               the pair), issues the pair's MMAs (four K=16 steps per slice)
+//               and commits, once to each CTA's `empty` barrier of the stage
+//               and, per tile, to each CTA's `acc_full`;
 //   warps 11-18 epilogue: accumulator -> registers (two warps per lane
-//               quarter, half the columns each), accumulator handed back, then
-//               bf16 rows to HBM while the next tile's MMAs run.
+//               quarter, half the columns each), accumulator handed back (an
+//               arrival on the even CTA's `acc_empty`), then bf16 rows to HBM
+//               while the next tile's MMAs run.
 // Every wait is bounded; a wait that gives up raises MOE_DEVERR_TIMEOUT and
 // the CTA winds down (copies in flight are waited for, tensor memory freed).
+// No load is multicast: each CTA loads its own rows of h and its own half of
+// W2.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -42,38 +59,40 @@
 namespace moe {
 namespace {
 
-constexpr int kBM = 128;     // rows per tile: the MMA's M, one tensor-memory lane per row
-constexpr int kBN = 256;     // output columns per tile: the MMA's N
-constexpr int kBK = 64;      // contraction per stage: one 128-byte swizzle row of bf16
-constexpr int kUmmaK = 16;   // contraction per MMA instruction (16-bit operands)
-constexpr int kStagesA = 3;       // h slices in shared memory
-// W2 slices in shared memory and scaled h slices in tensor memory share one
-// ring index, so one barrier says "both operands of slice j are in place" and
-// one commit frees both
-constexpr int kStages = 5;
-constexpr int kPrologueWarps = 8; // two per lane quarter, half the K range each
-constexpr int kEpilogueWarps = 8; // two per lane quarter, half the columns each
+constexpr int kBM = 128;          // rows per CTA: the accumulator's tensor-memory lanes
+constexpr int kBN = 256;          // output columns per tile (the pair's MMA N)
+constexpr int kBNHalf = kBN / 2;  // W2 rows held by one CTA
+constexpr int kBK = 64;           // contraction per stage: one 128-byte swizzle row of bf16
+constexpr int kUmmaK = 16;        // contraction per MMA instruction (16-bit operands)
+constexpr int kStagesA = 4;       // h slices in shared memory
+// W2 half-slices in shared memory and scaled h slices in tensor memory share
+// one ring index: one barrier says "both operands of slice j are in place in
+// both CTAs", one commit per CTA frees both
+constexpr int kStages = 8;
+constexpr int kPrologueWarps = 8;  // two per lane quarter, half the K range each
+constexpr int kEpilogueWarps = 8;  // two per lane quarter, half the columns each
 constexpr int kFirstPrologueWarp = 3;
 constexpr int kFirstEpilogueWarp = kFirstPrologueWarp + kPrologueWarps;
 constexpr int kThreads = 32 * (kFirstEpilogueWarp + kEpilogueWarps);
 constexpr uint32_t kABytes = kBM * kBK * 2;
-constexpr uint32_t kBBytes = kBN * kBK * 2;
-constexpr uint32_t kAccCols = kBN;         // fp32 accumulator: a column per output column
-constexpr uint32_t kACols = kBK / 2;       // a scaled h slice: two bf16 per 32-bit column
-constexpr uint32_t kTmemCols = 512;        // accumulator + kStages A stages (power of 2)
+constexpr uint32_t kBBytes = kBNHalf * kBK * 2;
+constexpr uint32_t kAccCols = kBN;    // fp32 accumulator: a column per output column
+constexpr uint32_t kACols = kBK / 2;  // a scaled h slice: two bf16 per 32-bit column
+constexpr uint32_t kTmemCols = 512;   // accumulator + kStages A stages (power of 2)
 static_assert(kAccCols + kStages * kACols <= kTmemCols, "tensor memory budget");
-static_assert(8 * (2 * kStagesA + 2 * kStages + 2) + 16 <= 512, "barrier area");
+constexpr size_t kBarrierBytes = 512;
+static_assert(8 * (2 * kStagesA + 2 * kStages + 2) + 16 <= kBarrierBytes, "barrier area");
 // operand rings, barriers and the tables of at most MOE_MAX_EXPERTS experts
-constexpr size_t kBarrierBytes = 512;  // 34 mbarriers and the tensor-memory address
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStagesA * kABytes + kStages * kBBytes +
                               kBarrierBytes + sizeof(int32_t) * (3 * MOE_MAX_EXPERTS + 2);
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A
 // and B bf16 (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
-// in bits 17-22, M >> 4 in bits 24-28.
+// in bits 17-22, M >> 4 in bits 24-28; M = 256 rows over the CTA pair.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                             (static_cast<uint32_t>(kBN >> 3) << 17) |
-                            (static_cast<uint32_t>(kBM >> 4) << 24);
+                            (static_cast<uint32_t>((2 * kBM) >> 4) << 24);
 
 struct W2Args {
   const float* recv_w;
@@ -82,7 +101,7 @@ struct W2Args {
   __nv_bfloat16* y;
   uint32_t* flags;
   unsigned long long wait_ns;  // limit of every mbarrier wait
-  int rows;     // receive rows of h and y (T*K plus the pads)
+  int rows;                    // receive rows of h and y (T*K plus the pads)
   int E, I, H;
   int n_tiles;  // H / kBN
 };
@@ -109,27 +128,86 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // Wait for the phase of `bar` with the given parity; false after limit_ns.
+// Every wait and arrival here has the default semantics (acquire / release at
+// CTA scope), also across the pair: what crosses between the CTAs is tensor
+// memory (ordered by the tcgen05 fences around the barrier) and the bulk
+// copies (complete_tx makes them visible to the thread that observes the
+// phase).  Cluster-scope releases cost about 0.6 us each on this part, which
+// at one per slice and warp made the pair slower than a single CTA.
+// The test suspends the thread until the phase completes or about
+// kSuspendNs have passed, so that waiting warps (an epilogue waits a whole
+// tile) do not spend the issue slots the prologue needs.
+constexpr uint32_t kSuspendNs = 20000;
+
+__device__ __forceinline__ bool phase_done(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return done != 0;
+}
+
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity,
                                            unsigned long long limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (phase_done(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (;;) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (phase_done(bar, parity)) return true;
     if (global_ns() - t0 > limit_ns) return false;
   }
+}
+
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of both CTAs of the pair.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// Arrive on a barrier of either CTA of the pair (`cluster_bar`, a cluster
+// shared-memory address).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// Tensor copy into this CTA's shared memory, completing on a barrier of this
+// CTA.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
       "l"(map), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Tensor copy into this CTA's shared memory, completing on a barrier of
+// either CTA of the pair (`cluster_bar`, a cluster shared-memory address).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y,
+                                                 uint32_t cluster_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(cluster_bar)
       : "memory");
 }
 
@@ -140,15 +218,28 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T: A from tensor memory (lane = row, 32-bit
-// column j = bf16 elements 2j, 2j+1 of the row's K range).
-__device__ __forceinline__ void umma_bf16_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc,
-                                                 uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem]^T over the CTA pair (issued by the even
+// CTA): A rows 0-127 from this CTA's tensor memory and 128-255 from the
+// peer's, B columns 0-127 from this CTA's shared memory and 128-255 from the
+// peer's (same addresses); each CTA's tensor memory receives its 128 rows.
+// A in tensor memory: lane = row, 32-bit column j = bf16 elements 2j, 2j+1.
+__device__ __forceinline__ void umma_pair(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc,
+                                          uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %3, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t}" ::"r"(tmem_d),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %4, p;\n\t}" ::"r"(tmem_d),
       "r"(tmem_a), "l"(b_desc), "r"(accumulate), "r"(kIdesc)
+      : "memory");
+}
+
+// Arrive on the barrier at cluster shared-memory address `cluster_bar` (in
+// either CTA of the pair) once every MMA this thread issued so far has
+// completed.
+__device__ __forceinline__ void umma_commit_to(uint32_t cluster_bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          cluster_bar)
       : "memory");
 }
 
@@ -163,14 +254,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
       "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
       "r"(v[15])
-      : "memory");
-}
-
-// Arrive on `bar` once every MMA this thread issued so far has completed.
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_addr(bar))
       : "memory");
 }
 
@@ -196,7 +279,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // Shared-memory tables of one CTA: the layout's expert segments and, per
-// expert, the index of its first 128-row m-tile (tile_first[E] = all m-tiles).
+// expert, the index of its first pair of 128-row m-tiles (tile_first[E] = all
+// pairs).
 struct Tables {
   int32_t* tile_first;  // [E + 1]
   int32_t* off;         // [E + 1]
@@ -209,10 +293,13 @@ struct Tile {
   int real_end;  // end of the expert's real rows
 };
 
-// Tile `tile` (n-tile fastest) -> expert and rows: the last expert whose first
-// m-tile is <= the tile's m-tile (an empty expert shares its first m-tile with
-// the next expert and is never the last such one).
-__device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles, int tile) {
+// Pair tile `tile` (n-tile fastest) -> expert and this CTA's rows: the last
+// expert whose first pair is <= the tile's pair (an empty expert shares its
+// first pair with the next expert and is never the last such one).  CTA
+// `rank` takes m-tile 2 * pair + rank of the expert; past the expert's last
+// m-tile it has no rows (row0 >= seg_end) but still holds its W2 half.
+__device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles, int tile,
+                                            int rank) {
   const int mt = tile / n_tiles;
   int lo = 0, hi = E - 1;
   while (lo < hi) {
@@ -225,31 +312,32 @@ __device__ __forceinline__ Tile decode_tile(const Tables& tb, int E, int n_tiles
   Tile t;
   t.expert = lo;
   t.nt = tile - mt * n_tiles;
-  t.row0 = tb.off[lo] + (mt - tb.tile_first[lo]) * kBM;
+  t.row0 = tb.off[lo] + (2 * (mt - tb.tile_first[lo]) + rank) * kBM;
   t.seg_end = tb.off[lo + 1];
   t.real_end = tb.off[lo] + tb.cnt[lo];
   return t;
 }
 
-// Persistent: CTA b takes tiles b, b + gridDim.x, ... in every role, so the
-// roles walk the same sequence of (tile, K slice) jobs; each ring runs on
-// across tiles.
+// Persistent: pair p takes pair tiles p, p + npairs, ... in every role of
+// both CTAs, so all roles walk the same sequence of (tile, K slice) jobs;
+// each ring runs on across tiles.
 __global__ void __launch_bounds__(kThreads, 1)
     w2_absorbed_kernel(const __grid_constant__ CUtensorMap tm_h,
                        const __grid_constant__ CUtensorMap tm_w2, W2Args a) {
   extern __shared__ uint8_t smem_raw[];
   // operand tiles start on 1024-byte shared-memory boundaries (the swizzle
-  // pattern repeats every 8 rows of 128 bytes)
+  // pattern repeats every 8 rows of 128 bytes); the offsets are the same in
+  // both CTAs, as the pair's MMA requires
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;                       // [kStagesA][kBM x kBK] bf16, swizzled
-  uint8_t* sB = smem + kStagesA * kABytes;  // [kStages][kBN x kBK] bf16, swizzled
+  uint8_t* sB = smem + kStagesA * kABytes;  // [kStages][kBNHalf x kBK] bf16, swizzled
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
-  uint64_t* full_a = bars;                   // [kStagesA] h slice landed
-  uint64_t* free_a = full_a + kStagesA;      // [kStagesA] h slice read by the prologue
-  uint64_t* full = free_a + kStagesA;       // [kStages] W2 slice landed, scaled h slice stored
-  uint64_t* empty = full + kStages;         // [kStages] MMAs done with both
-  uint64_t* acc_full = empty + kStages;     // accumulator complete
-  uint64_t* acc_empty = acc_full + 1;        // accumulator drained
+  uint64_t* full_a = bars;               // [kStagesA] h slice landed
+  uint64_t* free_a = full_a + kStagesA;  // [kStagesA] h slice consumed by the prologue
+  uint64_t* full = free_a + kStagesA;    // [kStages] even CTA: both W2 halves, all A stores
+  uint64_t* empty = full + kStages;      // [kStages] the pair's MMAs done with the stage
+  uint64_t* acc_full = empty + kStages;  // accumulator complete
+  uint64_t* acc_empty = acc_full + 1;    // even CTA: both CTAs' accumulators drained
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
   Tables tb;
   tb.tile_first = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(bars) + kBarrierBytes);
@@ -258,10 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (a.I + kBK - 1) / kBK;
+  const int rank = static_cast<int>(cluster_rank());
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   // the segments, checked: 0 <= off[e] <= off[e] + cnt[e] <= off[e+1] <=
   // rows; a layout that breaks this (corrupted or not this handle's) raises
-  // MOE_DEVERR_BAD_LAYOUT and the kernel computes nothing
+  // MOE_DEVERR_BAD_LAYOUT and the kernel computes nothing (both CTAs of a
+  // pair read the same layout and decide alike)
   int bad = 0;
   for (int e = threadIdx.x; e <= a.E; e += kThreads) {
     const int lo = a.off_e[e];
@@ -273,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (__syncthreads_or(bad)) {
-    if (threadIdx.x == 0) raise_flag(a.flags, MOE_DEVERR_BAD_LAYOUT);
+    if (threadIdx.x == 0 && rank == 0) raise_flag(a.flags, MOE_DEVERR_BAD_LAYOUT);
     for (int e = threadIdx.x; e <= a.E; e += kThreads) {
       tb.off[e] = 0;
       if (e < a.E) tb.cnt[e] = 0;
@@ -281,11 +372,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (warp == 0) {
-    // exclusive scan of the per-expert m-tile counts
+    // exclusive scan of the per-expert counts of m-tile pairs
     int running = 0;
     for (int base = 0; base < a.E; base += 32) {
       const int e = base + lane;
-      const int tiles = e < a.E ? (tb.off[e + 1] - tb.off[e] + kBM - 1) / kBM : 0;
+      const int tiles = e < a.E ? ((tb.off[e + 1] - tb.off[e] + kBM - 1) / kBM + 1) / 2 : 0;
       int incl = tiles;
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
@@ -302,65 +393,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&free_a[s], kPrologueWarps);
       }
       for (int s = 0; s < kStages; ++s) {
-        mbar_init(&full[s], 1 + kPrologueWarps);  // W2 producer + prologue warps
-        mbar_init(&empty[s], 1);
+        // even CTA: its W2 producer's arrival (with both halves' bytes) and
+        // the prologue warps of both CTAs; the odd CTA's is unused
+        mbar_init(&full[s], 1 + 2 * kPrologueWarps);
+        mbar_init(&empty[s], 1);  // the pair's commit
       }
-      mbar_init(acc_full, 1);
-      mbar_init(acc_empty, kEpilogueWarps);
+      mbar_init(acc_full, 1);                    // the pair's commit
+      mbar_init(acc_empty, 2 * kEpilogueWarps);  // epilogue warps of both CTAs
       fence_mbar_init();
     }
   } else if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+    // the pair allocates together: one warp of each CTA
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  // the peer's barriers must be initialised before its arrivals, copies and
+  // commits can reach them
+  cluster_sync();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;     // accumulator: columns [0, 256)
+  const uint32_t tmem = *tmem_slot;         // accumulator: columns [0, 256)
   const uint32_t tmem_a = tmem + kAccCols;  // A stages: 32 columns each
   const int total = tb.tile_first[a.E] * a.n_tiles;
-  const int my_tiles =
-      blockIdx.x < total ? (total - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x : 0;
+  const int my_tiles = pair < total ? (total - pair + npairs - 1) / npairs : 0;
 
   bool ok = true;
   if (warp == 0 || warp == 2) {
-    // TMA producers: warp 0 the W2 slices, warp 2 the h slices
+    // TMA producers: warp 0 this CTA's halves of the W2 slices, warp 2 the h
+    // slices
     if (lane == 0) {
       const bool is_b = warp == 0;
       const int stages = is_b ? kStages : kStagesA;
-      uint64_t* landed = is_b ? full : full_a;
-      uint64_t* freed = is_b ? empty : free_a;
       int it = 0;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const Tile t = decode_tile(tb, a.E, a.n_tiles, tile);
+      for (int tile = pair; tile < total && ok; tile += npairs) {
+        const Tile t = decode_tile(tb, a.E, a.n_tiles, tile, rank);
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % stages;
           const uint32_t ph = (it / stages) & 1u;
-          if (it >= stages && !wait_phase(&freed[s], ph ^ 1u, a.wait_ns)) {
-            ok = false;
-            break;
-          }
           if (is_b) {
-            mbar_arrive_expect_tx(&landed[s], kBBytes);
-            tma_load_2d(sB + s * kBBytes, &tm_w2, kb * kBK, t.expert * a.H + t.nt * kBN, &landed[s]);
+            // the stage is free in both CTAs once the pair's MMAs that read
+            // it have completed (a commit reaches each CTA's `empty`)
+            if (it >= stages && !wait_phase(&empty[s], ph ^ 1u, a.wait_ns)) {
+              ok = false;
+              break;
+            }
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * kBBytes);
+            tma_load_2d_pair(sB + s * kBBytes, &tm_w2, kb * kBK,
+                             t.expert * a.H + t.nt * kBN + rank * kBNHalf,
+                             cluster_addr(&full[s], 0));
           } else {
-            mbar_arrive_expect_tx(&landed[s], kABytes);
-            tma_load_2d(sA + s * kABytes, &tm_h, kb * kBK, t.row0, &landed[s]);
+            if (it >= stages && !wait_phase(&free_a[s], ph ^ 1u, a.wait_ns)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full_a[s], kABytes);
+            tma_load_2d(sA + s * kABytes, &tm_h, kb * kBK, t.row0, &full_a[s]);
           }
         }
       }
-      // the last copies must have landed before the CTA may exit
-      // (the W2 barrier also needs the prologue's arrivals; its phases for the
-      // last slices complete once the prologue has stored them)
-      for (int j = it - stages < 0 ? 0 : it - stages; j < it; ++j)
-        if (!wait_phase(&landed[j % stages], (j / stages) & 1u, a.wait_ns)) ok = false;
+      // the last copies must have landed before the CTA may exit: for h, its
+      // own barrier says so; for W2, the pair's last commits on this CTA's
+      // stages (the MMAs that read a stage ran after its copies landed)
+      for (int j = it - stages < 0 ? 0 : it - stages; j < it; ++j) {
+        if (is_b) {
+          if (!wait_phase(&empty[j % stages], (j / stages) & 1u, a.wait_ns)) ok = false;
+        } else if (!wait_phase(&full_a[j % stages], (j / stages) & 1u, a.wait_ns)) {
+          ok = false;
+        }
+      }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int it = 0, n = 0;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
+      const uint32_t acc_full_peer = cluster_addr(acc_full, 1);
+      for (int tile = pair; tile < total && ok; tile += npairs, ++n) {
         if (n >= 1 && !wait_phase(acc_empty, (n - 1) & 1u, a.wait_ns)) {
           ok = false;
           break;
@@ -376,11 +484,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b0 = smem_addr(sB + s * kBBytes);
 #pragma unroll
           for (int k = 0; k < kBK / kUmmaK; ++k)
-            umma_bf16_tmem_a(tmem, tmem_a + s * kACols + k * (kUmmaK / 2),
-                             sw128_desc(b0 + k * kUmmaK * 2), (kb | k) != 0);
-          umma_commit(&empty[s]);
+            umma_pair(tmem, tmem_a + s * kACols + k * (kUmmaK / 2),
+                      sw128_desc(b0 + k * kUmmaK * 2), (kb | k) != 0);
+          // frees the stage in both CTAs
+          umma_commit_to(smem_addr(&empty[s]));
+          umma_commit_to(cluster_addr(&empty[s], 1));
         }
-        umma_commit(acc_full);
+        if (!ok) break;
+        umma_commit_to(smem_addr(acc_full));
+        umma_commit_to(acc_full_peer);
       }
     }
   } else if (warp < kFirstEpilogueWarp) {
@@ -392,20 +504,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
     auto score_of = [&](int tile) {
       if (tile >= total) return 0.0f;
-      const Tile t = decode_tile(tb, a.E, a.n_tiles, tile);
+      const Tile t = decode_tile(tb, a.E, a.n_tiles, tile, rank);
       const int row = t.row0 + prow;
       return row < t.real_end ? __ldg(a.recv_w + row) : 0.0f;
     };
-    float next_score = score_of(blockIdx.x);
+    float next_score = score_of(pair);
     int it = 0;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+    for (int tile = pair; tile < total && ok; tile += npairs) {
       const float score = next_score;
-      next_score = score_of(tile + gridDim.x);
+      next_score = score_of(tile + npairs);
       for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int sa = it % kStagesA, st = it % kStages;
+        const int sa = it % kStagesA, s = it % kStages;
         // each lane waits itself (acquiring the copy); the warp leaves together
         bool got = wait_phase(&full_a[sa], (it / kStagesA) & 1u, a.wait_ns);
-        if (got && it >= kStages) got = wait_phase(&empty[st], ((it / kStages) & 1u) ^ 1u, a.wait_ns);
+        if (got && it >= kStages)
+          got = wait_phase(&empty[s], ((it / kStages) & 1u) ^ 1u, a.wait_ns);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
@@ -428,12 +541,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             packed[c * 4 + j] = pack_bf16x2(lo, hi);
           }
         }
-        tmem_st16(tmem_a + lane_bits + st * kACols + kh * 16, packed);
+        tmem_st16(tmem_a + lane_bits + s * kACols + kh * 16, packed);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&free_a[sa]);  // the h slice may be refilled
-          mbar_arrive(&full[st]);
+          // the h slice may be refilled only after the store above consumed
+          // the loaded values; the even CTA's MMA needs this A stage
+          mbar_arrive(&free_a[sa]);
+          mbar_arrive_cluster(cluster_addr(&full[s], 0));
         }
       }
     }
@@ -442,9 +557,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ch of the accumulator
     const int q = warp & 3;
     const int ch = (warp - kFirstEpilogueWarp) >> 2;
+    const uint32_t acc_empty_even = cluster_addr(acc_empty, 0);
     int n = 0;
-    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++n) {
-      const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile);
+    for (int tile = pair; tile < total && ok; tile += npairs, ++n) {
+      const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile, rank);
       if (!__all_sync(0xffffffffu, wait_phase(acc_full, n & 1u, a.wait_ns))) {
         ok = false;
         break;
@@ -469,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();  // the loads above precede the MMAs that reuse the columns
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
+      if (lane == 0) mbar_arrive_cluster(acc_empty_even);
       if (real || pad) {
 #pragma unroll
         for (int j = 0; j < kBN / 2 / 8; ++j) {
@@ -485,16 +601,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (!ok) raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
   tc_fence_before();
-  __syncthreads();
+  // neither CTA leaves while the other may still reach its shared memory or
+  // tensor memory
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     // every MMA must be complete before the columns are released: wait for
     // the last tile's accumulator commit (on the normal path the epilogue
     // already has, and this returns at once)
-    if (lane == 0 && my_tiles > 0 && !wait_phase(acc_full, (my_tiles - 1) & 1u, a.wait_ns))
+    if (lane == 0 && my_tiles > 0 &&
+        !wait_phase(acc_full, (my_tiles - 1) & 1u, a.wait_ns))
       raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
     __syncwarp();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
   }
@@ -548,9 +667,10 @@ cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, co
   const long long rows_cap = static_cast<long long>(h->T) * c.top_k +
                              static_cast<long long>(E) * (h->pad - 1);
   if (rows_cap <= 0) return cudaSuccess;
+  if (static_cast<long long>(E) * H > 0x7fffffffLL) return cudaErrorInvalidValue;
   CUtensorMap tm_h, tm_w2;
   if (!encode_rows(&tm_h, hrows, static_cast<uint64_t>(rows_cap), I, kBM) ||
-      !encode_rows(&tm_w2, w2, static_cast<uint64_t>(E) * H, I, kBN))
+      !encode_rows(&tm_w2, w2, static_cast<uint64_t>(E) * H, I, kBNHalf))
     return cudaErrorInvalidValue;
   W2Args a;
   a.recv_w = recv_w;
@@ -564,16 +684,37 @@ cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, co
   a.I = I;
   a.H = H;
   a.n_tiles = H / kBN;
-  // sum over experts of ceil(segment / kBM) <= (rows + E * (kBM - 1)) / kBM
+  // sum over experts of ceil(ceil(segment / kBM) / 2) <= pair tiles below
   const long long m_tiles = (rows_cap + static_cast<long long>(E) * (kBM - 1)) / kBM;
-  const long long tiles = m_tiles * a.n_tiles;
-  if (static_cast<long long>(E) * H > 0x7fffffffLL) return cudaErrorInvalidValue;
-  if (tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-  // one CTA per SM (the operand ring fills its shared memory), never more
-  // CTAs than tiles could exist
-  const int grid = static_cast<int>(tiles < h->num_sms ? tiles : h->num_sms);
-  w2_absorbed_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_h, tm_w2, a);
-  return cudaGetLastError();
+  const long long pair_tiles = ((m_tiles + E) / 2) * a.n_tiles;
+  if (pair_tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+  // CTA pairs in clusters of two, as many as can be resident at once (one
+  // CTA per SM: the rings fill its shared memory), never more than there
+  // can be pair tiles
+  static int max_pairs[64] = {0};
+  const int dev = h->device >= 0 && h->device < 64 ? h->device : 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (max_pairs[dev] == 0) {
+    cfg.gridDim = dim3(2 * (h->num_sms / 2), 1, 1);
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, w2_absorbed_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_pairs[dev] = n;
+  }
+  const long long pairs = pair_tiles < max_pairs[dev] ? pair_tiles : max_pairs[dev];
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * (pairs < 1 ? 1 : pairs)), 1, 1);
+  return cudaLaunchKernelEx(&cfg, w2_absorbed_kernel, tm_h, tm_w2, a);
 }
 
 }  // namespace moe
