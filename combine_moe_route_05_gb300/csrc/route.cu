@@ -29,6 +29,7 @@
 // together, one (token, k) per lane, so each fp64 instruction serves TB
 // tokens.
 #include <cfloat>
+#include <cmath>
 #include <climits>
 
 #include "common.cuh"
@@ -43,6 +44,11 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr float kDeltaAbs = 5e-7f;
 constexpr float kDeltaRel = 1.25e-7f;
 
+// A float-float value hi + lo (see the routing weights below).
+struct FF {
+  float hi, lo;
+};
+
 struct RouteArgs {
   const float* logits;
   const float* bias;
@@ -52,6 +58,8 @@ struct RouteArgs {
   int vec4;
   int fast;  // the fp32 selection applies to this configuration
   double scale;
+  FF scale_ff;      // scale as float-float
+  int scale_ff_ok;  // scale is 0 or within [2^-60, 2^60] in magnitude, exact to 2^-48 as FF
   int32_t* idx;
   float* w;
   uint32_t* flags;
@@ -597,6 +605,187 @@ __device__ __forceinline__ double rcp_weight(double d) {
   return fma(r0, fma(-d, r0, 1.0), r0);
 }
 
+// ---------------------------------------------------------------------------
+// The weights in float-float arithmetic (a value is hi + lo, two fp32 with
+// |lo| <= half an ulp of hi): Dekker's and Knuth's error-free sum and product
+// steps with fused multiply-add, about 2^-44 relative overall, so each fp32
+// weight is the fp64 reference's rounding or one ulp from it (only where the
+// exact value lies within about 2^-20 ulp of a rounding midpoint).  fp32 issues
+// many times faster than fp64 on this part, which is what bounds the weights.
+// Tokens with a non-finite selected logit, or sigmoid logits below -700
+// (where the fp64 reference's exp overflows and its weights become 0 or
+// NaN), keep the fp64 path; the decision is per warp.
+
+__device__ __forceinline__ FF ff_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+
+// |a| >= |b| (or a = 0)
+__device__ __forceinline__ FF ff_fast_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  FF s = ff_two_sum(a.hi, b.hi);
+  const FF t = ff_two_sum(a.lo, b.lo);
+  s = ff_fast_two_sum(s.hi, __fadd_rn(s.lo, t.hi));
+  return ff_fast_two_sum(s.hi, __fadd_rn(s.lo, t.lo));
+}
+
+__device__ __forceinline__ FF ff_mul(FF a, FF b) {
+  const float p = __fmul_rn(a.hi, b.hi);
+  float e = __fmaf_rn(a.hi, b.hi, -p);
+  e = __fmaf_rn(a.hi, b.lo, e);
+  e = __fmaf_rn(a.lo, b.hi, e);
+  return ff_fast_two_sum(p, e);
+}
+
+// a / b for b > 0 in the normal range: the rounded quotient, then the
+// quotient of the exact remainder
+__device__ __forceinline__ FF ff_div(FF a, FF b) {
+  const float q1 = __fdiv_rn(a.hi, b.hi);
+  const float p = __fmul_rn(q1, b.hi);
+  const float pe = __fmaf_rn(q1, b.hi, -p);
+  float r = __fsub_rn(a.hi, p);  // exact: p is within a few ulps of a.hi
+  r = __fsub_rn(r, pe);
+  r = __fadd_rn(r, a.lo);
+  r = __fmaf_rn(-q1, b.lo, r);
+  return ff_fast_two_sum(q1, __fdiv_rn(r, b.hi));
+}
+
+// 2^e for e in [-126, 127]
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+
+// v * 2^e for e <= 0 (both parts; what falls below the fp32 range is lost,
+// which only happens to terms far below the sums they enter)
+__device__ __forceinline__ FF ff_scale(FF v, int e) {
+  if (e < -250) return {0.0f, 0.0f};
+  const int e1 = e < -125 ? -125 : e;  // both factors within pow2f's range
+  const float f1 = pow2f(e1), f2 = pow2f(e - e1);
+  return {__fmul_rn(__fmul_rn(v.hi, f1), f2), __fmul_rn(__fmul_rn(v.lo, f1), f2)};
+}
+
+// The fp32 weight round(v * 2^e), e <= 0, v > 0 in the normal range: v.hi is
+// v rounded to fp32, so in the normal range the scaled v.hi is the rounding;
+// below it one rounding of v.hi * 2^e (the first factor keeps the product
+// normal and exact)
+__device__ __forceinline__ float ff_to_weight(FF v, int e) {
+  if (e < -160) return 0.0f;
+  const int e1 = e < -100 ? -100 : e;
+  return __fmul_rn(__fmul_rn(v.hi, pow2f(e1)), pow2f(e - e1));
+}
+
+// ln 2 = kLn2A + kLn2B + kLn2C: kLn2A = 355/512 has 9 significant bits, so
+// n * kLn2A is exact for |n| < 2^15
+constexpr float kLn2A = 0.693359375f;
+constexpr float kLn2B = -0x1.bd0106p-13f;
+constexpr float kLn2C = 0x1.cf79acp-40f;
+constexpr float kLog2E = 0x1.715476p+0f;
+
+// e^r for |r| <= 0.35 (float-float r): the Taylor polynomial of degree 11,
+// whose truncation error is below 0.35^12 / 12! = 2^-47; the terms of
+// degree 7 and up (below 2^-12 of the sum) in plain fp32, the rest with
+// float-float coefficients 1/k!
+__device__ __forceinline__ FF ff_exp_reduced(FF r) {
+  const FF c[7] = {{1.0f, 0.0f},
+                   {1.0f, 0.0f},
+                   {0.5f, 0.0f},
+                   {0x1.555556p-3f, -0x1.555556p-28f},
+                   {0x1.555556p-5f, -0x1.555556p-30f},
+                   {0x1.111112p-7f, -0x1.dddddep-32f},
+                   {0x1.6c16c2p-10f, -0x1.27d27ep-35f}};
+  float t = 0x1.ae6456p-26f;  // 1/11!
+  t = __fmaf_rn(t, r.hi, 0x1.27e4fcp-22f);
+  t = __fmaf_rn(t, r.hi, 0x1.71de3ap-19f);
+  t = __fmaf_rn(t, r.hi, 0x1.a01a02p-16f);
+  t = __fmaf_rn(t, r.hi, 0x1.a01a02p-13f);
+  FF p = {t, 0.0f};
+#pragma unroll
+  for (int k = 6; k >= 0; --k) p = ff_add(ff_mul(p, r), c[k]);
+  return p;
+}
+
+// e^x = m * 2^n for x <= 0, x.hi >= -760: n = round(x / ln 2) and
+// m = e^(x - n ln 2) in [0.70, 1.42]; the reduced argument is exact to
+// about 2^-60 (x.hi - n kLn2A is exact, n kLn2B is split exactly)
+__device__ __forceinline__ FF ff_exp_nonpos(FF x, int& n) {
+  const float nf = rintf(__fmul_rn(x.hi, kLog2E));
+  n = static_cast<int>(nf);
+  FF r = ff_two_sum(__fmaf_rn(-nf, kLn2A, x.hi), x.lo);
+  const float b = __fmul_rn(-nf, kLn2B);
+  r = ff_add(r, FF{b, __fmaf_rn(-nf, kLn2B, -b)});
+  r = ff_add(r, FF{__fmul_rn(-nf, kLn2C), 0.0f});
+  return ff_exp_reduced(r);
+}
+
+// The token's K entries sit on lanes base .. base + K - 1.  Sum over them:
+// a butterfly when K is a power of two, else in k order.
+__device__ __forceinline__ FF ff_token_sum(FF v, int base, int K) {
+  if ((K & (K - 1)) == 0) {
+    for (int off = 1; off < K; off <<= 1)
+      v = ff_add(v, FF{__shfl_xor_sync(kFull, v.hi, off), __shfl_xor_sync(kFull, v.lo, off)});
+    return v;
+  }
+  FF s{0.0f, 0.0f};
+  for (int k = 0; k < K; ++k)
+    s = ff_add(s, FF{__shfl_sync(kFull, v.hi, (base + k) & 31), __shfl_sync(kFull, v.lo, (base + k) & 31)});
+  return s;
+}
+
+__device__ __forceinline__ int token_max(int v, int base, int K) {
+  if ((K & (K - 1)) == 0) {
+    for (int off = 1; off < K; off <<= 1) v = max(v, __shfl_xor_sync(kFull, v, off));
+    return v;
+  }
+  int m = INT_MIN;
+  for (int k = 0; k < K; ++k) m = max(m, __shfl_sync(kFull, v, (base + k) & 31));
+  return m;
+}
+
+// The fp32 weight of this lane's entry (logit l of the token whose entries
+// sit on lanes base ..), as the fp64 definition gives it; every lane of the
+// warp calls it together.
+template <bool SIGMOID>
+__device__ __forceinline__ float weight_ff(const RouteArgs& a, float l, int base) {
+  FF m;
+  int n;
+  if (!SIGMOID) {
+    // e^(l - l_max) / sum over the selected; l_max is the first pick, so the
+    // sum is at least 1 and every exponent is <= 0
+    const float top = __shfl_sync(kFull, l, base & 31);
+    const FF d = ff_two_sum(l, -top);  // exact
+    if (d.hi < -104.0f) {
+      m = FF{0.0f, 0.0f};  // its weight is below half the smallest subnormal
+      n = 0;
+    } else {
+      m = ff_exp_nonpos(d, n);
+    }
+    const FF den = ff_token_sum(ff_scale(m, n), base, a.K);
+    return ff_to_weight(ff_mul(ff_div(m, den), a.scale_ff), n);
+  }
+  // s = 1 / (1 + e^-l) = m 2^n: for l >= 0 from e^-l, for l < 0 as
+  // e^l / (1 + e^l) (no overflow)
+  const FF x{-fabsf(l), 0.0f};
+  int ne;
+  const FF e = ff_exp_nonpos(x, ne);
+  const FF onep = ff_add(FF{1.0f, 0.0f}, ff_scale(e, ne));
+  if (l >= 0.0f) {
+    m = ff_div(FF{1.0f, 0.0f}, onep);
+    n = 0;
+  } else {
+    m = ff_div(e, onep);
+    n = ne;
+  }
+  if (!a.renorm) return ff_to_weight(ff_mul(m, a.scale_ff), n);
+  // s_k / sum_j s_j, each term scaled by the largest 2^n of the token
+  const int N = token_max(n, base, a.K);
+  const FF den = ff_token_sum(ff_scale(m, n - N), base, a.K);
+  return ff_to_weight(ff_mul(ff_div(m, den), a.scale_ff), n - N);
+}
+
 template <int VPL, bool SIGMOID>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
   extern __shared__ double route_smem[];
@@ -638,28 +827,38 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
         softmax_token_full<VPL>(a, t, lane);
       }
     }
-    // fp64 weights of the tokens selected in fp32: lane = (token j, rank k)
+    // weights of the tokens selected in fp32: lane = (token j, rank k);
+    // float-float unless a token of the warp has a selected logit outside its
+    // range (then fp64)
     const int t = wid + (i0 + j_of_lane) * W;
-    double val;
-    if (SIGMOID) {
-      val = rcp_weight(1.0 + exp_weight(-static_cast<double>(my_logit)));
+    const bool in_range = isfinite(my_logit) && (!SIGMOID || my_logit >= -700.0f);
+    const int base = (j_of_lane * a.K) & 31;
+    float wv;
+    if (a.scale_ff_ok && __all_sync(kFull, !my_fast || in_range)) {
+      wv = weight_ff<SIGMOID>(a, my_fast ? my_logit : 0.0f, base);
     } else {
-      const float top = __shfl_sync(kFull, my_logit, (j_of_lane * a.K) & 31);
-      val = exp_weight(static_cast<double>(my_logit) - static_cast<double>(top));
-    }
-    // the sum over the token's K lanes: a butterfly when K is a power of two
-    // (every lane then holds the same bits), else in k order
-    double den = 0.0;
-    if ((a.K & (a.K - 1)) == 0) {
-      den = val;
-      for (int off = 1; off < a.K; off <<= 1) den += __shfl_xor_sync(kFull, den, off);
-    } else {
-      for (int k = 0; k < a.K; ++k) den += __shfl_sync(kFull, val, (j_of_lane * a.K + k) & 31);
+      double val;
+      if (SIGMOID) {
+        val = rcp_weight(1.0 + exp_weight(-static_cast<double>(my_logit)));
+      } else {
+        const float top = __shfl_sync(kFull, my_logit, base);
+        val = exp_weight(static_cast<double>(my_logit) - static_cast<double>(top));
+      }
+      // the sum over the token's K lanes: a butterfly when K is a power of
+      // two (every lane then holds the same bits), else in k order
+      double den = 0.0;
+      if ((a.K & (a.K - 1)) == 0) {
+        den = val;
+        for (int off = 1; off < a.K; off <<= 1) den += __shfl_xor_sync(kFull, den, off);
+      } else {
+        for (int k = 0; k < a.K; ++k) den += __shfl_sync(kFull, val, (j_of_lane * a.K + k) & 31);
+      }
+      const double p = (SIGMOID && !a.renorm) ? val : val * rcp_weight(den);
+      wv = static_cast<float>(p * a.scale);
     }
     if (my_fast && j_of_lane < TB && t < a.T) {
-      const double p = (SIGMOID && !a.renorm) ? val : val * rcp_weight(den);
       a.idx[static_cast<size_t>(t) * a.K + k_of_lane] = my_idx;
-      a.w[static_cast<size_t>(t) * a.K + k_of_lane] = static_cast<float>(p * a.scale);
+      a.w[static_cast<size_t>(t) * a.K + k_of_lane] = wv;
     }
   }
 }
@@ -796,6 +995,12 @@ cudaError_t launch_route_topk(const moe_handle* h, const float* logits, const fl
   a.renorm = c.renorm;
   a.vec4 = (c.num_experts % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
   a.scale = c.route_scale;
+  {
+    const double sc = c.route_scale;
+    const float sh = static_cast<float>(sc);
+    a.scale_ff = FF{sh, static_cast<float>(sc - static_cast<double>(sh))};
+    a.scale_ff_ok = sc == 0.0 || (std::fabs(sc) >= 0x1p-60 && std::fabs(sc) <= 0x1p60);
+  }
   a.idx = idx;
   a.w = w;
   a.flags = h->flags;
