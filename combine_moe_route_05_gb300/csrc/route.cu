@@ -13,10 +13,13 @@
 // on this GPU, so the kernel first selects on fp32 keys and keeps that result
 // only when it provably equals the fp64 one:
 //   |key32 - key64| <= DELTA = 5e-7 + 1.25e-7 * max|key32| for every expert
-// (expf is accurate to 2 ulp, i.e. 2^-22 relative; 1 + e and the reciprocal
-// are each rounded once, 2^-24; so the sigmoid is within 1.5 * 2^-22 of its
-// value, at most 3.6e-7 since it is <= 1; adding the bias rounds once more,
-// 2^-24 |key|; fp64 keys are exact to 1e-15).  A group score (sum of the
+// (the fast e^-l is documented within 2 + floor(1.173 |l|) ulp, a relative
+// error that moves s = 1 / (1 + e^-l) by at most s (1 - s) times it, below
+// 7.5e-8 for every l; 1 + e^-l rounds once, 6e-8 in s; the fast division is
+// documented within 2 ulp, 2.4e-7 at s <= 1, and returns 0 for divisors above
+// 2^126, where s < 2^-126; so the sigmoid is within 3.8e-7 of its value;
+// adding the bias rounds once more, 2^-24 |key|; fp64 keys are exact to
+// 1e-15).  A group score (sum of the
 // group's top GK keys) is then within GK * (DELTA + 1.25e-7 * max|gs|) of the
 // fp64 one, since a top-m sum moves by at most m times the largest change of
 // its inputs.  If the fp32 gap between the last kept and the first dropped
@@ -358,10 +361,16 @@ __device__ __forceinline__ double key_fp64(const RouteArgs& a, int e, float l) {
   return s + (a.bias ? static_cast<double>(__ldg(a.bias + e)) : 0.0);
 }
 
-// The fp32 selection key (sigmoid + bias), the same expression everywhere.
+// The fp32 selection key (sigmoid + bias), the same expression everywhere:
+// the fast exponential and the fast division (their documented error bounds
+// enter DELTA above).
+__device__ __forceinline__ float sigmoid_key(float l, float b) {
+  const float s = __fdividef(1.0f, __fadd_rn(1.0f, __expf(-l)));
+  return __fadd_rn(s, b);
+}
+
 __device__ __forceinline__ float key_fp32(const RouteArgs& a, int e, float l) {
-  const float s = __frcp_rn(__fadd_rn(1.0f, expf(-l)));
-  return __fadd_rn(s, a.bias ? __ldg(a.bias + e) : 0.0f);
+  return sigmoid_key(l, a.bias ? __ldg(a.bias + e) : 0.0f);
 }
 
 // Gathers the lanes' candidate experts (bit j of `mask`: expert lane*VPL + j)
@@ -786,6 +795,73 @@ __device__ __forceinline__ float weight_ff(const RouteArgs& a, float l, int base
   return ff_to_weight(ff_mul(ff_div(m, den), a.scale_ff), n - N);
 }
 
+// Routes the tokens t0, t0 + stride, ..., count of them (at most 32 / K),
+// with the whole warp: the selection one token at a time, then the weights of
+// all of them in one pass, lane j * K + k holding rank k of token j.
+template <int VPL, bool SIGMOID>
+__device__ __forceinline__ void warp_route_tokens(const RouteArgs& a, int t0, int stride, int count,
+                                                  int lane, double* wkeys, int2* list) {
+  const int j_of_lane = lane / a.K, k_of_lane = lane % a.K;
+  int my_idx = 0;
+  float my_logit = 0.0f;
+  bool my_fast = false;
+  for (int j = 0; j < count; ++j) {
+    const int t = t0 + j * stride;
+    float v[VPL];
+    const bool bad = load_logits<VPL>(a, t, lane, v);
+    if (__any_sync(kFull, bad) && lane == 0) raise_flag(a.flags, MOE_DEVERR_NONFINITE);
+    // a softmax selection on fp32 logits is exact even with infinities; a
+    // sigmoid token with a non-finite logit goes to the fp64 path
+    const bool use_fast = a.fast && !(SIGMOID && __any_sync(kFull, bad));
+    int sel_idx = 0;
+    const bool ok = use_fast && select_fp32<VPL, SIGMOID>(a, t, lane, v, j * a.K, sel_idx, list);
+    if (ok) {
+      if (j_of_lane == j) {
+        my_idx = sel_idx;
+        my_logit = __ldg(a.logits + static_cast<size_t>(t) * a.E + sel_idx);
+        my_fast = true;
+      }
+    } else if (SIGMOID) {
+      sigmoid_token_fp64<VPL>(a, t, lane, wkeys);
+    } else {
+      softmax_token_full<VPL>(a, t, lane);
+    }
+  }
+  // weights of the tokens selected in fp32: lane = (token j, rank k);
+  // float-float unless a token of the warp has a selected logit outside its
+  // range (then fp64)
+  const int t = t0 + j_of_lane * stride;
+  const bool in_range = isfinite(my_logit) && (!SIGMOID || my_logit >= -700.0f);
+  const int base = (j_of_lane * a.K) & 31;
+  float wv;
+  if (a.scale_ff_ok && __all_sync(kFull, !my_fast || in_range)) {
+    wv = weight_ff<SIGMOID>(a, my_fast ? my_logit : 0.0f, base);
+  } else {
+    double val;
+    if (SIGMOID) {
+      val = rcp_weight(1.0 + exp_weight(-static_cast<double>(my_logit)));
+    } else {
+      const float top = __shfl_sync(kFull, my_logit, base);
+      val = exp_weight(static_cast<double>(my_logit) - static_cast<double>(top));
+    }
+    // the sum over the token's K lanes: a butterfly when K is a power of
+    // two (every lane then holds the same bits), else in k order
+    double den = 0.0;
+    if ((a.K & (a.K - 1)) == 0) {
+      den = val;
+      for (int off = 1; off < a.K; off <<= 1) den += __shfl_xor_sync(kFull, den, off);
+    } else {
+      for (int k = 0; k < a.K; ++k) den += __shfl_sync(kFull, val, (j_of_lane * a.K + k) & 31);
+    }
+    const double p = (SIGMOID && !a.renorm) ? val : val * rcp_weight(den);
+    wv = static_cast<float>(p * a.scale);
+  }
+  if (my_fast && j_of_lane < count) {
+    a.idx[static_cast<size_t>(t) * a.K + k_of_lane] = my_idx;
+    a.w[static_cast<size_t>(t) * a.K + k_of_lane] = wv;
+  }
+}
+
 template <int VPL, bool SIGMOID>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
   extern __shared__ double route_smem[];
@@ -793,74 +869,323 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
   double* wkeys = route_smem + (threadIdx.x >> 5) * a.E;
   int2* list = cand_lists[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
-  const int TB = 32 / a.K;  // tokens per fp64 weight pass
+  const int TB = 32 / a.K;  // tokens per weight pass
   // persistent grid: warp w takes tokens w, w + W, w + 2W, ... (W warps in
   // all), TB at a time, so every warp gets the same number of tokens to
   // within one
   const int W = gridDim.x * kRouteWarps;
   const int wid = blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
-  const int j_of_lane = lane / a.K, k_of_lane = lane % a.K;
   for (int i0 = 0; wid + i0 * W < a.T; i0 += TB) {
-    int my_idx = 0;
-    float my_logit = 0.0f;
-    bool my_fast = false;
-    for (int j = 0; j < TB; ++j) {
-      const int t = wid + (i0 + j) * W;
-      if (t >= a.T) break;
-      float v[VPL];
-      const bool bad = load_logits<VPL>(a, t, lane, v);
-      if (__any_sync(kFull, bad) && lane == 0) raise_flag(a.flags, MOE_DEVERR_NONFINITE);
-      // a softmax selection on fp32 logits is exact even with infinities; a
-      // sigmoid token with a non-finite logit goes to the fp64 path
-      const bool use_fast = a.fast && !(SIGMOID && __any_sync(kFull, bad));
-      int sel_idx = 0;
-      const bool ok = use_fast && select_fp32<VPL, SIGMOID>(a, t, lane, v, j * a.K, sel_idx, list);
-      if (ok) {
-        if (j_of_lane == j) {
-          my_idx = sel_idx;
-          my_logit = __ldg(a.logits + static_cast<size_t>(t) * a.E + sel_idx);
-          my_fast = true;
-        }
-      } else if (SIGMOID) {
-        sigmoid_token_fp64<VPL>(a, t, lane, wkeys);
-      } else {
-        softmax_token_full<VPL>(a, t, lane);
-      }
-    }
-    // weights of the tokens selected in fp32: lane = (token j, rank k);
-    // float-float unless a token of the warp has a selected logit outside its
-    // range (then fp64)
-    const int t = wid + (i0 + j_of_lane) * W;
-    const bool in_range = isfinite(my_logit) && (!SIGMOID || my_logit >= -700.0f);
-    const int base = (j_of_lane * a.K) & 31;
-    float wv;
-    if (a.scale_ff_ok && __all_sync(kFull, !my_fast || in_range)) {
-      wv = weight_ff<SIGMOID>(a, my_fast ? my_logit : 0.0f, base);
-    } else {
-      double val;
-      if (SIGMOID) {
-        val = rcp_weight(1.0 + exp_weight(-static_cast<double>(my_logit)));
-      } else {
-        const float top = __shfl_sync(kFull, my_logit, base);
-        val = exp_weight(static_cast<double>(my_logit) - static_cast<double>(top));
-      }
-      // the sum over the token's K lanes: a butterfly when K is a power of
-      // two (every lane then holds the same bits), else in k order
-      double den = 0.0;
-      if ((a.K & (a.K - 1)) == 0) {
-        den = val;
-        for (int off = 1; off < a.K; off <<= 1) den += __shfl_xor_sync(kFull, den, off);
-      } else {
-        for (int k = 0; k < a.K; ++k) den += __shfl_sync(kFull, val, (j_of_lane * a.K + k) & 31);
-      }
-      const double p = (SIGMOID && !a.renorm) ? val : val * rcp_weight(den);
-      wv = static_cast<float>(p * a.scale);
-    }
-    if (my_fast && j_of_lane < TB && t < a.T) {
-      a.idx[static_cast<size_t>(t) * a.K + k_of_lane] = my_idx;
-      a.w[static_cast<size_t>(t) * a.K + k_of_lane] = wv;
-    }
+    const int t0 = wid + i0 * W;
+    const int count = min(TB, (a.T - t0 + W - 1) / W);
+    warp_route_tokens<VPL, SIGMOID>(a, t0, W, count, lane, wkeys, list);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Eight threads per token, where E is 64, 128 or 256, K <= 8, the rows are
+// 16-byte aligned and, for group-limited sigmoid routing, a group is one,
+// two, four or eight threads' experts: thread p of a token's team holds
+// experts [p E/8, (p + 1) E/8) in registers, keeps its own sorted list of
+// candidate words, and the team merges the lists in three butterfly rounds,
+// so a token takes a few hundred instructions instead of the warp path's
+// K + 1 warp-wide selection rounds.  Four tokens per warp.
+//
+// Each candidate is one 32-bit word, q << 8 | (255 - e), with q a 23-bit
+// quantisation of its key that never ranks a smaller key above a larger one:
+// the larger word has the larger q, or the same q and the lower expert, and
+// no two words are equal.  A list is the 8 largest words, sorted, plus the
+// largest word below them: a thread sorts its words 8 at a time (Batcher's
+// odd-even merge network) and folds each sorted 8 into its list, and the team
+// folds its threads' lists together, by a bitonic step: the larger of L[i]
+// and B[7 - i] for each i is the top 8 as a bitonic sequence, which three
+// half-cleaner stages sort, and the largest of the smaller ones (and of the
+// two lists' ninth words) is the ninth.  Where the listed q strictly decrease, every
+// listed key is strictly above the next and above every unlisted key, so
+// the first K are the K largest keys, in order, and no two are equal.
+//   softmax: the key is the logit and q its position in a window of width 32
+//     around the largest of the row's first 8 logits, in steps of 2^-18;
+//     logits outside the window clamp to its ends.
+//   sigmoid: the key is the fp32 sigmoid + bias (within DELTA of the fp64
+//     key), q its position in [min bias, 1 + max bias], rounded, in steps of
+//     1/qs, so a key lies within half a step of its q.  Two listed keys whose
+//     q differ by more than 1 + 2 DELTA qs are more than 2 DELTA apart, and
+//     so are the K-th and any unlisted key when the K-th and (K+1)-th differ
+//     that much; then the fp64 keys rank the same.  Group scores (the sum of
+//     a group's top GK fp32 keys) are ranked exactly, ties to the lower
+//     group, and the TG kept groups must be more than 2 DG above the next, as
+//     in the warp path; only the kept groups' threads list their experts.
+// A token that fails a test, has a non-finite logit or bias, or a selected
+// sigmoid logit below -700, is routed again by its warp on the
+// warp-per-token path above.  The weights are weight_ff's, lane p of the team
+// holding rank p.
+
+constexpr int kTeam = 8;       // threads per token
+constexpr int kTeamWarps = 4;  // warps per block
+
+// a >= b afterwards
+__device__ __forceinline__ void cmp_desc(uint32_t& a, uint32_t& b) {
+  const uint32_t hi = max(a, b);
+  b = min(a, b);
+  a = hi;
+}
+
+// Batcher's odd-even merge sort of 8 words, descending (19 comparators).
+__device__ __forceinline__ void sort8_desc(uint32_t (&v)[8]) {
+  cmp_desc(v[0], v[1]); cmp_desc(v[2], v[3]); cmp_desc(v[4], v[5]); cmp_desc(v[6], v[7]);
+  cmp_desc(v[0], v[2]); cmp_desc(v[1], v[3]); cmp_desc(v[4], v[6]); cmp_desc(v[5], v[7]);
+  cmp_desc(v[1], v[2]); cmp_desc(v[5], v[6]);
+  cmp_desc(v[0], v[4]); cmp_desc(v[1], v[5]); cmp_desc(v[2], v[6]); cmp_desc(v[3], v[7]);
+  cmp_desc(v[2], v[4]); cmp_desc(v[3], v[5]);
+  cmp_desc(v[1], v[2]); cmp_desc(v[3], v[4]); cmp_desc(v[5], v[6]);
+}
+
+// (L, l9) becomes the 8 largest words of both lists, sorted, and the ninth.
+__device__ __forceinline__ void merge8(uint32_t (&L)[8], uint32_t& l9, const uint32_t (&B)[8],
+                                       uint32_t b9) {
+  uint32_t d = max(l9, b9);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t x = L[i], y = B[7 - i];
+    L[i] = max(x, y);
+    d = max(d, min(x, y));
+  }
+  l9 = d;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) cmp_desc(L[i], L[i + 4]);
+  cmp_desc(L[0], L[2]); cmp_desc(L[1], L[3]); cmp_desc(L[4], L[6]); cmp_desc(L[5], L[7]);
+  cmp_desc(L[0], L[1]); cmp_desc(L[2], L[3]); cmp_desc(L[4], L[5]); cmp_desc(L[6], L[7]);
+}
+
+// Folds 8 words (unsorted) into the list (L, l9); `first`: the list is empty.
+__device__ __forceinline__ void fold8(uint32_t (&L)[8], uint32_t& l9, uint32_t (&w)[8], bool first) {
+  sort8_desc(w);
+  if (first) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) L[i] = w[i];
+    l9 = 0u;
+  } else {
+    merge8(L, l9, w, 0u);
+  }
+}
+
+// The word of expert e whose scaled key is v = key * qs + qo: an fp32 in
+// [2^23, 2^24) is 2^23 plus an integer, which is its mantissa field; v is
+// clamped to that range (as bit patterns, which order like the values, with
+// negative ones below) and the mantissa shifted up by 8 bits.
+__device__ __forceinline__ uint32_t pack_word(float v, int e) {
+  const int bits = min(max(__float_as_int(v), 0x4B000000), 0x4B7FFFFF);
+  return static_cast<uint32_t>(bits) * 256u + static_cast<uint32_t>(255 - e);
+}
+
+__device__ __forceinline__ int word_expert(uint32_t w) { return 255 - static_cast<int>(w & 255u); }
+
+template <int EP, bool SIGMOID>
+__global__ void __launch_bounds__(kTeamWarps * 32) route_team_kernel(RouteArgs a) {
+  extern __shared__ double route_smem[];  // the fallback's fp64 keys: E per warp (sigmoid)
+  __shared__ int2 cand_lists[kTeamWarps][32];
+  __shared__ __align__(16) float bias_s[256];
+  __shared__ float brange[2][kTeamWarps];
+  __shared__ int bias_bad;
+  constexpr int VPL = EP / 4;  // the warp path's experts per lane for this E
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int p = lane & (kTeam - 1), base = lane & ~(kTeam - 1);
+  double* wkeys = route_smem + warp * a.E;
+  int2* list = cand_lists[warp];
+
+  // sigmoid: the bias (shared), and the scaling of keys to words from its range
+  float qs = 0.0f, qo = 0.0f;
+  bool bias_ok = true;
+  if (SIGMOID) {
+    if (threadIdx.x == 0) bias_bad = 0;
+    __syncthreads();
+    float bmin = INFINITY, bmax = -INFINITY;
+    for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+      const float b = a.bias ? __ldg(a.bias + e) : 0.0f;
+      bias_s[e] = b;
+      if (!isfinite(b)) bias_bad = 1;
+      bmin = fminf(bmin, b);
+      bmax = fmaxf(bmax, b);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      bmin = fminf(bmin, __shfl_xor_sync(kFull, bmin, off));
+      bmax = fmaxf(bmax, __shfl_xor_sync(kFull, bmax, off));
+    }
+    if (lane == 0) {
+      brange[0][warp] = bmin;
+      brange[1][warp] = bmax;
+    }
+    __syncthreads();
+    bmin = brange[0][0];
+    bmax = brange[1][0];
+    for (int w = 1; w < kTeamWarps; ++w) {
+      bmin = fminf(bmin, brange[0][w]);
+      bmax = fmaxf(bmax, brange[1][w]);
+    }
+    bias_ok = bias_bad == 0;
+    qs = 0x1p23f / __fsub_rn(__fadd_rn(1.0f, bmax), bmin);
+    qo = __fmaf_rn(-bmin, qs, 0x1p23f);
+  }
+  const int gsz = a.E / a.G;
+  const int m = SIGMOID && a.G > 1 ? gsz / EP : 1;  // threads per group
+  const int n_elig = SIGMOID && a.G > 1 ? a.TG * gsz : a.E;
+  const int n_list = a.K < n_elig ? a.K + 1 : a.K;
+
+  const int stride = gridDim.x * kTeamWarps * (32 / kTeam);
+  for (int t0 = (blockIdx.x * kTeamWarps + warp) * (32 / kTeam); t0 < a.T; t0 += stride) {
+    const int t = t0 + lane / kTeam;
+    const bool active = t < a.T;
+    const float* row = a.logits + static_cast<size_t>(active ? t : t0) * a.E;
+    float kx[EP];
+#pragma unroll
+    for (int c = 0; c < EP; c += 4) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(row + p * EP + c));
+      kx[c] = f.x;
+      kx[c + 1] = f.y;
+      kx[c + 2] = f.z;
+      kx[c + 3] = f.w;
+    }
+    float fin = 0.0f;  // NaN once a logit of the token is not finite
+#pragma unroll
+    for (int c = 0; c < EP; ++c) fin = __fmaf_rn(kx[c], 0.0f, fin);
+    uint32_t L[8], l9;
+    bool ok = active && bias_ok;
+    float gap = 0.0f;  // q difference a listed pair must exceed (sigmoid)
+    if (!SIGMOID) {
+      float m0 = kx[0];
+#pragma unroll
+      for (int c = 1; c < 8; ++c) m0 = fmaxf(m0, kx[c]);
+      m0 = __shfl_sync(kFull, m0, base);
+      const float so = __fmaf_rn(-__fsub_rn(m0, 16.0f), 0x1p18f, 0x1p23f);
+#pragma unroll
+      for (int b = 0; b < EP; b += 8) {
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = pack_word(__fmaf_rn(kx[b + j], 0x1p18f, so), p * EP + b + j);
+        fold8(L, l9, w, b == 0);
+      }
+    } else {
+      float maxabs = 0.0f, t0v = -INFINITY, t1v = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < EP; c += 4) {
+        const float4 b = *reinterpret_cast<const float4*>(bias_s + p * EP + c);
+        kx[c] = sigmoid_key(kx[c], b.x);
+        kx[c + 1] = sigmoid_key(kx[c + 1], b.y);
+        kx[c + 2] = sigmoid_key(kx[c + 2], b.z);
+        kx[c + 3] = sigmoid_key(kx[c + 3], b.w);
+      }
+#pragma unroll
+      for (int c = 0; c < EP; ++c) {
+        maxabs = fmaxf(maxabs, fabsf(kx[c]));
+        const float n0 = fmaxf(t0v, kx[c]);
+        t1v = fmaxf(t1v, fminf(t0v, kx[c]));
+        t0v = n0;
+      }
+#pragma unroll
+      for (int off = 1; off < kTeam; off <<= 1)
+        maxabs = fmaxf(maxabs, __shfl_xor_sync(kFull, maxabs, off));
+      const float delta = kDeltaAbs + kDeltaRel * maxabs;
+      ok = ok && delta < 1e-3f;  // huge or non-finite keys fail here
+      gap = __fmaf_rn(2.0f * delta, qs, 1.0f);
+      bool kept = true;
+      if (a.G > 1) {
+        // the group's top two over its m threads, then its score
+        group_top2_fp32(t0v, t1v, m);
+        const float gs = a.GK >= 2 ? __fadd_rn(__fadd_rn(0.0f, t0v), t1v) : t0v;
+        const int g = p / m;
+        int rank = 0;  // groups ranked before this one (score desc, group asc)
+        float gmax = 0.0f;
+        for (int j = 0; j < a.G; ++j) {
+          const float sj = __shfl_sync(kFull, gs, base + j * m);
+          gmax = fmaxf(gmax, fabsf(sj));
+          if (sj > gs || (sj == gs && j < g)) ++rank;
+        }
+        kept = rank < a.TG;
+        if (a.TG < a.G) {
+          // the lowest kept score must clear the highest dropped one
+          float last = kept ? gs : INFINITY, next = kept ? -INFINITY : gs;
+#pragma unroll
+          for (int off = 1; off < kTeam; off <<= 1) {
+            last = fminf(last, __shfl_xor_sync(kFull, last, off));
+            next = fmaxf(next, __shfl_xor_sync(kFull, next, off));
+          }
+          const float dg = a.GK * (delta + kDeltaRel * gmax);
+          ok = ok && last - next > 2.0f * dg;
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < EP; b += 8) {
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = pack_word(__fmaf_rn(kx[b + j], qs, qo), p * EP + b + j);
+        fold8(L, l9, w, b == 0);
+      }
+      if (!kept) {  // a dropped group's experts are not candidates
+#pragma unroll
+        for (int i = 0; i < 8; ++i) L[i] = 0u;
+        l9 = 0u;
+      }
+    }
+    // the team's lists merged: every thread of the team ends with the same list
+#pragma unroll
+    for (int off = 1; off < kTeam; off <<= 1) {
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) o[i] = __shfl_xor_sync(kFull, L[i], off);
+      merge8(L, l9, o, __shfl_xor_sync(kFull, l9, off));
+      fin = __fadd_rn(fin, __shfl_xor_sync(kFull, fin, off));
+    }
+    // the listed q strictly decrease, for sigmoid by more than the gap
+#pragma unroll
+    for (int i = 1; i <= 8; ++i) {
+      if (i >= n_list) break;
+      const uint32_t hi = L[i - 1], lo = i < 8 ? L[i] : l9;
+      const float d = static_cast<float>(static_cast<int>(hi >> 8) - static_cast<int>(lo >> 8));
+      if (SIGMOID ? !(d > gap) : !(d > 0.0f)) ok = false;
+    }
+    ok = ok && fin == 0.0f;
+    // rank p of the token: its expert, logit and weight
+    int my_e = 0;
+#pragma unroll
+    for (int i = 0; i < kTeam; ++i)
+      if (i == p) my_e = word_expert(L[i]);
+    const bool mine = p < a.K;
+    const float l = mine ? __ldg(row + my_e) : 0.0f;
+    if (SIGMOID && mine && !(l >= -700.0f)) ok = false;  // the fp64 path's range
+    // the verdict so far is the team's except for that range test: share it
+    ok = (__ballot_sync(kFull, !ok) & (0xffu << base)) == 0;
+    const float wv = weight_ff<SIGMOID>(a, ok ? l : 0.0f, base);
+    if (ok && mine) {
+      a.idx[static_cast<size_t>(t) * a.K + p] = my_e;
+      a.w[static_cast<size_t>(t) * a.K + p] = wv;
+    }
+    // the tokens that failed a test, one at a time by the whole warp
+    for (uint32_t fb = __ballot_sync(kFull, active && !ok && p == 0); fb; fb &= fb - 1)
+      warp_route_tokens<VPL, SIGMOID>(a, t0 + (__ffs(fb) - 1) / kTeam, 0, 1, lane, wkeys, list);
+  }
+}
+
+// Whether the eight-threads-per-token kernel applies (else the warp kernel).
+bool team_path(const RouteArgs& a, bool sigmoid) {
+  if ((a.E != 64 && a.E != 128 && a.E != 256) || a.K > kTeam || !a.vec4 || !a.scale_ff_ok) return false;
+  if (!sigmoid) return a.renorm != 0;
+  if (a.G == 1) return true;
+  const int ep = a.E / kTeam, gsz = a.E / a.G;
+  const int m = gsz / ep;
+  return a.GK <= 2 && gsz % ep == 0 && (m & (m - 1)) == 0;
+}
+
+template <int EP, bool SIGMOID>
+void launch_team(const RouteArgs& a, int num_sms, cudaStream_t s) {
+  auto k = route_team_kernel<EP, SIGMOID>;
+  const size_t smem = SIGMOID ? static_cast<size_t>(kTeamWarps) * a.E * sizeof(double) : 0;
+  const int per_block = kTeamWarps * (32 / kTeam);
+  const long long blocks_needed = (static_cast<long long>(a.T) + per_block - 1) / per_block;
+  long long grid = static_cast<long long>(resident_blocks(reinterpret_cast<const void*>(k),
+                                                          kTeamWarps * 32, smem)) * num_sms;
+  if (blocks_needed < grid) grid = blocks_needed;
+  k<<<static_cast<int>(grid < 1 ? 1 : grid), kTeamWarps * 32, smem, s>>>(a);
 }
 
 // One wave of resident blocks (or fewer if there are fewer tokens): a second,
@@ -1016,6 +1341,14 @@ cudaError_t launch_route_topk(const moe_handle* h, const float* logits, const fl
     a.fast = a.G == 1 || (gsz % vpl == 0 && L >= 1 && (L & (L - 1)) == 0 && a.GK <= 2);
   } else {
     a.fast = a.renorm;  // without renormalisation the weights need all E exponentials
+  }
+  if (team_path(a, sigmoid)) {
+    switch (a.E) {
+      case 64: sigmoid ? launch_team<8, true>(a, h->num_sms, s) : launch_team<8, false>(a, h->num_sms, s); break;
+      case 128: sigmoid ? launch_team<16, true>(a, h->num_sms, s) : launch_team<16, false>(a, h->num_sms, s); break;
+      default: sigmoid ? launch_team<32, true>(a, h->num_sms, s) : launch_team<32, false>(a, h->num_sms, s); break;
+    }
+    return cudaGetLastError();
   }
   const size_t smem = sigmoid && a.G > 1 ? static_cast<size_t>(kRouteWarps) * a.E * sizeof(double) : 0;
   switch (vpl) {
