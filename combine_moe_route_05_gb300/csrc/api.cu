@@ -59,7 +59,7 @@ Plan plan(const moe_config* c) {
     return at;
   };
   p.flags = take(i4);
-  p.ticket = take(i4);
+  p.ticket = take(sizeof(uint64_t));
   p.cnt_e = take(E * i4);
   p.off_e = take((E + 1) * i4);
   p.cnt_send_r = take(R * i4);

@@ -16,7 +16,7 @@ struct moe_handle {
   int pad;  // receive segments rounded up to a multiple of pad rows (>= 1)
   unsigned long long wait_ns;  // limit of the kernels' bounded waits
   uint32_t* flags;   // device status word (MOE_DEVERR_* bits)
-  uint32_t* ticket;  // [0] arrival counter of the layout's tile hand-over, [1] its epoch
+  uint32_t* ticket;  // the layout's tile hand-over: [0] arrivals, [1] epoch (one 64-bit word)
   int32_t* cnt_e;
   int32_t* off_e;
   int32_t* cnt_send_r;

@@ -51,7 +51,8 @@ struct LayoutArgs {
   int pad;       // receive segments rounded up to a multiple of pad rows
   int recv_cap;  // receive rows: T*K + E*(pad-1)
   uint32_t* flags;
-  uint32_t* ticket;  // [0] arrival counter, [1] epoch of the single-pass kernel
+  // arrivals of the tile hand-over (low 32 bits) and its epoch (high 32 bits)
+  unsigned long long* ticket;
   unsigned long long wait_ns;  // limit of the single-pass kernel's wait for the epoch
   int32_t* cnt_e;
   int32_t* off_e;
@@ -124,67 +125,108 @@ __device__ __forceinline__ uint32_t mark_token(const LayoutArgs& a, int t, uint3
   return valid;
 }
 
-// Exclusive scans of the column totals, tot[0, E) (expert segments rounded up
-// to the padding) and tot[E, E + R) (ranks), into off_e[0..E] and off_s[0..R]
-// (shared memory; warp 0 scans the experts, warp 1 the ranks).  With
-// `publish`, also writes the layout's count and offset arrays and S.  Ends
-// with a barrier.
-__device__ void scan_totals(const LayoutArgs& a, const int32_t* tot, int32_t* off_e, int32_t* off_s,
-                            bool publish) {
+// Exclusive scan, in place, of v[0, n) (n <= 4 * kThreads) by the whole
+// block: each thread a run of up to four entries, a warp scan of the runs'
+// sums, and a scan of the warps' totals.  `ws`: kThreads / 32 + 1 ints of
+// shared memory.  Ends with a barrier.
+__device__ void block_scan(int32_t* v, int n, int32_t* ws) {
+  constexpr int kWarps = kThreads / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < 2) {
-    const int n = warp == 0 ? a.E : a.R;
-    const int32_t* src = tot + (warp == 0 ? 0 : a.E);
-    int32_t* off = warp == 0 ? off_e : off_s;
-    int32_t* cnt_g = warp == 0 ? a.cnt_e : a.cnt_send_r;
-    int32_t* off_g = warp == 0 ? a.off_e : a.off_send_r;
-    // expert segments are rounded up to the padding; rank counts are not
-    const int pad = warp == 0 ? a.pad : 1;
-    const int per = (n + 31) / 32;
-    const int lo = lane * per, hi = min(n, lo + per);
-    int local = 0;
-    for (int i = lo; i < hi; ++i) local += (src[i] + pad - 1) / pad * pad;
-    int incl = local;
+  const int per = (n + kThreads - 1) / kThreads;  // 1 .. 4
+  const int i0 = per * threadIdx.x;
+  int x[4];
+  int s = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    x[j] = j < per && i0 + j < n ? v[i0 + j] : 0;
+    s += x[j];
+  }
+  int incl = s;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) ws[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < kWarps ? ws[lane] : 0;
+    int wi = w;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += o;
+      const int o = __shfl_up_sync(0xffffffffu, wi, d);
+      if (lane >= d) wi += o;
     }
-    int run = incl - local;
-    for (int i = lo; i < hi; ++i) {
-      off[i] = run;
-      if (publish) {
-        cnt_g[i] = src[i];
-        off_g[i] = run;
-      }
-      run += (src[i] + pad - 1) / pad * pad;
-    }
-    const int total = __shfl_sync(0xffffffffu, incl, 31);
-    if (lane == 0) {
-      off[n] = total;
-      if (publish) {
-        off_g[n] = total;
-        if (warp == 1) *a.S = total;
-      }
-    }
+    if (lane < kWarps) ws[lane] = wi - w;
   }
   __syncthreads();
+  int run = ws[warp] + incl - s;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (j < per && i0 + j < n) v[i0 + j] = run;
+    run += x[j];
+  }
+  __syncthreads();
+}
+
+// Column values c[0, E) and c[E, E + R) scanned into the split form
+// o[0..E] | o[E+1..E+R+1]: experts then ranks, each from zero, each with its
+// total at the end (o: E + R + 2 ints of shared memory, which may be c's own
+// split slots).  Expert values are rounded up to a multiple of `pad` first.
+// Ends with a barrier.
+__device__ void scan_split(const LayoutArgs& a, int32_t* o, int pad, int32_t* ws) {
+  const int cols = a.E + a.R;
+  if (pad > 1)
+    for (int e = threadIdx.x; e < a.E; e += kThreads) o[e] = (o[e] + pad - 1) / pad * pad;
+  if (threadIdx.x == 0) {
+    o[a.E] = 0;
+    o[cols + 1] = 0;
+  }
+  __syncthreads();
+  block_scan(o, cols + 2, ws);
+  // the rank entries continue the expert scan: restart them at zero
+  const int tot_e = o[a.E];
+  for (int j = a.E + 1 + threadIdx.x; j < cols + 2; j += kThreads) o[j] -= tot_e;
+  __syncthreads();
+}
+
+// Exclusive scans of the column totals, tot[0, E) (expert segments rounded up
+// to the padding) and tot[E, E + R) (ranks), into off[0..E] (off_e) and
+// off[E+1..E+R+1] (off_s), shared memory.  With `publish`, also writes the
+// layout's count and offset arrays and S.  Ends with a barrier.
+__device__ void scan_totals(const LayoutArgs& a, const int32_t* tot, int32_t* off, int32_t* ws,
+                            bool publish) {
+  const int cols = a.E + a.R;
+  for (int c = threadIdx.x; c < cols; c += kThreads) off[c + (c >= a.E ? 1 : 0)] = tot[c];
+  scan_split(a, off, a.pad, ws);
   if (publish) {
-    for (int r = threadIdx.x; r < a.R; r += blockDim.x) {
+    const int32_t* off_s = off + a.E + 1;
+    for (int e = threadIdx.x; e < a.E; e += kThreads) {
+      a.cnt_e[e] = tot[e];
+      a.off_e[e] = off[e];
+    }
+    for (int r = threadIdx.x; r < a.R; r += kThreads) {
+      a.cnt_send_r[r] = tot[a.E + r];
+      a.off_send_r[r] = off_s[r];
       // rows that arrive at rank r (pads excluded); its region starts at the
       // padded offset of its first expert
       int n = 0;
       for (int e = r * a.epr; e < (r + 1) * a.epr; ++e) n += tot[e];
-      a.off_recv_r[r] = off_e[r * a.epr];
+      a.off_recv_r[r] = off[r * a.epr];
       a.cnt_recv_r[r] = n;
     }
-    if (threadIdx.x == 0) a.off_recv_r[a.R] = off_e[a.E];
+    if (threadIdx.x == 0) {
+      a.off_e[a.E] = off[a.E];
+      a.off_send_r[a.R] = off_s[a.R];
+      *a.S = off_s[a.R];
+      a.off_recv_r[a.R] = off[a.E];
+    }
   }
 }
 
 // The last block of the two-launch path: exclusive scan of each column over
 // the tiles (in place in tile_hist), then the scans of the column totals.
-// `scratch`: 2 (E + R) + 2 ints of shared memory.
+// `scratch`: 2 (E + R) + 2 + kThreads / 32 + 1 ints of shared memory.
 __device__ void scan_tiles(const LayoutArgs& a, int32_t* scratch) {
   const int cols = a.E + a.R;
   int32_t* tot = scratch;
@@ -204,7 +246,7 @@ __device__ void scan_tiles(const LayoutArgs& a, int32_t* scratch) {
     tot[col] = run;
   }
   __syncthreads();
-  scan_totals(a, tot, scratch + cols, scratch + cols + a.E + 1, true);
+  scan_totals(a, tot, scratch + cols, scratch + 2 * cols + 2, true);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a) {
@@ -227,16 +269,19 @@ __global__ void __launch_bounds__(kThreads, 1) layout_count_kernel(LayoutArgs a)
     for (int w = 0; w < kWords; ++w) c += __popc(masks[w * cp + col]);
     a.tile_hist[static_cast<size_t>(tile) * cols + col] = c;
   }
-  __threadfence();
   __syncthreads();
   __shared__ int is_last;
-  if (threadIdx.x == 0) is_last = atomicAdd(a.ticket, 1u) == static_cast<uint32_t>(a.ntiles - 1);
+  if (threadIdx.x == 0) {
+    __threadfence();  // the tile's counts before its arrival
+    is_last = static_cast<uint32_t>(atomicAdd(a.ticket, 1ull)) == static_cast<uint32_t>(a.ntiles - 1);
+  }
   __syncthreads();
   if (!is_last) return;
   __threadfence();
 
   scan_tiles(a, reinterpret_cast<int32_t*>(masks));  // masks are dead now (16 (E + R + 1) ints)
-  if (threadIdx.x == 0) *a.ticket = 0;  // ready for the next layout
+  // ready for the next layout: arrivals back to zero, the epoch advanced
+  if (threadIdx.x == 0) atomicAdd(a.ticket, (1ull << 32) - static_cast<unsigned long long>(a.ntiles));
 }
 
 // shared memory of the scatter kernel, in order
@@ -257,10 +302,9 @@ struct ScatterSmem {
   __host__ __device__ size_t off() const { return base() + sizeof(int32_t) * cols; }
   __host__ __device__ size_t rank_of() const { return off() + sizeof(int32_t) * (cols + 2); }
   __host__ __device__ size_t tot() const { return rank_of() + sizeof(int32_t) * E; }
-  // the single-pass kernel also needs the column totals of its scan
-  __host__ __device__ size_t bytes(bool with_tot = false) const {
-    return tot() + (with_tot ? sizeof(int32_t) * cols : 0);
-  }
+  __host__ __device__ size_t ws() const { return tot() + sizeof(int32_t) * cols; }
+  // the column totals (single pass) and the block scan's warp sums
+  __host__ __device__ size_t bytes() const { return ws() + sizeof(int32_t) * (kThreads / 32 + 1); }
   __host__ __device__ static size_t align(size_t x) { return (x + 15) & ~static_cast<size_t>(15); }
 };
 
@@ -272,9 +316,9 @@ __device__ __forceinline__ uint32_t pack_send(int r, int tl) {
   return static_cast<uint32_t>(r) | (static_cast<uint32_t>(tl) << 9);
 }
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
@@ -309,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   int32_t* off = reinterpret_cast<int32_t*>(ssm + L.off());        // off_e[E+1] | off_s[R+1]
   int32_t* rank_of = reinterpret_cast<int32_t*>(ssm + L.rank_of()); // [E] expert -> rank
   const int tile = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int tile_t0 = tile * kTile;
   const int tile_n = max(0, min(kTile, a.T - tile_t0));  // tokens in this tile
 
@@ -332,8 +376,34 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
   __syncthreads();
   const uint32_t valid = mark_token(a, t, masks, cp, rank_of, ek);
   __syncthreads();
-  // exclusive prefix of the popcounts over the words of each column; the
-  // column's count in this tile goes to seg (scanned below)
+  // the tile's column counts (the single pass publishes them at once)
+  for (int col = threadIdx.x; col < cols; col += kThreads) {
+    int run = 0;
+#pragma unroll 8
+    for (int w = 0; w < kWords; ++w) run += __popc(masks[w * cp + col]);
+    seg[col + (col >= a.E ? 1 : 0)] = run;
+    if (kSinglePass) a.tile_hist[static_cast<size_t>(tile) * cols + col] = run;
+  }
+  __syncthreads();
+  // grid-wide hand-over of the tile counts (single pass): one 64-bit word
+  // holds the arrivals and the epoch; the last block to arrive resets the
+  // arrivals and advances the epoch in one atomic, the others wait for the
+  // epoch below, after the work that does not need the other tiles
+  __shared__ uint32_t epoch0;
+  __shared__ int last, failed;
+  if (kSinglePass && threadIdx.x == 0) {
+    __threadfence();  // the tile's counts before its arrival
+    const unsigned long long old = atomicAdd(a.ticket, 1ull);
+    epoch0 = static_cast<uint32_t>(old >> 32);
+    last = static_cast<uint32_t>(old) == static_cast<uint32_t>(a.ntiles - 1);
+    failed = 0;
+    if (last) {
+      __threadfence();
+      atomicAdd(a.ticket, (1ull << 32) - static_cast<unsigned long long>(a.ntiles));
+    }
+  }
+  // exclusive prefix of the popcounts over the words of each column, and the
+  // tile's column offsets (experts, ranks)
   for (int col = threadIdx.x; col < cols; col += kThreads) {
     int run = 0;
 #pragma unroll 8
@@ -341,87 +411,63 @@ __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs 
       pre[w * cp + col] = static_cast<uint16_t>(run);
       run += __popc(masks[w * cp + col]);
     }
-    seg[col + (col >= a.E ? 1 : 0)] = run;
-    if (kSinglePass) a.tile_hist[static_cast<size_t>(tile) * cols + col] = run;
   }
-  __syncthreads();
-  if (warp < 2) {
-    // exclusive scan of the tile's column counts: warp 0 experts, warp 1 ranks
-    const int n = warp == 0 ? a.E : a.R;
-    int32_t* v = seg + (warp == 0 ? 0 : a.E + 1);
-    const int per = (n + 31) / 32;
-    const int lo = lane * per, hi = min(n, lo + per);
-    int local = 0;
-    for (int i = lo; i < hi; ++i) local += v[i];
-    int incl = local;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += o;
-    }
-    int run = incl - local;
-    for (int i = lo; i < hi; ++i) {
-      const int c = v[i];
-      v[i] = run;
-      run += c;
-    }
-    if (lane == 31) v[n] = incl;
-  }
-  __syncthreads();
+  int32_t* ws = reinterpret_cast<int32_t*>(ssm + L.ws());
+  scan_split(a, seg, 1, ws);
 
   if (kSinglePass) {
-    // grid-wide hand-over of the tile counts: the last block to arrive
-    // publishes a new epoch at once; then every block reads all the tiles'
-    // counts itself (its tile bases and the column totals), so no block waits
-    // on another's scan
-    __shared__ uint32_t epoch0;
-    __shared__ int last, failed;
-    __threadfence();  // this tile's counts are visible device-wide
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      epoch0 = ld_acquire(a.ticket + 1);  // read before arriving
-      last = atomicAdd(a.ticket, 1u) == static_cast<uint32_t>(a.ntiles - 1);
-      failed = 0;
-      if (last) {
-        *a.ticket = 0;  // ready for the next layout
-        __threadfence();
-        atomicAdd(a.ticket + 1, 1u);  // publish
-      } else {
-        const unsigned long long t0 = global_ns();
-        while (ld_acquire(a.ticket + 1) == epoch0) {
-          if (global_ns() - t0 > a.wait_ns) {
-            raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
-            failed = 1;
-            break;
-          }
+    if (threadIdx.x == 0 && !last) {
+      const unsigned long long t0 = global_ns();
+      while (static_cast<uint32_t>(ld_acquire_u64(a.ticket) >> 32) == epoch0) {
+        if (global_ns() - t0 > a.wait_ns) {
+          raise_flag(a.flags, MOE_DEVERR_TIMEOUT);
+          failed = 1;
+          break;
         }
       }
     }
     __syncthreads();
     if (failed) return;
     // per column: the counts of the tiles before this one (its base) and of
-    // all tiles (the column total), 16 loads in flight per thread
+    // all tiles (the column total), 16 loads in flight per thread; where a
+    // column has several threads (kThreads / cols of them), they take
+    // alternate tiles and add up in shared memory
     int32_t* tot = reinterpret_cast<int32_t*>(ssm + L.tot());
-    for (int col = threadIdx.x; col < cols; col += kThreads) {
-      int before = 0, all = 0;
-      for (int t0 = 0; t0 < a.ntiles; t0 += 16) {
-        int v[16];
+    const int per = cols <= kThreads ? kThreads / cols : 1;
+    for (int c = threadIdx.x; c < cols; c += kThreads) {
+      base[c] = 0;
+      tot[c] = 0;
+    }
+    __syncthreads();
+    if (threadIdx.x < per * cols || per == 1) {
+      const int part = per == 1 ? 0 : threadIdx.x / cols;
+      for (int col = per == 1 ? threadIdx.x : threadIdx.x % cols; col < cols; col += kThreads) {
+        int before = 0, all = 0;
+        for (int t0 = part; t0 < a.ntiles; t0 += 16 * per) {
+          int v[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          v[i] = t0 + i < a.ntiles ? __ldcg(a.tile_hist + static_cast<size_t>(t0 + i) * cols + col)
-                                   : 0;
+          for (int i = 0; i < 16; ++i) {
+            const int tt = t0 + i * per;
+            v[i] = tt < a.ntiles ? __ldcg(a.tile_hist + static_cast<size_t>(tt) * cols + col) : 0;
+          }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (t0 + i < tile) before += v[i];
-          all += v[i];
+          for (int i = 0; i < 16; ++i) {
+            if (t0 + i * per < tile) before += v[i];
+            all += v[i];
+          }
+        }
+        if (per == 1) {
+          base[col] = before;
+          tot[col] = all;
+        } else {
+          atomicAdd(&base[col], before);
+          atomicAdd(&tot[col], all);
         }
       }
-      base[col] = before;
-      tot[col] = all;
     }
     __syncthreads();
     // offsets in shared memory; block 0 also publishes the count arrays
-    scan_totals(a, tot, off, off + a.E + 1, tile == 0);
+    scan_totals(a, tot, off, ws, tile == 0);
   }
 
   // base[c] becomes the first global row of this tile's run of column c
@@ -555,14 +601,14 @@ size_t count_smem(int cols, int E) {
   return (static_cast<size_t>(kWords) * col_stride(cols) + E) * sizeof(uint32_t);
 }
 
-size_t scatter_smem(int cols, int K, int R, bool single_pass = false) {
-  return ScatterSmem{cols, col_stride(cols), K, K < R ? K : R, cols - R}.bytes(single_pass);
+size_t scatter_smem(int cols, int K, int R) {
+  return ScatterSmem{cols, col_stride(cols), K, K < R ? K : R, cols - R}.bytes();
 }
 
 }  // namespace
 
 size_t layout_smem_bytes(int E, int R) {
-  const size_t a = count_smem(E + R, E), b = scatter_smem(E + R, MOE_MAX_TOPK, R, true);
+  const size_t a = count_smem(E + R, E), b = scatter_smem(E + R, MOE_MAX_TOPK, R);
   return a > b ? a : b;
 }
 
@@ -628,7 +674,7 @@ cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T
   a.pad = c.pad_align > 1 ? c.pad_align : 1;
   a.recv_cap = T * a.K + a.E * (a.pad - 1);
   a.flags = flags;
-  a.ticket = ticket;
+  a.ticket = reinterpret_cast<unsigned long long*>(ticket);
   a.wait_ns = wait_ns;
   a.cnt_e = out.cnt_e;
   a.off_e = out.off_e;
@@ -647,7 +693,7 @@ cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T
   const int cols = a.E + a.R;
   // one cooperative launch when every tile's block can be resident at once
   // (the blocks wait for the last one's scan), else two launches
-  const size_t one_smem = scatter_smem(cols, a.K, a.R, true);
+  const size_t one_smem = scatter_smem(cols, a.K, a.R);
   if (a.ntiles <= resident_single_pass_blocks(one_smem)) {
     void* params[] = {&a};
     const cudaError_t e = cudaLaunchCooperativeKernel(
@@ -665,7 +711,7 @@ cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T
 
 int layout_launches(const moe_config& c, int T) {
   const int cols = c.num_experts + c.num_ranks;
-  const size_t one_smem = scatter_smem(cols, c.top_k, c.num_ranks, true);
+  const size_t one_smem = scatter_smem(cols, c.top_k, c.num_ranks);
   return layout_tiles(T) <= resident_single_pass_blocks(one_smem) ? 1 : 2;
 }
 
