@@ -125,6 +125,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: the routing, layout and dispatch kernels are
+// launched (by launch_chained) so that a kernel's blocks may be scheduled
+// while the previous grid drains, which hides most of the launch gap after
+// the short routing and layout kernels; each such kernel first lets its own
+// successor do the same, then waits until the previous grid has completed
+// and its memory is visible, before any global access.
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.launch_dependents;\n\tgriddepcontrol.wait;" ::: "memory");
+}
+
+// Launches `kernel` with programmatic stream serialization (and, with
+// `cooperative`, as a cooperative grid).  The kernel must begin with
+// grid_dependency_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t s, bool cooperative, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeCooperative;
+  at[1].val.cooperative = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = cooperative ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// ---------------------------------------------------------------------------
 // warp helpers
 
 __device__ __forceinline__ uint32_t lanemask_lt() {

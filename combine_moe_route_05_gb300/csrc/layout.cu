@@ -338,6 +338,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // memory.
 template <bool kSinglePass>
 __global__ void __launch_bounds__(kThreads, 1) layout_scatter_kernel(LayoutArgs a) {
+  if (kSinglePass) grid_dependency_wait();
   extern __shared__ __align__(16) uint8_t ssm[];
   const int cols = a.E + a.R;
   const int cp = col_stride(cols);
@@ -695,10 +696,8 @@ cudaError_t launch_layout_buffers(const moe_config& c, const int32_t* idx, int T
   // (the blocks wait for the last one's scan), else two launches
   const size_t one_smem = scatter_smem(cols, a.K, a.R);
   if (a.ntiles <= resident_single_pass_blocks(one_smem)) {
-    void* params[] = {&a};
-    const cudaError_t e = cudaLaunchCooperativeKernel(
-        reinterpret_cast<const void*>(layout_scatter_kernel<true>), dim3(a.ntiles), dim3(kThreads),
-        params, one_smem, s);
+    const cudaError_t e =
+        launch_chained(layout_scatter_kernel<true>, dim3(a.ntiles), dim3(kThreads), one_smem, s, true, a);
     if (e == cudaSuccess) return cudaSuccess;
     (void)cudaGetLastError();  // not launched: take the two-launch path
   }

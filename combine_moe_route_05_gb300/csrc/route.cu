@@ -864,6 +864,7 @@ __device__ __forceinline__ void warp_route_tokens(const RouteArgs& a, int t0, in
 
 template <int VPL, bool SIGMOID>
 __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
+  grid_dependency_wait();
   extern __shared__ double route_smem[];
   __shared__ int2 cand_lists[kRouteWarps][32];
   double* wkeys = route_smem + (threadIdx.x >> 5) * a.E;
@@ -982,6 +983,7 @@ __device__ __forceinline__ int word_expert(uint32_t w) { return 255 - static_cas
 
 template <int EP, bool SIGMOID>
 __global__ void __launch_bounds__(kTeamWarps * 32) route_team_kernel(RouteArgs a) {
+  grid_dependency_wait();
   extern __shared__ double route_smem[];  // the fallback's fp64 keys: E per warp (sigmoid)
   __shared__ int2 cand_lists[kTeamWarps][32];
   __shared__ __align__(16) float bias_s[256];
@@ -1185,7 +1187,7 @@ void launch_team(const RouteArgs& a, int num_sms, cudaStream_t s) {
   long long grid = static_cast<long long>(resident_blocks(reinterpret_cast<const void*>(k),
                                                           kTeamWarps * 32, smem)) * num_sms;
   if (blocks_needed < grid) grid = blocks_needed;
-  k<<<static_cast<int>(grid < 1 ? 1 : grid), kTeamWarps * 32, smem, s>>>(a);
+  (void)launch_chained(k, dim3(static_cast<int>(grid < 1 ? 1 : grid)), dim3(kTeamWarps * 32), smem, s, false, a);
 }
 
 // One wave of resident blocks (or fewer if there are fewer tokens): a second,
@@ -1199,7 +1201,7 @@ void launch_one(const RouteArgs& a, int num_sms, size_t smem, cudaStream_t s) {
   long long grid = static_cast<long long>(resident_blocks(reinterpret_cast<const void*>(k),
                                                           kRouteWarps * 32, smem)) * num_sms;
   if (blocks_needed < grid) grid = blocks_needed;
-  k<<<static_cast<int>(grid < 1 ? 1 : grid), kRouteWarps * 32, smem, s>>>(a);
+  (void)launch_chained(k, dim3(static_cast<int>(grid < 1 ? 1 : grid)), dim3(kRouteWarps * 32), smem, s, false, a);
 }
 
 // ---------------------------------------------------------------------------
