@@ -77,11 +77,11 @@ __global__ void __launch_bounds__(1024) dispatch_kernel(DispatchArgs a) {
     }
     const uint8_t* xrow = a.x + static_cast<int64_t>(t) * a.row_bytes;
     for (int v = threadIdx.x; v < a.nvec; v += blockDim.x) {
-      const Vec16 val = ld_stream(xrow + v * 16);
+      const Vec16 val = ld_vec(xrow + v * 16);
 #pragma unroll
       for (int k = 0; k < KMAX; ++k) {
-        if (p[k] >= 0) st_vec(a.recv + static_cast<int64_t>(p[k]) * a.row_bytes + v * 16, val);
-        if (srow[k] >= 0) st_vec(a.send + static_cast<int64_t>(srow[k]) * a.row_bytes + v * 16, val);
+        if (p[k] >= 0) st_vec_cs(a.recv + static_cast<int64_t>(p[k]) * a.row_bytes + v * 16, val);
+        if (srow[k] >= 0) st_vec_cs(a.send + static_cast<int64_t>(srow[k]) * a.row_bytes + v * 16, val);
       }
     }
   }
@@ -248,7 +248,7 @@ __device__ __forceinline__ void combine_bwd_token(const RowArgs<Elt>& a, int t, 
     if (DOT) {
 #pragma unroll
       for (int k = 0; k < KMAX; ++k)
-        if (p[k] >= 0) yv[k] = ld_stream(a.y + static_cast<int64_t>(p[k]) * a.row_bytes + v * 16);
+        if (p[k] >= 0) yv[k] = ld_vec(a.y + static_cast<int64_t>(p[k]) * a.row_bytes + v * 16);
     }
     float gf[N];
     VT::to_f32(gv, gf);
