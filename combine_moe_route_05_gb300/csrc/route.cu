@@ -897,13 +897,14 @@ __global__ void __launch_bounds__(kRouteWarps * 32) route_kernel(RouteArgs a) {
 // the larger word has the larger q, or the same q and the lower expert, and
 // no two words are equal.  A list is the 8 largest words, sorted, plus the
 // largest word below them: a thread sorts its words 8 at a time (Batcher's
-// odd-even merge network) and folds each sorted 8 into its list, and the team
-// folds its threads' lists together, by a bitonic step: the larger of L[i]
-// and B[7 - i] for each i is the top 8 as a bitonic sequence, which three
-// half-cleaner stages sort, and the largest of the smaller ones (and of the
-// two lists' ninth words) is the ninth.  Where the listed q strictly decrease, every
-// listed key is strictly above the next and above every unlisted key, so
-// the first K are the K largest keys, in order, and no two are equal.
+// odd-even merge network) and folds each sorted 8 into its list, and the
+// team folds its threads' lists together, by a bitonic step: the larger of
+// L[i] and B[7 - i] for each i is the top 8 as a bitonic sequence, which
+// three half-cleaner stages sort, and the largest of the smaller ones (and
+// of the two lists' ninth words) is the ninth.  Where the listed q strictly
+// decrease, every listed key is strictly above the next and above every
+// unlisted key, so the first K are the K largest keys, in order, and no two
+// are equal.
 //   softmax: the key is the logit and q its position in a window of width 32
 //     around the largest of the row's first 8 logits, in steps of 2^-18;
 //     logits outside the window clamp to its ends.
