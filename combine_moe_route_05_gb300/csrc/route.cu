@@ -1156,7 +1156,7 @@ __global__ void __launch_bounds__(kTeamWarps * 32) route_team_kernel(RouteArgs a
     const bool mine = p < a.K;
     const float l = mine ? __ldg(row + my_e) : 0.0f;
     if (SIGMOID && mine && !(l >= -700.0f)) ok = false;  // the fp64 path's range
-    // the verdict so far is the team's except for that range test: share it
+    // every test so far gave the whole team one answer, except that range test: share it
     ok = (__ballot_sync(kFull, !ok) & (0xffu << base)) == 0;
     const float wv = weight_ff<SIGMOID>(a, ok ? l : 0.0f, base);
     if (ok && mine) {
