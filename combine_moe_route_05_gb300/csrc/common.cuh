@@ -44,9 +44,11 @@ __device__ __forceinline__ Vec16 ld_stream(const void* p) {
 }
 
 // 16-byte load through L1 (coherent path, default caching).  The combine
-// backward's gathered expert-output rows and the dispatch's token rows load
-// faster this way than by the non-coherent path without L1 allocation
-// (DeepSeek-V3 shape: combine backward 616.6 against 630.1 us a launch).
+// backward's gathered expert-output rows, the dispatch's token rows and the
+// absorption backward's gathered rows load faster this way than by the
+// non-coherent path without L1 allocation (DeepSeek-V3 shape: combine
+// backward 616.6 against 630.1 us a launch; Qwen3-235B shape: the step 2140
+// against 2149 us).
 __device__ __forceinline__ Vec16 ld_vec(const void* p) {
   Vec16 v;
   asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -529,8 +529,8 @@ __global__ void __launch_bounds__(kRowThreads) scale_rows_bwd_kernel(
       uint8_t* orow = gh + static_cast<int64_t>(p) * row_bytes;
       for (int v = lane; v < nvec; v += 32) {
         float gf[N], hf[N], o[N];
-        VT::to_f32(ld_stream(grow + v * 16), gf);
-        VT::to_f32(ld_stream(hrow + v * 16), hf);
+        VT::to_f32(ld_vec(grow + v * 16), gf);
+        VT::to_f32(ld_vec(hrow + v * 16), hf);
 #pragma unroll
         for (int j = 0; j < N; ++j) {
           o[j] = __fmul_rn(s, gf[j]);
