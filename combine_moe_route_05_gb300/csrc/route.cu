@@ -1,4 +1,5 @@
-// Top-K routing, one warp per token (sm_103a).
+// Top-K routing (sm_103a): eight threads per token where E is 64, 128 or 256
+// and K <= 8 (route_team_kernel), else one warp per token (route_kernel).
 //
 // Softmax routing selects the K largest logits (softmax is strictly
 // increasing, so the set and order equal those of the probabilities) and
@@ -6,8 +7,8 @@
 // key = sigmoid(logit) + score-correction bias and weights by the unbiased
 // sigmoid (DeepSpeed "Avoid collective token preparation for AutoEP DeepEP",
 // "Testing Done": exact routes, score-correction bias).  Selection order is
-// descending key, equal keys to the lower expert index.  Weights are computed
-// in fp64 and rounded once to fp32.
+// descending key, equal keys to the lower expert index.  Weights follow the
+// fp64 definition (float-float arithmetic below, rounded once to fp32).
 //
 // The sigmoid selection is defined on fp64 keys, but fp64 arithmetic is slow
 // on this GPU, so the kernel first selects on fp32 keys and keeps that result
@@ -25,12 +26,13 @@
 // its inputs.  If the fp32 gap between the last kept and the first dropped
 // group exceeds twice that bound, and the gap between each of the K + 1 best
 // eligible experts and the next exceeds 2 * DELTA, the fp64 selection is the
-// same set in the same order; otherwise the token is recomputed in fp64.
+// same set in the same order; otherwise the warp path gives fp64 keys to the
+// candidates that can cross the decision (and the team kernel hands the
+// token to the warp path).
 //
-// Each lane holds VPL consecutive experts (e = lane*VPL + j).  The fp64
-// weights of the K selected experts of TB = 32 / K tokens are computed
-// together, one (token, k) per lane, so each fp64 instruction serves TB
-// tokens.
+// Warp path: each lane holds VPL consecutive experts (e = lane*VPL + j), and
+// the weights of the K selected experts of TB = 32 / K tokens are computed
+// together, one (token, k) per lane.
 #include <cfloat>
 #include <cmath>
 #include <climits>

@@ -188,7 +188,10 @@ moe_status moe_handle_destroy(moe_handle* h);
  *   d_logits [T,E] fp32 router logits; d_bias [E] fp32 score-correction bias
  *   (sigmoid only; NULL = none).  Outputs d_idx [T,K] int32 in descending key
  *   order, equal keys to the lower expert index; d_w [T,K] fp32.
- *   Weights are computed in fp64 and rounded once to fp32.
+ *   The selection is that of fp64 keys exactly.  Weights follow the fp64
+ *   definition: computed in float-float arithmetic (about 2^-44 relative;
+ *   fp64 for out-of-range logits) and rounded once to fp32, so each is the
+ *   fp64 weight's rounding or one ulp from it.
  */
 moe_status moe_route_topk(moe_handle* h, const float* d_logits, const float* d_bias, int32_t T,
                           int32_t* d_idx, float* d_w, void* stream);
