@@ -121,9 +121,25 @@ def _ptr(t):
     return None if t is None else t.data_ptr()
 
 
-def _stream(stream):
-    s = torch.cuda.current_stream() if stream is None else stream
-    return s.cuda_stream
+def _stream(stream, device=None):
+    """The raw handle of `stream`, else of the current stream of `device` (the
+    handle's device; the current device when None)."""
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if device is not None and stream.device != device:
+        raise ValueError("stream is on %s, the handle on %s" % (stream.device, device))
+    return stream.cuda_stream
+
+
+def _call(h, fn, *args):
+    """Library function `fn` called with the handle's device current (the
+    library refuses a call made while another device is current)."""
+    f = getattr(lib(), fn)
+    if torch.cuda.current_device() != h.device.index:
+        with torch.cuda.device(h.device):
+            _check(fn, f(*args))
+    else:
+        _check(fn, f(*args))
 
 
 def _row_dtype(t):
@@ -134,13 +150,15 @@ def _row_dtype(t):
     raise TypeError("row tensors must be bfloat16 or float32, got %s" % t.dtype)
 
 
-def _req(t, dtype=None, shape=None, name="tensor"):
+def _req(t, dtype=None, shape=None, name="tensor", device=None):
     if t is None:
         return
     if shape is not None and any(d < 0 for d in shape):
         shape = None  # no layout yet: the library itself reports MOE_ERR_STATE
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, the handle on %s" % (name, t.device, device))
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
     if dtype is not None and t.dtype != dtype:
@@ -220,28 +238,30 @@ class Handle:
 
 def moe_route_topk(h, logits, bias, idx, w, stream=None):
     T = logits.shape[0]
-    _req(logits, torch.float32, (T, h.E), "logits")
-    _req(bias, torch.float32, (h.E,), "bias")
-    _req(idx, torch.int32, (T, h.K), "idx")
-    _req(w, torch.float32, (T, h.K), "w")
-    _check("moe_route_topk", lib().moe_route_topk(h.ptr, _ptr(logits), _ptr(bias), T, _ptr(idx),
-                                                  _ptr(w), _stream(stream)))
+    d = h.device
+    _req(logits, torch.float32, (T, h.E), "logits", d)
+    _req(bias, torch.float32, (h.E,), "bias", d)
+    _req(idx, torch.int32, (T, h.K), "idx", d)
+    _req(w, torch.float32, (T, h.K), "w", d)
+    _call(h, "moe_route_topk", h.ptr, _ptr(logits), _ptr(bias), T, _ptr(idx), _ptr(w),
+          _stream(stream, d))
 
 
 def moe_route_bwd(h, logits, idx, gw, glogits, stream=None):
     T = logits.shape[0]
-    _req(logits, torch.float32, (T, h.E), "logits")
-    _req(idx, torch.int32, (T, h.K), "idx")
-    _req(gw, torch.float32, (T, h.K), "gw")
-    _req(glogits, torch.float32, (T, h.E), "glogits")
-    _check("moe_route_bwd", lib().moe_route_bwd(h.ptr, _ptr(logits), _ptr(idx), _ptr(gw), T,
-                                                _ptr(glogits), _stream(stream)))
+    d = h.device
+    _req(logits, torch.float32, (T, h.E), "logits", d)
+    _req(idx, torch.int32, (T, h.K), "idx", d)
+    _req(gw, torch.float32, (T, h.K), "gw", d)
+    _req(glogits, torch.float32, (T, h.E), "glogits", d)
+    _call(h, "moe_route_bwd", h.ptr, _ptr(logits), _ptr(idx), _ptr(gw), T, _ptr(glogits),
+          _stream(stream, d))
 
 
 def moe_dispatch_layout(h, idx, stream=None):
     T = idx.shape[0]
-    _req(idx, torch.int32, (T, h.K), "idx")
-    _check("moe_dispatch_layout", lib().moe_dispatch_layout(h.ptr, _ptr(idx), T, _stream(stream)))
+    _req(idx, torch.int32, (T, h.K), "idx", h.device)
+    _call(h, "moe_dispatch_layout", h.ptr, _ptr(idx), T, _stream(stream, h.device))
     h.T = T
 
 
@@ -253,55 +273,58 @@ def moe_layout_view(h):
 
 def moe_dispatch(h, x, w, recv, recv_w, send=None, stream=None):
     T, H = x.shape
-    _req(x, None, (h.T, H), "x")
-    _req(recv, x.dtype, (h.recv_rows, H), "recv")
-    _req(w, torch.float32, (h.T, h.K), "w")
-    _req(recv_w, torch.float32, (h.recv_rows,), "recv_w")
-    _req(send, x.dtype, (h.T * min(h.K, h.R), H), "send")
-    _check("moe_dispatch", lib().moe_dispatch(h.ptr, _ptr(x), H, _row_dtype(x), _ptr(w), _ptr(recv),
-                                              _ptr(recv_w), _ptr(send), _stream(stream)))
+    d = h.device
+    _req(x, None, (h.T, H), "x", d)
+    _req(recv, x.dtype, (h.recv_rows, H), "recv", d)
+    _req(w, torch.float32, (h.T, h.K), "w", d)
+    _req(recv_w, torch.float32, (h.recv_rows,), "recv_w", d)
+    _req(send, x.dtype, (h.T * min(h.K, h.R), H), "send", d)
+    _call(h, "moe_dispatch", h.ptr, _ptr(x), H, _row_dtype(x), _ptr(w), _ptr(recv),
+          _ptr(recv_w), _ptr(send), _stream(stream, d))
 
 
 def moe_combine(h, y, w, out, stream=None):
     H = y.shape[1]
-    _req(y, None, (h.recv_rows, H), "y")
-    _req(w, torch.float32, (h.T, h.K), "w")
-    _req(out, y.dtype, (h.T, H), "out")
-    _check("moe_combine", lib().moe_combine(h.ptr, _ptr(y), H, _row_dtype(y), _ptr(w), _ptr(out),
-                                            _stream(stream)))
+    d = h.device
+    _req(y, None, (h.recv_rows, H), "y", d)
+    _req(w, torch.float32, (h.T, h.K), "w", d)
+    _req(out, y.dtype, (h.T, H), "out", d)
+    _call(h, "moe_combine", h.ptr, _ptr(y), H, _row_dtype(y), _ptr(w), _ptr(out),
+          _stream(stream, d))
 
 
 def moe_combine_bwd(h, g, y, w, gy, gw, stream=None):
     H = g.shape[1]
-    _req(g, None, (h.T, H), "g")
-    _req(y, g.dtype, (h.recv_rows, H), "y")
-    _req(w, torch.float32, (h.T, h.K), "w")
-    _req(gy, g.dtype, (h.recv_rows, H), "gy")
-    _req(gw, torch.float32, (h.T, h.K), "gw")
-    _check("moe_combine_bwd", lib().moe_combine_bwd(h.ptr, _ptr(g), _ptr(y), H, _row_dtype(g), _ptr(w),
-                                                    _ptr(gy), _ptr(gw), _stream(stream)))
+    d = h.device
+    _req(g, None, (h.T, H), "g", d)
+    _req(y, g.dtype, (h.recv_rows, H), "y", d)
+    _req(w, torch.float32, (h.T, h.K), "w", d)
+    _req(gy, g.dtype, (h.recv_rows, H), "gy", d)
+    _req(gw, torch.float32, (h.T, h.K), "gw", d)
+    _call(h, "moe_combine_bwd", h.ptr, _ptr(g), _ptr(y), H, _row_dtype(g), _ptr(w), _ptr(gy),
+          _ptr(gw), _stream(stream, d))
 
 
 def moe_dispatch_bwd(h, grecv, gx, stream=None):
     H = grecv.shape[1]
-    _req(grecv, None, (h.recv_rows, H), "grecv")
-    _req(gx, grecv.dtype, (h.T, H), "gx")
-    _check("moe_dispatch_bwd", lib().moe_dispatch_bwd(h.ptr, _ptr(grecv), H, _row_dtype(grecv),
-                                                      _ptr(gx), _stream(stream)))
+    d = h.device
+    _req(grecv, None, (h.recv_rows, H), "grecv", d)
+    _req(gx, grecv.dtype, (h.T, H), "gx", d)
+    _call(h, "moe_dispatch_bwd", h.ptr, _ptr(grecv), H, _row_dtype(grecv), _ptr(gx),
+          _stream(stream, d))
 
 
 def moe_dispatch_bwd_route(h, grecv, logits, idx, gw, gx, glogits, stream=None):
     H = grecv.shape[1]
-    _req(grecv, None, (h.recv_rows, H), "grecv")
-    _req(logits, torch.float32, (h.T, h.E), "logits")
-    _req(idx, torch.int32, (h.T, h.K), "idx")
-    _req(gw, torch.float32, (h.T, h.K), "gw")
-    _req(gx, grecv.dtype, (h.T, H), "gx")
-    _req(glogits, torch.float32, (h.T, h.E), "glogits")
-    _check("moe_dispatch_bwd_route",
-           lib().moe_dispatch_bwd_route(h.ptr, _ptr(grecv), H, _row_dtype(grecv), _ptr(logits),
-                                        _ptr(idx), _ptr(gw), _ptr(gx), _ptr(glogits),
-                                        _stream(stream)))
+    d = h.device
+    _req(grecv, None, (h.recv_rows, H), "grecv", d)
+    _req(logits, torch.float32, (h.T, h.E), "logits", d)
+    _req(idx, torch.int32, (h.T, h.K), "idx", d)
+    _req(gw, torch.float32, (h.T, h.K), "gw", d)
+    _req(gx, grecv.dtype, (h.T, H), "gx", d)
+    _req(glogits, torch.float32, (h.T, h.E), "glogits", d)
+    _call(h, "moe_dispatch_bwd_route", h.ptr, _ptr(grecv), H, _row_dtype(grecv), _ptr(logits),
+          _ptr(idx), _ptr(gw), _ptr(gx), _ptr(glogits), _stream(stream, d))
 
 
 def moe_dispatch_bwd_route_launches(h):
@@ -314,61 +337,64 @@ def moe_dispatch_bwd_route_launches(h):
 
 def moe_expand(h, send, recv, stream=None):
     H = send.shape[1]
-    _req(send, None, (h.T * min(h.K, h.R), H), "send")
-    _req(recv, send.dtype, (h.recv_rows, H), "recv")
-    _check("moe_expand", lib().moe_expand(h.ptr, _ptr(send), H, _row_dtype(send), _ptr(recv),
-                                          _stream(stream)))
+    d = h.device
+    _req(send, None, (h.T * min(h.K, h.R), H), "send", d)
+    _req(recv, send.dtype, (h.recv_rows, H), "recv", d)
+    _call(h, "moe_expand", h.ptr, _ptr(send), H, _row_dtype(send), _ptr(recv), _stream(stream, d))
 
 
 def moe_combine_partial(h, y, w, partial, stream=None):
     H = y.shape[1]
-    _req(y, None, (h.recv_rows, H), "y")
-    _req(w, torch.float32, (h.T, h.K), "w")
-    _req(partial, y.dtype, (h.T * min(h.K, h.R), H), "partial")
-    _check("moe_combine_partial", lib().moe_combine_partial(h.ptr, _ptr(y), H, _row_dtype(y),
-                                                            _ptr(w), _ptr(partial), _stream(stream)))
+    d = h.device
+    _req(y, None, (h.recv_rows, H), "y", d)
+    _req(w, torch.float32, (h.T, h.K), "w", d)
+    _req(partial, y.dtype, (h.T * min(h.K, h.R), H), "partial", d)
+    _call(h, "moe_combine_partial", h.ptr, _ptr(y), H, _row_dtype(y), _ptr(w), _ptr(partial),
+          _stream(stream, d))
 
 
 def moe_combine_reduce(h, partial, out, stream=None):
     H = partial.shape[1]
-    _req(partial, None, (h.T * min(h.K, h.R), H), "partial")
-    _req(out, partial.dtype, (h.T, H), "out")
-    _check("moe_combine_reduce", lib().moe_combine_reduce(h.ptr, _ptr(partial), H,
-                                                          _row_dtype(partial), _ptr(out),
-                                                          _stream(stream)))
+    d = h.device
+    _req(partial, None, (h.T * min(h.K, h.R), H), "partial", d)
+    _req(out, partial.dtype, (h.T, H), "out", d)
+    _call(h, "moe_combine_reduce", h.ptr, _ptr(partial), H, _row_dtype(partial), _ptr(out),
+          _stream(stream, d))
 
 
 def moe_scale_rows(h, hrows, recv_w, hs, stream=None):
     I = hrows.shape[1]
-    _req(hrows, None, (h.recv_rows, I), "h")
-    _req(recv_w, torch.float32, (h.recv_rows,), "recv_w")
-    _req(hs, hrows.dtype, (h.recv_rows, I), "hs")
-    _check("moe_scale_rows", lib().moe_scale_rows(h.ptr, _ptr(hrows), I, _row_dtype(hrows),
-                                                  _ptr(recv_w), _ptr(hs), _stream(stream)))
+    d = h.device
+    _req(hrows, None, (h.recv_rows, I), "h", d)
+    _req(recv_w, torch.float32, (h.recv_rows,), "recv_w", d)
+    _req(hs, hrows.dtype, (h.recv_rows, I), "hs", d)
+    _call(h, "moe_scale_rows", h.ptr, _ptr(hrows), I, _row_dtype(hrows), _ptr(recv_w), _ptr(hs),
+          _stream(stream, d))
 
 
 def moe_scale_rows_bwd(h, ghs, hrows, recv_w, gh, gw, stream=None):
     I = hrows.shape[1]
-    _req(ghs, None, (h.recv_rows, I), "ghs")
-    _req(hrows, ghs.dtype, (h.recv_rows, I), "h")
-    _req(recv_w, torch.float32, (h.recv_rows,), "recv_w")
-    _req(gh, ghs.dtype, (h.recv_rows, I), "gh")
-    _req(gw, torch.float32, (h.T, h.K), "gw")
-    _check("moe_scale_rows_bwd", lib().moe_scale_rows_bwd(h.ptr, _ptr(ghs), _ptr(hrows), I,
-                                                          _row_dtype(ghs), _ptr(recv_w), _ptr(gh),
-                                                          _ptr(gw), _stream(stream)))
+    d = h.device
+    _req(ghs, None, (h.recv_rows, I), "ghs", d)
+    _req(hrows, ghs.dtype, (h.recv_rows, I), "h", d)
+    _req(recv_w, torch.float32, (h.recv_rows,), "recv_w", d)
+    _req(gh, ghs.dtype, (h.recv_rows, I), "gh", d)
+    _req(gw, torch.float32, (h.T, h.K), "gw", d)
+    _call(h, "moe_scale_rows_bwd", h.ptr, _ptr(ghs), _ptr(hrows), I, _row_dtype(ghs),
+          _ptr(recv_w), _ptr(gh), _ptr(gw), _stream(stream, d))
 
 
 def moe_w2_absorbed(h, hrows, recv_w, w2, y, stream=None):
     """y = bf16(bf16(h * recv_w) @ W2[e].T) per expert segment (W2 [E, H, I])."""
     I = hrows.shape[1]
     H = w2.shape[1]
-    _req(hrows, torch.bfloat16, (h.recv_rows, I), "h")
-    _req(recv_w, torch.float32, (h.recv_rows,), "recv_w")
-    _req(w2, torch.bfloat16, (h.E, H, I), "w2")
-    _req(y, torch.bfloat16, (h.recv_rows, H), "y")
-    _check("moe_w2_absorbed", lib().moe_w2_absorbed(h.ptr, _ptr(hrows), I, _ptr(recv_w), _ptr(w2),
-                                                    H, _ptr(y), _stream(stream)))
+    d = h.device
+    _req(hrows, torch.bfloat16, (h.recv_rows, I), "h", d)
+    _req(recv_w, torch.float32, (h.recv_rows,), "recv_w", d)
+    _req(w2, torch.bfloat16, (h.E, H, I), "w2", d)
+    _req(y, torch.bfloat16, (h.recv_rows, H), "y", d)
+    _call(h, "moe_w2_absorbed", h.ptr, _ptr(hrows), I, _ptr(recv_w), _ptr(w2), H, _ptr(y),
+          _stream(stream, d))
 
 
 def moe_dispatch_layout_launches(h, T):
@@ -386,7 +412,7 @@ def moe_read_device_status(h):
 
 
 def moe_clear_device_status(h, stream=None):
-    _check("moe_clear_device_status", lib().moe_clear_device_status(h.ptr, _stream(stream)))
+    _call(h, "moe_clear_device_status", h.ptr, _stream(stream, h.device))
 
 
 def moe_set_wait_limit(h, limit_ns):
@@ -409,22 +435,25 @@ def layout_sizes(T, K, E, R, pad=1):
 def moe_dispatch_layout_static(cfg, idx, out, status=None, stream=None):
     """Allocation-free layout into caller-owned int32 tensors `out` (a dict
     keyed like LAYOUT_FIELDS, sized by layout_sizes); `status` an optional
-    one-element int32 CUDA tensor that collects MOE_DEVERR_* bits."""
+    one-element int32 CUDA tensor that collects MOE_DEVERR_* bits.  Every
+    tensor and the stream are on idx's device; the call runs there."""
     T = idx.shape[0]
     _req(idx, torch.int32, (T, cfg.top_k), "idx")
+    d = idx.device
     sizes = layout_sizes(T, cfg.top_k, cfg.num_experts, cfg.num_ranks, cfg.pad_align)
     v = MoeLayout()
     for name in LAYOUT_FIELDS:
         t = out[name]
-        _req(t, torch.int32, None, name)
+        _req(t, torch.int32, None, name, d)
         if t.numel() != sizes[name]:
             raise ValueError("%s must have %d elements, got %d" % (name, sizes[name], t.numel()))
         setattr(v, name, t.data_ptr() if t.numel() else None)
     v.num_tokens = T
-    _req(status, torch.int32, (1,), "status")
-    _check("moe_dispatch_layout_static",
-           lib().moe_dispatch_layout_static(ctypes.byref(cfg), _ptr(idx), T, ctypes.byref(v),
-                                            _ptr(status), _stream(stream)))
+    _req(status, torch.int32, (1,), "status", d)
+    with torch.cuda.device(d):
+        _check("moe_dispatch_layout_static",
+               lib().moe_dispatch_layout_static(ctypes.byref(cfg), _ptr(idx), T, ctypes.byref(v),
+                                                _ptr(status), _stream(stream, d)))
 
 
 def layout_tensors(h):

@@ -102,6 +102,14 @@ moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
+// Every launch goes to the current device, and every pointer a call gets must
+// live on the handle's device: a call made while another device is current
+// is refused before anything is launched.
+bool on_handle_device(const moe_handle* h) {
+  int dev = -1;
+  return cudaGetDevice(&dev) == cudaSuccess && dev == h->device;
+}
+
 }  // namespace
 
 namespace moe {
@@ -185,6 +193,7 @@ moe_status moe_handle_destroy(moe_handle* h) {
 moe_status moe_route_topk(moe_handle* h, const float* d_logits, const float* d_bias, int32_t T,
                           int32_t* d_idx, float* d_w, void* stream) {
   if (!h || T < 0) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (T > h->cfg.max_tokens) return MOE_ERR_CAPACITY;
   if (T > 0 && (!d_logits || !d_idx || !d_w)) return MOE_ERR_INVALID;
   if (!aligned(d_logits, 4) || !aligned(d_idx, 4) || !aligned(d_w, 4) || !aligned(d_bias, 4))
@@ -196,6 +205,7 @@ moe_status moe_route_topk(moe_handle* h, const float* d_logits, const float* d_b
 moe_status moe_route_bwd(const moe_handle* h, const float* d_logits, const int32_t* d_idx,
                          const float* d_gw, int32_t T, float* d_glogits, void* stream) {
   if (!h || T < 0) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (T > h->cfg.max_tokens) return MOE_ERR_CAPACITY;
   if (T > 0 && (!d_logits || !d_idx || !d_gw || !d_glogits)) return MOE_ERR_INVALID;
   if (!aligned(d_logits, 4) || !aligned(d_idx, 4) || !aligned(d_gw, 4) || !aligned(d_glogits, 4))
@@ -206,6 +216,7 @@ moe_status moe_route_bwd(const moe_handle* h, const float* d_logits, const int32
 
 moe_status moe_dispatch_layout(moe_handle* h, const int32_t* d_idx, int32_t T, void* stream) {
   if (!h || T < 0) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (T > h->cfg.max_tokens) return MOE_ERR_CAPACITY;
   if (T > 0 && (!d_idx || !aligned(d_idx, 4))) return MOE_ERR_INVALID;
   const moe_status st = from_cuda(moe::launch_layout(h, d_idx, T, as_stream(stream)));
@@ -237,6 +248,7 @@ moe_status moe_dispatch(const moe_handle* h, const void* d_x, int32_t H, int32_t
                         const float* d_w, void* d_recv, float* d_recv_w, void* d_send,
                         void* stream) {
   if (!h) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (h->T < 0) return MOE_ERR_STATE;
   if (h->T == 0) return empty_rows_ok(H, dtype) ? MOE_OK : MOE_ERR_INVALID;
   if (!row_ok(d_x, H, dtype) || !row_ok(d_recv, H, dtype)) return MOE_ERR_INVALID;
@@ -251,6 +263,7 @@ moe_status moe_dispatch(const moe_handle* h, const void* d_x, int32_t H, int32_t
 moe_status moe_combine(const moe_handle* h, const void* d_y, int32_t H, int32_t dtype,
                        const float* d_w, void* d_out, void* stream) {
   if (!h) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (h->T < 0) return MOE_ERR_STATE;
   if (h->T == 0) return empty_rows_ok(H, dtype) ? MOE_OK : MOE_ERR_INVALID;
   if (!row_ok(d_y, H, dtype) || !row_ok(d_out, H, dtype) || !aligned(d_w, 4))
@@ -262,6 +275,7 @@ moe_status moe_combine_bwd(const moe_handle* h, const void* d_g, const void* d_y
                            int32_t dtype, const float* d_w, void* d_gy, float* d_gw,
                            void* stream) {
   if (!h) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (h->T < 0) return MOE_ERR_STATE;
   if (h->T == 0) return empty_rows_ok(H, dtype) ? MOE_OK : MOE_ERR_INVALID;
   if (!row_ok(d_g, H, dtype) || !row_ok(d_gy, H, dtype)) return MOE_ERR_INVALID;
@@ -274,6 +288,7 @@ moe_status moe_combine_bwd(const moe_handle* h, const void* d_g, const void* d_y
 moe_status moe_dispatch_bwd(const moe_handle* h, const void* d_grecv, int32_t H, int32_t dtype,
                             void* d_gx, void* stream) {
   if (!h) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (h->T < 0) return MOE_ERR_STATE;
   if (h->T == 0) return empty_rows_ok(H, dtype) ? MOE_OK : MOE_ERR_INVALID;
   if (!row_ok(d_grecv, H, dtype) || !row_ok(d_gx, H, dtype)) return MOE_ERR_INVALID;
@@ -284,6 +299,7 @@ moe_status moe_dispatch_bwd_route(const moe_handle* h, const void* d_grecv, int3
                                   int32_t dtype, const float* d_logits, const int32_t* d_idx,
                                   const float* d_gw, void* d_gx, float* d_glogits, void* stream) {
   if (!h) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (h->T < 0) return MOE_ERR_STATE;
   if (h->T == 0) return empty_rows_ok(H, dtype) ? MOE_OK : MOE_ERR_INVALID;
   if (!row_ok(d_grecv, H, dtype) || !row_ok(d_gx, H, dtype)) return MOE_ERR_INVALID;
@@ -303,6 +319,7 @@ moe_status moe_dispatch_bwd_route_launches(const moe_handle* h, int32_t* n_launc
 moe_status moe_expand(const moe_handle* h, const void* d_send, int32_t H, int32_t dtype,
                       void* d_recv, void* stream) {
   if (!h) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (h->T < 0) return MOE_ERR_STATE;
   if (h->T == 0) return empty_rows_ok(H, dtype) ? MOE_OK : MOE_ERR_INVALID;
   if (!row_ok(d_send, H, dtype) || !row_ok(d_recv, H, dtype)) return MOE_ERR_INVALID;
@@ -312,6 +329,7 @@ moe_status moe_expand(const moe_handle* h, const void* d_send, int32_t H, int32_
 moe_status moe_combine_partial(const moe_handle* h, const void* d_y, int32_t H, int32_t dtype,
                                const float* d_w, void* d_partial, void* stream) {
   if (!h) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (h->T < 0) return MOE_ERR_STATE;
   if (h->T == 0) return empty_rows_ok(H, dtype) ? MOE_OK : MOE_ERR_INVALID;
   if (!row_ok(d_y, H, dtype) || !row_ok(d_partial, H, dtype) || !aligned(d_w, 4))
@@ -322,6 +340,7 @@ moe_status moe_combine_partial(const moe_handle* h, const void* d_y, int32_t H, 
 moe_status moe_combine_reduce(const moe_handle* h, const void* d_partial, int32_t H,
                               int32_t dtype, void* d_out, void* stream) {
   if (!h) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (h->T < 0) return MOE_ERR_STATE;
   if (h->T == 0) return empty_rows_ok(H, dtype) ? MOE_OK : MOE_ERR_INVALID;
   if (!row_ok(d_partial, H, dtype) || !row_ok(d_out, H, dtype)) return MOE_ERR_INVALID;
@@ -331,6 +350,7 @@ moe_status moe_combine_reduce(const moe_handle* h, const void* d_partial, int32_
 moe_status moe_scale_rows(const moe_handle* h, const void* d_h, int32_t I, int32_t dtype,
                           const float* d_recv_w, void* d_hs, void* stream) {
   if (!h) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (h->T < 0) return MOE_ERR_STATE;
   if (h->T == 0) return empty_rows_ok(I, dtype) ? MOE_OK : MOE_ERR_INVALID;
   if (!row_ok(d_h, I, dtype) || !row_ok(d_hs, I, dtype)) return MOE_ERR_INVALID;
@@ -342,6 +362,7 @@ moe_status moe_scale_rows_bwd(const moe_handle* h, const void* d_ghs, const void
                               int32_t dtype, const float* d_recv_w, void* d_gh, float* d_gw,
                               void* stream) {
   if (!h) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (h->T < 0) return MOE_ERR_STATE;
   if (h->T == 0) return empty_rows_ok(I, dtype) ? MOE_OK : MOE_ERR_INVALID;
   if (!row_ok(d_ghs, I, dtype) || !row_ok(d_h, I, dtype) || !row_ok(d_gh, I, dtype))
@@ -365,6 +386,7 @@ moe_status moe_dispatch_layout_launches(const moe_handle* h, int32_t T, int32_t*
 moe_status moe_w2_absorbed(const moe_handle* h, const void* d_h, int32_t I, const float* d_recv_w,
                            const void* d_w2, int32_t H, void* d_y, void* stream) {
   if (!h) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   if (!moe::w2_shape_ok(I, H)) return MOE_ERR_INVALID;
   if (static_cast<int64_t>(h->cfg.num_experts) * H > INT32_MAX) return MOE_ERR_INVALID;
   if (h->T < 0) return MOE_ERR_STATE;
@@ -389,6 +411,7 @@ moe_status moe_read_device_status(const moe_handle* h, uint32_t* host_flags) {
 
 moe_status moe_clear_device_status(moe_handle* h, void* stream) {
   if (!h) return MOE_ERR_INVALID;
+  if (!on_handle_device(h)) return MOE_ERR_INVALID;
   cudaError_t e = cudaMemsetAsync(h->flags, 0, sizeof(uint32_t), as_stream(stream));
   // a layout whose hand-over timed out left its arrival counter short of
   // zero-on-exit: re-arm it (the epoch word is only ever compared relatively)

@@ -27,6 +27,10 @@
  *     current when the handle was created; the caller owns all memory
  *     (tensors and workspace).  Row tensors must be 16-byte aligned and their
  *     row size (H or I times the element size) a multiple of 16 bytes.
+ *   - Calls that launch work or write device memory must be made while the
+ *     handle's device is current (and with a stream of that device): a call
+ *     made while another device is current returns MOE_ERR_INVALID and
+ *     launches nothing.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All
  *     compute calls are asynchronous on it: none synchronises the host,
  *     allocates memory or copies device -> host.

@@ -110,3 +110,30 @@ def test_host_validation_rejects_bad_arguments_without_a_gpu(lib):
     assert L.moe_dispatch_bwd(None, 0x1000, 8, 0, 0x1000, None) == lib.MOE_ERR_INVALID
     assert L.moe_read_device_status(None, None) == lib.MOE_ERR_INVALID
     assert L.moe_handle_destroy(None) == lib.MOE_ERR_INVALID
+
+
+class _FakeCudaTensor:
+    """Stands in for a CUDA tensor on a given device (no GPU needed)."""
+    is_cuda = True
+
+    def __init__(self, device, shape, dtype):
+        self.device, self.shape, self.dtype = device, shape, dtype
+
+    def is_contiguous(self):
+        return True
+
+
+class _FakeStream:
+    def __init__(self, device):
+        self.device, self.cuda_stream = device, 0
+
+
+def test_binding_rejects_tensors_and_streams_of_another_device(lib):
+    import torch
+    d0, d1 = torch.device("cuda", 0), torch.device("cuda", 1)
+    lib._req(_FakeCudaTensor(d0, (4, 8), torch.float32), torch.float32, (4, 8), "x", d0)
+    with pytest.raises(ValueError, match="x is on cuda:1, the handle on cuda:0"):
+        lib._req(_FakeCudaTensor(d1, (4, 8), torch.float32), torch.float32, (4, 8), "x", d0)
+    assert lib._stream(_FakeStream(d0), d0) == 0
+    with pytest.raises(ValueError, match="stream is on cuda:1"):
+        lib._stream(_FakeStream(d1), d0)
