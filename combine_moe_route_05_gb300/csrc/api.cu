@@ -143,9 +143,10 @@ moe_status moe_handle_create(const moe_config* c, void* d_workspace, size_t work
   if (workspace_bytes < p.total) return MOE_ERR_INVALID;
   if (moe::layout_smem_bytes(c->num_experts, c->num_ranks) > 227 * 1024) return MOE_ERR_INVALID;
 
-  int dev = 0, sms = 0;
+  int dev = 0, sms = 0, l2 = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
     return MOE_ERR_CUDA;
   // fails with "no kernel image" on a device the library was not built for
   if (moe::prepare_layout_kernels() != cudaSuccess) return MOE_ERR_CUDA;
@@ -160,6 +161,7 @@ moe_status moe_handle_create(const moe_config* c, void* d_workspace, size_t work
   h->cfg = *c;
   h->device = dev;
   h->num_sms = sms;
+  h->l2_bytes = l2;
   h->T = -1;
   h->max_tiles = p.max_tiles;
   h->pad = c->pad_align > 1 ? c->pad_align : 1;

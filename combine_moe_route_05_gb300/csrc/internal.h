@@ -11,6 +11,7 @@ struct moe_handle {
   moe_config cfg;
   int device;
   int num_sms;
+  long long l2_bytes;  // the device's L2 cache
   int T;  // tokens of the current layout, -1 before the first
   int max_tiles;
   int pad;  // receive segments rounded up to a multiple of pad rows (>= 1)
