@@ -70,3 +70,32 @@ def test_reference_arm_line():
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["e2e"]["value"] == line["value"] and line["e2e"]["unit"] == line["unit"]
     assert line["config"]["workload"].startswith("qwen3_30b")
+
+
+def test_traffic_records_are_consistent():
+    """The per-launch DRAM traffic the benchmark reports beside its roofline
+    (profiles/traffic.json) is one ncu pass per record: each names a workload,
+    the hash of the kernel sources it was taken on and the summary that cites
+    it; the figure lies at or a little below the kernel's algorithmic bytes
+    (the write-back L2 still holds the last writes when a launch ends) and
+    never well above them, which would mean re-reads."""
+    import re
+    with open(bench.TRAFFIC_RECORDS) as f:
+        recs = json.load(f)
+    by_name = {w.name: w for w in synth.WORKLOADS.values()}
+    algo = {}
+    wl = by_name[recs["combine_bwd"]["workload"]]
+    algo["combine_bwd"] = bench.step_bytes(wl)["combine_bwd"]
+    wl = by_name[recs["w2_absorbed"]["workload"]]
+    rows, H = wl.T * wl.K, 4096
+    algo["w2_absorbed"] = rows * wl.I * 2 + wl.E * H * wl.I * 2 + rows * H * 2 + rows * 4
+    for key, a in algo.items():
+        rec = recs[key]
+        traffic = rec["traffic_bytes_per_launch"]
+        assert 0.95 * a <= traffic <= 1.01 * a, (key, traffic, a)
+        assert re.fullmatch(r"[0-9a-f]{16}", rec["source"])
+        with open(os.path.join(ROOT, rec["summary"])) as f:
+            text = f.read()
+        cite = "(key `%s`): %.3fe9 bytes, workload %s, kernel source %s" % (
+            key, traffic / 1e9, rec["workload"], rec["source"])
+        assert cite in text, cite
