@@ -11,42 +11,49 @@
 // with W2 stored [E][H][I].  The scaling is the GEMM's prologue: the scaled
 // rows never reach HBM.  A pad row of a padded layout gets y = 0.
 //
-// Persistent clusters of two CTAs (a CTA pair) walk 256 x 256 output tiles:
+// Persistent clusters of two CTAs (a CTA pair) walk 256 x 384 output tiles:
 // each CTA owns 128 rows (adjacent 128-row m-tiles of one expert; each
 // expert's segment is cut into 128-row tiles, the last one ragged) and half
-// of the tile's 256 W2 columns in shared memory.  One MMA instruction of the
-// pair, issued by the even CTA, multiplies all 256 rows by all 256 columns;
-// each CTA keeps its 128 x 256 accumulator in its own tensor memory.  Per CTA
-// and 64-wide K slice, shared memory carries 16 KB of h and 16 KB of W2
-// landed by TMA, 16 KB of h read by the prologue and 16 KB of W2 read by the
-// tensor cores: two thirds of what one CTA computing 128 x 256 tiles on its
-// own moves for the same products.
+// of the tile's 384 W2 columns in shared memory.  Two MMA instructions of the
+// pair per K step, issued by the even CTA, multiply all 256 rows by the
+// tile's two 192-column halves; each CTA keeps its 128 x 384 accumulator in
+// its own tensor memory (384 of its 512 columns; the other 128 hold four
+// scaled-h stages).  Per CTA and 64-wide K slice, shared memory carries 16 KB
+// of h and 24 KB of W2 landed by TMA, 16 KB of h read by the prologue and
+// 24 KB of W2 read by the tensor cores, 80 KB for 768 cycles of MMAs (a
+// 256-column tile moved 64 KB for 512).  The h slice of a row block is
+// scaled once per 384 output columns.  Where H is not a multiple of 384 the
+// last tile of a row of tiles computes its full width and stores only the
+// columns inside H (narrower MMAs for it measured slower).
 //
 // Warp roles, in both CTAs:
 //   warp 2      TMA: h slices [128 x 64] into a 4-stage ring (128-byte
 //               swizzle), freed once the prologue has consumed them (after
 //               its tensor-memory store: the refill must not overtake the
 //               prologue's shared-memory loads);
-//   warp 0      TMA: this CTA's half [128 x 64] of each W2 slice into an
-//               8-stage ring.  The copies of BOTH CTAs complete on the even
-//               CTA's `full` barrier of the stage (the pair form of the bulk
-//               tensor copy lets the barrier sit in the peer CTA), and the
-//               even CTA's producer announces the bytes of both halves;
+//   warp 0      TMA: this CTA's part of each W2 slice, [96 x 64] for each
+//               of the two column halves, into a 4-stage ring.  The copies
+//               of BOTH CTAs complete on the even CTA's `full` barrier of the
+//               stage (the pair form of the bulk tensor copy lets the barrier
+//               sit in the peer CTA), and the even CTA's producer announces
+//               the bytes of both CTAs;
 //   warps 3-10  prologue: read an h slice (one row per thread, half of its K
 //               range per warp), scale it by the row's score (fp32 product,
 //               bf16 round-to-nearest-even), store it into the 32-column A
 //               stage in tensor memory that pairs with the W2 stage of the
 //               same index, and arrive on the even CTA's `full` barrier;
-//   warp 1      tensor memory (allocated by the pair together: one 256-column
-//               accumulator + eight A stages); in the even CTA one thread
-//               waits on `full` (both W2 halves and all sixteen A stores of
-//               the pair), issues the pair's MMAs (four K=16 steps per slice)
-//               and commits, once to each CTA's `empty` barrier of the stage
-//               and, per tile, to each CTA's `acc_full`;
-//   warps 11-18 epilogue: accumulator -> registers (two warps per lane
-//               quarter, half the columns each), accumulator handed back (an
-//               arrival on the even CTA's `acc_empty`), then bf16 rows to HBM
-//               while the next tile's MMAs run.
+//   warp 1      tensor memory (allocated by the pair together: a 384-column
+//               accumulator + four A stages); in the even CTA one thread
+//               waits on `full` (both CTAs' W2 parts and all sixteen A
+//               stores of the pair), issues the pair's MMAs (two halves of
+//               four K=16 steps per slice; a tile's first MMAs into a half
+//               wait until the epilogue has read that half) and commits, once
+//               to each CTA's `empty` barrier of the stage and, per tile, to
+//               each CTA's `acc_full`;
+//   warps 11-18 epilogue: per column half, accumulator -> registers (two
+//               warps per lane quarter, 96 columns each), the half handed
+//               back (an arrival on the even CTA's `acc_empty` of the half),
+//               then bf16 rows to HBM while the next tile's MMAs run.
 // Every wait is bounded; a wait that gives up raises MOE_DEVERR_TIMEOUT and
 // the CTA winds down (copies in flight are waited for, tensor memory freed).
 // No load is multicast: each CTA loads its own rows of h and its own half of
@@ -60,28 +67,34 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;          // rows per CTA: the accumulator's tensor-memory lanes
-constexpr int kBN = 256;          // output columns per tile (the pair's MMA N)
-constexpr int kBNHalf = kBN / 2;  // W2 rows held by one CTA
+constexpr int kMmaN = 192;            // columns of one MMA instruction of the pair
+constexpr int kHalves = 2;            // MMAs per K step: the tile's two column halves
+constexpr int kBN = kHalves * kMmaN;  // output columns per tile
+constexpr int kSubRows = kMmaN / 2;   // W2 rows one CTA holds for one MMA half
+constexpr int kBNHalf = kBN / 2;      // W2 rows held by one CTA
+constexpr int kHMultiple = 256;       // the entry point's contract: H a multiple of 256
 constexpr int kBK = 64;           // contraction per stage: one 128-byte swizzle row of bf16
 constexpr int kUmmaK = 16;        // contraction per MMA instruction (16-bit operands)
 constexpr int kStagesA = 4;       // h slices in shared memory
 // W2 half-slices in shared memory and scaled h slices in tensor memory share
 // one ring index: one barrier says "both operands of slice j are in place in
 // both CTAs", one commit per CTA frees both
-constexpr int kStages = 8;
+constexpr int kStages = 4;
 constexpr int kPrologueWarps = 8;  // two per lane quarter, half the K range each
 constexpr int kEpilogueWarps = 8;  // two per lane quarter, half the columns each
 constexpr int kFirstPrologueWarp = 3;
 constexpr int kFirstEpilogueWarp = kFirstPrologueWarp + kPrologueWarps;
 constexpr int kThreads = 32 * (kFirstEpilogueWarp + kEpilogueWarps);
 constexpr uint32_t kABytes = kBM * kBK * 2;
-constexpr uint32_t kBBytes = kBNHalf * kBK * 2;
+constexpr uint32_t kSubBytes = kSubRows * kBK * 2;  // one MMA half's W2 rows of a CTA
+constexpr uint32_t kBBytes = kHalves * kSubBytes;
+static_assert(kSubBytes % 1024 == 0, "W2 sub-tiles start on 1024-byte swizzle boundaries");
 constexpr uint32_t kAccCols = kBN;    // fp32 accumulator: a column per output column
 constexpr uint32_t kACols = kBK / 2;  // a scaled h slice: two bf16 per 32-bit column
 constexpr uint32_t kTmemCols = 512;   // accumulator + kStages A stages (power of 2)
 static_assert(kAccCols + kStages * kACols <= kTmemCols, "tensor memory budget");
 constexpr size_t kBarrierBytes = 512;
-static_assert(8 * (2 * kStagesA + 2 * kStages + 2) + 16 <= kBarrierBytes, "barrier area");
+static_assert(8 * (2 * kStagesA + 2 * kStages + 1 + kHalves) + 16 <= kBarrierBytes, "barrier area");
 // operand rings, barriers and the tables of at most MOE_MAX_EXPERTS experts
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStagesA * kABytes + kStages * kBBytes +
                               kBarrierBytes + sizeof(int32_t) * (3 * MOE_MAX_EXPERTS + 2);
@@ -90,9 +103,12 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A
 // and B bf16 (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
 // in bits 17-22, M >> 4 in bits 24-28; M = 256 rows over the CTA pair.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                            (static_cast<uint32_t>(kBN >> 3) << 17) |
-                            (static_cast<uint32_t>((2 * kBM) >> 4) << 24);
+constexpr uint32_t kIdescNoN = (1u << 4) | (1u << 7) | (1u << 10) |
+                               (static_cast<uint32_t>((2 * kBM) >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_for(int n) {
+  return kIdescNoN | (static_cast<uint32_t>(n >> 3) << 17);
+}
+
 
 struct W2Args {
   const float* recv_w;
@@ -103,7 +119,7 @@ struct W2Args {
   unsigned long long wait_ns;  // limit of every mbarrier wait
   int rows;                    // receive rows of h and y (T*K plus the pads)
   int E, I, H;
-  int n_tiles;  // H / kBN
+  int n_tiles;  // ceil(H / kBN): the last tile's columns past H are not stored
 };
 
 // Shared-memory matrix descriptor of a K-major operand tile in the 128-byte
@@ -224,12 +240,12 @@ __device__ __forceinline__ void tc_fence_after() {
 // peer's (same addresses); each CTA's tensor memory receives its 128 rows.
 // A in tensor memory: lane = row, 32-bit column j = bf16 elements 2j, 2j+1.
 __device__ __forceinline__ void umma_pair(uint32_t tmem_d, uint32_t tmem_a, uint64_t b_desc,
-                                          uint32_t accumulate) {
+                                          uint32_t accumulate, uint32_t idesc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %3, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %4, p;\n\t}" ::"r"(tmem_d),
-      "r"(tmem_a), "l"(b_desc), "r"(accumulate), "r"(kIdesc)
+      "r"(tmem_a), "l"(b_desc), "r"(accumulate), "r"(idesc)
       : "memory");
 }
 
@@ -330,15 +346,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // both CTAs, as the pair's MMA requires
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;                       // [kStagesA][kBM x kBK] bf16, swizzled
-  uint8_t* sB = smem + kStagesA * kABytes;  // [kStages][kBNHalf x kBK] bf16, swizzled
+  uint8_t* sB = smem + kStagesA * kABytes;  // [kStages][kHalves][kSubRows x kBK] bf16, swizzled
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
   uint64_t* full_a = bars;               // [kStagesA] h slice landed
   uint64_t* free_a = full_a + kStagesA;  // [kStagesA] h slice consumed by the prologue
   uint64_t* full = free_a + kStagesA;    // [kStages] even CTA: both W2 halves, all A stores
   uint64_t* empty = full + kStages;      // [kStages] the pair's MMAs done with the stage
   uint64_t* acc_full = empty + kStages;  // accumulator complete
-  uint64_t* acc_empty = acc_full + 1;    // even CTA: both CTAs' accumulators drained
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  uint64_t* acc_empty = acc_full + 1;    // [kHalves] even CTA: that column half drained in both CTAs
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + kHalves);
   Tables tb;
   tb.tile_first = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(bars) + kBarrierBytes);
   tb.off = tb.tile_first + (a.E + 1);
@@ -399,7 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&empty[s], 1);  // the pair's commit
       }
       mbar_init(acc_full, 1);                    // the pair's commit
-      mbar_init(acc_empty, 2 * kEpilogueWarps);  // epilogue warps of both CTAs
+      for (int j = 0; j < kHalves; ++j)
+        mbar_init(&acc_empty[j], 2 * kEpilogueWarps);  // epilogue warps of both CTAs
       fence_mbar_init();
     }
   } else if (warp == 1) {
@@ -440,9 +457,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * kBBytes);
-            tma_load_2d_pair(sB + s * kBBytes, &tm_w2, kb * kBK,
-                             t.expert * a.H + t.nt * kBN + rank * kBNHalf,
-                             cluster_addr(&full[s], 0));
+            // MMA half j takes W2 rows j kMmaN .. j kMmaN + kMmaN - 1 of the
+            // tile, the even CTA the first kSubRows of them.  In a ragged last
+            // tile the columns past H are not stored, so a box wholly past the
+            // expert's rows reads the expert's own last rows again (in L2)
+            // instead of the next expert's from HBM
+            const int row_end = (t.expert + 1) * a.H;
+#pragma unroll
+            for (int j = 0; j < kHalves; ++j) {
+              const int row = t.expert * a.H + t.nt * kBN + j * kMmaN + rank * kSubRows;
+              tma_load_2d_pair(sB + s * kBBytes + j * kSubBytes, &tm_w2, kb * kBK,
+                               row < row_end ? row : row_end - kSubRows,
+                               cluster_addr(&full[s], 0));
+            }
           } else {
             if (it >= stages && !wait_phase(&free_a[s], ph ^ 1u, a.wait_ns)) {
               ok = false;
@@ -469,11 +496,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0, n = 0;
       const uint32_t acc_full_peer = cluster_addr(acc_full, 1);
       for (int tile = pair; tile < total && ok; tile += npairs, ++n) {
-        if (n >= 1 && !wait_phase(acc_empty, (n - 1) & 1u, a.wait_ns)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kStages;
           if (!wait_phase(&full[s], (it / kStages) & 1u, a.wait_ns)) {
@@ -483,9 +505,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t b0 = smem_addr(sB + s * kBBytes);
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k)
-            umma_pair(tmem, tmem_a + s * kACols + k * (kUmmaK / 2),
-                      sw128_desc(b0 + k * kUmmaK * 2), (kb | k) != 0);
+          for (int j = 0; j < kHalves; ++j) {
+            // a tile's first MMAs into a column half wait until the epilogue
+            // of both CTAs has read the previous tile's values there
+            if (kb == 0 && n >= 1) {
+              if (!wait_phase(&acc_empty[j], (n - 1) & 1u, a.wait_ns)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k)
+              umma_pair(tmem + j * kMmaN, tmem_a + s * kACols + k * (kUmmaK / 2),
+                        sw128_desc(b0 + j * kSubBytes + k * kUmmaK * 2), (kb | k) != 0,
+                        idesc_for(kMmaN));
+          }
+          if (!ok) break;
           // frees the stage in both CTAs
           umma_commit_to(smem_addr(&empty[s]));
           umma_commit_to(cluster_addr(&empty[s], 1));
@@ -557,7 +593,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ch of the accumulator
     const int q = warp & 3;
     const int ch = (warp - kFirstEpilogueWarp) >> 2;
-    const uint32_t acc_empty_even = cluster_addr(acc_empty, 0);
     int n = 0;
     for (int tile = pair; tile < total && ok; tile += npairs, ++n) {
       const Tile ti = decode_tile(tb, a.E, a.n_tiles, tile, rank);
@@ -569,32 +604,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = ti.row0 + q * 32 + lane;
       const bool real = row < ti.real_end;
       const bool pad = !real && row < ti.seg_end;
-      __nv_bfloat16* dst = a.y + static_cast<size_t>(row) * a.H + ti.nt * kBN + ch * (kBN / 2);
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + ch * (kBN / 2);
-      // the row's 128 columns as bf16 pairs in registers, so the accumulator
-      // is handed back to the MMAs before the (slower) stores to HBM
-      uint32_t packed[kBN / 4];
+#pragma unroll 1
+      for (int j = 0; j < kHalves; ++j) {
+        // this warp's kMmaN / 2 columns of column half j, first output column c0
+        const int c0 = ti.nt * kBN + j * kMmaN + ch * (kMmaN / 2);
+        const uint32_t taddr =
+            tmem + (static_cast<uint32_t>(q * 32) << 16) + j * kMmaN + ch * (kMmaN / 2);
+        // the row's columns as bf16 pairs in registers, so the half is handed
+        // back to the MMAs before the (slower) stores to HBM
+        uint32_t packed[kMmaN / 4];
 #pragma unroll
-      for (int c = 0; c < kBN / 2 / 16; ++c) {
-        uint32_t v[16];
-        tmem_ld16(taddr + c * 16, v);
+        for (int c = 0; c < kMmaN / 2 / 16; ++c) {
+          uint32_t v[16];
+          tmem_ld16(taddr + c * 16, v);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          packed[c * 8 + j] =
-              real ? pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1])) : 0u;
-      }
-      tc_fence_before();  // the loads above precede the MMAs that reuse the columns
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty_even);
-      if (real || pad) {
+          for (int u = 0; u < 8; ++u)
+            packed[c * 8 + u] =
+                real ? pack_bf16x2(__uint_as_float(v[2 * u]), __uint_as_float(v[2 * u + 1])) : 0u;
+        }
+        tc_fence_before();  // the loads above precede the MMAs that reuse the columns
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(cluster_addr(&acc_empty[j], 0));
+        if (real || pad) {
+          __nv_bfloat16* dst = a.y + static_cast<size_t>(row) * a.H + c0;
 #pragma unroll
-        for (int j = 0; j < kBN / 2 / 8; ++j) {
-          Vec16 o;
-          o.u[0] = packed[4 * j];
-          o.u[1] = packed[4 * j + 1];
-          o.u[2] = packed[4 * j + 2];
-          o.u[3] = packed[4 * j + 3];
-          st_vec(dst + j * 8, o);
+          for (int u = 0; u < kMmaN / 2 / 8; ++u) {
+            if (c0 + u * 8 >= a.H) break;  // the last tile's columns past H
+            Vec16 o;
+            o.u[0] = packed[4 * u];
+            o.u[1] = packed[4 * u + 1];
+            o.u[2] = packed[4 * u + 2];
+            o.u[3] = packed[4 * u + 3];
+            st_vec(dst + u * 8, o);
+          }
         }
       }
     }
@@ -658,7 +700,9 @@ cudaError_t prepare_w2_kernel() {
                               static_cast<int>(kSmemBytes));
 }
 
-bool w2_shape_ok(int I, int H) { return I >= 8 && I % 8 == 0 && H >= kBN && H % kBN == 0; }
+bool w2_shape_ok(int I, int H) {
+  return I >= 8 && I % 8 == 0 && H >= kHMultiple && H % kHMultiple == 0;
+}
 
 cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, const float* recv_w,
                                const void* w2, int H, void* y, cudaStream_t s) {
@@ -670,7 +714,7 @@ cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, co
   if (static_cast<long long>(E) * H > 0x7fffffffLL) return cudaErrorInvalidValue;
   CUtensorMap tm_h, tm_w2;
   if (!encode_rows(&tm_h, hrows, static_cast<uint64_t>(rows_cap), I, kBM) ||
-      !encode_rows(&tm_w2, w2, static_cast<uint64_t>(E) * H, I, kBNHalf))
+      !encode_rows(&tm_w2, w2, static_cast<uint64_t>(E) * H, I, kSubRows))
     return cudaErrorInvalidValue;
   W2Args a;
   a.recv_w = recv_w;
@@ -683,7 +727,7 @@ cudaError_t launch_w2_absorbed(const moe_handle* h, const void* hrows, int I, co
   a.E = E;
   a.I = I;
   a.H = H;
-  a.n_tiles = H / kBN;
+  a.n_tiles = (H + kBN - 1) / kBN;
   // sum over experts of ceil(ceil(segment / kBM) / 2) <= pair tiles below
   const long long m_tiles = (rows_cap + static_cast<long long>(E) * (kBM - 1)) / kBM;
   const long long pair_tiles = ((m_tiles + E) / 2) * a.n_tiles;

@@ -151,7 +151,7 @@ def test_w2_absorbed_full_size_sampled_rows():
 
 @pytest.mark.parametrize("E,K,R,T,I,H", [(512, 8, 64, 300, 8, 256),   # E at its maximum, I at its minimum
                                          (8, 2, 2, 1, 64, 256),        # one token
-                                         (16, 4, 4, 257, 72, 768)])    # ragged I past one slice, 3 n-tiles
+                                         (16, 4, 4, 257, 72, 768)])    # ragged I past one slice, two n-tiles
 def test_w2_absorbed_shapes(E, K, R, T, I, H):
     wl = dataclasses.replace(synth.WORKLOADS[1], E=E, K=K, R=R).with_tokens(T)
     wl, r, L, recv_w, h, w2 = problem(wl, I=I, H=H)
