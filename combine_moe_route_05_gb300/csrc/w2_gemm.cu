@@ -37,20 +37,21 @@
 //               stage (the pair form of the bulk tensor copy lets the barrier
 //               sit in the peer CTA), and the even CTA's producer announces
 //               the bytes of both CTAs;
-//   warps 3-10  prologue: read an h slice (one row per thread, half of its K
-//               range per warp), scale it by the row's score (fp32 product,
-//               bf16 round-to-nearest-even), store it into the 32-column A
-//               stage in tensor memory that pairs with the W2 stage of the
-//               same index, and arrive on the even CTA's `full` barrier;
+//   warps 3-6   prologue: read an h slice (one row per thread, one warp per
+//               tensor-memory lane quarter), scale it by the row's score
+//               (fp32 product, bf16 round-to-nearest-even), store it into the
+//               32-column A stage in tensor memory that pairs with the W2
+//               stage of the same index, and arrive on the even CTA's `full`
+//               barrier;
 //   warp 1      tensor memory (allocated by the pair together: a 384-column
 //               accumulator + four A stages); in the even CTA one thread
-//               waits on `full` (both CTAs' W2 parts and all sixteen A
+//               waits on `full` (both CTAs' W2 parts and all eight A
 //               stores of the pair), issues the pair's MMAs (two halves of
 //               four K=16 steps per slice; a tile's first MMAs into a half
 //               wait until the epilogue has read that half) and commits, once
 //               to each CTA's `empty` barrier of the stage and, per tile, to
 //               each CTA's `acc_full`;
-//   warps 11-18 epilogue: per column half, accumulator -> registers (two
+//   warps 7-14  epilogue: per column half, accumulator -> registers (two
 //               warps per lane quarter, 96 columns each), the half handed
 //               back (an arrival on the even CTA's `acc_empty` of the half),
 //               then bf16 rows to HBM while the next tile's MMAs run.
@@ -80,7 +81,7 @@ constexpr int kStagesA = 4;       // h slices in shared memory
 // one ring index: one barrier says "both operands of slice j are in place in
 // both CTAs", one commit per CTA frees both
 constexpr int kStages = 4;
-constexpr int kPrologueWarps = 8;  // two per lane quarter, half the K range each
+constexpr int kPrologueWarps = 4;  // one per lane quarter, the whole K range of a slice
 constexpr int kEpilogueWarps = 8;  // two per lane quarter, half the columns each
 constexpr int kFirstPrologueWarp = 3;
 constexpr int kFirstEpilogueWarp = kFirstPrologueWarp + kPrologueWarps;
@@ -533,9 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kFirstEpilogueWarp) {
     // prologue: lane quarter q = warp % 4 (tensor memory is reachable by the
-    // warps of that quarter only), K half kh; thread = row 32 q + lane
+    // warps of that quarter only); thread = row 32 q + lane, the slice's two
+    // K halves in turn
     const int q = warp & 3;
-    const int kh = (warp - kFirstPrologueWarp) >> 2;
     const int prow = q * 32 + lane;
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
     auto score_of = [&](int tile) {
@@ -560,24 +561,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        // 16-byte chunk c of row r sits at r * 128 + ((c ^ (r % 8)) * 16); this
-        // warp's K half is chunks 4 kh .. 4 kh + 3 (eight rows of a phase hit
-        // eight distinct banks)
+        // 16-byte chunk c of row r sits at r * 128 + ((c ^ (r % 8)) * 16); K
+        // half kh is chunks 4 kh .. 4 kh + 3 (eight rows of a phase hit eight
+        // distinct banks)
         const uint8_t* line = sA + sa * kABytes + prow * 128;
-        uint32_t packed[16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int chunk = kh * 4 + c;
-          const uint4 v = *reinterpret_cast<const uint4*>(line + ((chunk ^ (prow & 7)) << 4));
-          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+        for (int kh = 0; kh < 2; ++kh) {
+          uint32_t packed[16];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float lo = __fmul_rn(__uint_as_float(u[j] << 16), score);
-            const float hi = __fmul_rn(__uint_as_float(u[j] & 0xffff0000u), score);
-            packed[c * 4 + j] = pack_bf16x2(lo, hi);
+          for (int c = 0; c < 4; ++c) {
+            const int chunk = kh * 4 + c;
+            const uint4 v = *reinterpret_cast<const uint4*>(line + ((chunk ^ (prow & 7)) << 4));
+            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float lo = __fmul_rn(__uint_as_float(u[j] << 16), score);
+              const float hi = __fmul_rn(__uint_as_float(u[j] & 0xffff0000u), score);
+              packed[c * 4 + j] = pack_bf16x2(lo, hi);
+            }
           }
+          tmem_st16(tmem_a + lane_bits + s * kACols + kh * 16, packed);
         }
-        tmem_st16(tmem_a + lane_bits + s * kACols + kh * 16, packed);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
