@@ -41,12 +41,14 @@
 //               tensor-memory lane quarter), scale it by the row's score
 //               (fp32 product, bf16 round-to-nearest-even), store it into the
 //               32-column A stage in tensor memory that pairs with the W2
-//               stage of the same index, and arrive on the even CTA's `full`
-//               barrier;
+//               stage of the same index; the four warps meet at a named
+//               barrier, and one thread arrives on the even CTA's `full`
+//               barrier for the CTA (two remote arrivals per slice, not one
+//               per warp);
 //   warp 1      tensor memory (allocated by the pair together: a 384-column
 //               accumulator + four A stages); in the even CTA one thread
-//               waits on `full` (both CTAs' W2 parts and all eight A
-//               stores of the pair), issues the pair's MMAs (two halves of
+//               waits on `full` (both CTAs' W2 parts and both CTAs' A
+//               stages), issues the pair's MMAs (two halves of
 //               four K=16 steps per slice; a tile's first MMAs into a half
 //               wait until the epilogue has read that half) and commits, once
 //               to each CTA's `empty` barrier of the stage and, per tile, to
@@ -228,6 +230,21 @@ __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// AND of `p` over the nthreads threads (whole warps) that meet at named
+// barrier `id`; every one of them must reach it.
+__device__ __forceinline__ bool bar_and(bool p, int id, int nthreads) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -407,12 +424,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tb.tile_first[a.E] = running;
       for (int s = 0; s < kStagesA; ++s) {
         mbar_init(&full_a[s], 1);
-        mbar_init(&free_a[s], kPrologueWarps);
+        mbar_init(&free_a[s], 1);  // one arrival for the CTA's prologue warps
       }
       for (int s = 0; s < kStages; ++s) {
         // even CTA: its W2 producer's arrival (with both halves' bytes) and
         // the prologue warps of both CTAs; the odd CTA's is unused
-        mbar_init(&full[s], 1 + 2 * kPrologueWarps);
+        mbar_init(&full[s], 1 + 2);  // the W2 producer's arrival, one per CTA's prologue
         mbar_init(&empty[s], 1);  // the pair's commit
       }
       mbar_init(acc_full, 1);                    // the pair's commit
@@ -556,37 +573,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool got = wait_phase(&full_a[sa], (it / kStagesA) & 1u, a.wait_ns);
         if (got && it >= kStages)
           got = wait_phase(&empty[s], ((it / kStages) & 1u) ^ 1u, a.wait_ns);
-        if (!__all_sync(0xffffffffu, got)) {
+        got = __all_sync(0xffffffffu, got);
+        if (got) {
+          tc_fence_after();
+          // 16-byte chunk c of row r sits at r * 128 + ((c ^ (r % 8)) * 16); K
+          // half kh is chunks 4 kh .. 4 kh + 3 (eight rows of a phase hit eight
+          // distinct banks)
+          const uint8_t* line = sA + sa * kABytes + prow * 128;
+#pragma unroll
+          for (int kh = 0; kh < 2; ++kh) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int chunk = kh * 4 + c;
+              const uint4 v =
+                  *reinterpret_cast<const uint4*>(line + ((chunk ^ (prow & 7)) << 4));
+              const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float lo = __fmul_rn(__uint_as_float(u[j] << 16), score);
+                const float hi = __fmul_rn(__uint_as_float(u[j] & 0xffff0000u), score);
+                packed[c * 4 + j] = pack_bf16x2(lo, hi);
+              }
+            }
+            tmem_st16(tmem_a + lane_bits + s * kACols + kh * 16, packed);
+          }
+          tc_fence_before();
+        }
+        // the CTA's prologue warps meet once per slice (every one of them,
+        // also after a wait that gave up: then all leave together); one
+        // thread then frees the h slot (the loads it held are consumed) and
+        // tells the even CTA's MMA that this CTA's A stage is in place
+        if (!bar_and(got, 1, 32 * kPrologueWarps)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        // 16-byte chunk c of row r sits at r * 128 + ((c ^ (r % 8)) * 16); K
-        // half kh is chunks 4 kh .. 4 kh + 3 (eight rows of a phase hit eight
-        // distinct banks)
-        const uint8_t* line = sA + sa * kABytes + prow * 128;
-#pragma unroll
-        for (int kh = 0; kh < 2; ++kh) {
-          uint32_t packed[16];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int chunk = kh * 4 + c;
-            const uint4 v = *reinterpret_cast<const uint4*>(line + ((chunk ^ (prow & 7)) << 4));
-            const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float lo = __fmul_rn(__uint_as_float(u[j] << 16), score);
-              const float hi = __fmul_rn(__uint_as_float(u[j] & 0xffff0000u), score);
-              packed[c * 4 + j] = pack_bf16x2(lo, hi);
-            }
-          }
-          tmem_st16(tmem_a + lane_bits + s * kACols + kh * 16, packed);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          // the h slice may be refilled only after the store above consumed
-          // the loaded values; the even CTA's MMA needs this A stage
+        if (warp == kFirstPrologueWarp && lane == 0) {
           mbar_arrive(&free_a[sa]);
           mbar_arrive_cluster(cluster_addr(&full[s], 0));
         }
