@@ -102,6 +102,7 @@ static_assert(8 * (2 * kStagesA + 2 * kStages + 1 + kHalves) + 16 <= kBarrierByt
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kStagesA * kABytes + kStages * kBBytes +
                               kBarrierBytes + sizeof(int32_t) * (3 * MOE_MAX_EXPERTS + 2);
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kSmemBytes < (1u << 18), "descriptor start addresses fit 14 bits of 16 bytes");
 
 // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1), A
 // and B bf16 (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3
@@ -513,6 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && rank == 0) {
       int it = 0, n = 0;
       const uint32_t acc_full_peer = cluster_addr(acc_full, 1);
+      // the stages' `empty` barriers are 8 bytes apart in both CTAs
+      const uint32_t empty_own = smem_addr(empty), empty_peer = cluster_addr(empty, 1);
       for (int tile = pair; tile < total && ok; tile += npairs, ++n) {
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           const int s = it % kStages;
@@ -521,7 +524,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t b0 = smem_addr(sB + s * kBBytes);
+          // the descriptor's start-address field is the address >> 4 (14 bits:
+          // shared memory ends below 256 KB), so the other MMAs of the slice
+          // add their byte offset >> 4 to the stage's descriptor
+          const uint64_t d0 = sw128_desc(smem_addr(sB + s * kBBytes));
 #pragma unroll
           for (int j = 0; j < kHalves; ++j) {
             // a tile's first MMAs into a column half wait until the epilogue
@@ -536,13 +542,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k)
               umma_pair(tmem + j * kMmaN, tmem_a + s * kACols + k * (kUmmaK / 2),
-                        sw128_desc(b0 + j * kSubBytes + k * kUmmaK * 2), (kb | k) != 0,
+                        d0 + ((j * kSubBytes + k * kUmmaK * 2) >> 4), (kb | k) != 0,
                         idesc_for(kMmaN));
           }
           if (!ok) break;
           // frees the stage in both CTAs
-          umma_commit_to(smem_addr(&empty[s]));
-          umma_commit_to(cluster_addr(&empty[s], 1));
+          umma_commit_to(empty_own + 8 * s);
+          umma_commit_to(empty_peer + 8 * s);
         }
         if (!ok) break;
         umma_commit_to(smem_addr(acc_full));
